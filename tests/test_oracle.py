@@ -1,0 +1,355 @@
+"""Pins for the CPU oracle: it is checked against mathematics and printed
+values, never against itself. All CPU-only."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs as gen
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bf16(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * scale).to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------- attention
+
+@pytest.mark.parametrize("B,N,H,Hkv,d,causal", [
+    (2, 37, 4, 2, 64, False), (2, 37, 4, 2, 64, True),
+    (1, 130, 2, 1, 128, False), (1, 130, 2, 1, 128, True),
+    (1, 20, 2, 2, 256, True), (1, 1, 1, 1, 64, False), (3, 5, 8, 1, 64, True),
+])
+def test_bruteforce_agreement(B, N, H, Hkv, d, causal):
+    q, k, v = gen.qkv_fixed(B, N, H, Hkv, d, seed=3)
+    o, lse = O.attention(q, k, v, causal=causal)
+    ob, lb = O.attention_bruteforce(q, k, v, causal=causal)
+    assert np.abs(o - ob).max() <= 1e-12
+    assert np.abs(lse - lb).max() <= 1e-12
+
+
+def test_varlen_matches_per_sequence_bruteforce():
+    lengths = [5, 1, 33, 130]
+    H, Hkv, d = 4, 2, 64
+    q, k, v, cu = gen.qkv_varlen(lengths, H, Hkv, d, seed=5)
+    for causal in (False, True):
+        o, lse = O.attention(q, k, v, causal=causal, cu_seqlens=cu)
+        for s, n in enumerate(lengths):
+            a, b = cu[s], cu[s + 1]
+            ob, lb = O.attention_bruteforce(q[a:b][None], k[a:b][None], v[a:b][None], causal=causal)
+            assert np.abs(o[a:b] - ob[0]).max() <= 1e-12
+            assert np.abs(lse[:, a:b] - lb[0]).max() <= 1e-12
+
+
+def test_rows_mode_matches_full():
+    q, k, v = gen.qkv_fixed(2, 64, 4, 2, 64, seed=9)
+    o, lse = O.attention(q, k, v, causal=True)
+    rs = np.array([0, 1, 1, 0]); rh = np.array([3, 0, 2, 1]); ri = np.array([0, 63, 17, 5])
+    o2, l2 = O.attention(q, k, v, causal=True, rows=(rs, rh, ri))
+    for r in range(4):
+        assert np.array_equal(o2[r], o[rs[r], ri[r], rh[r]])
+        assert l2[r] == lse[rs[r], rh[r], ri[r]]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_weights_sum_to_one(causal):
+    # V = identity rows turns the output row into the softmax weight row.
+    N, d = 48, 64
+    q = _bf16((1, N, 1, d), 1)
+    k = _bf16((1, N, 1, d), 2)
+    v = torch.zeros(1, N, 1, d)
+    v[0, torch.arange(N), 0, torch.arange(N)] = 1.0
+    o, _ = O.attention(q, k, v, causal=causal)
+    w = o[0, :, 0, :N]
+    assert np.all(w >= 0)
+    assert np.abs(w.sum(axis=1) - 1.0).max() <= 1e-14
+    if causal:
+        assert np.all(np.triu(w, 1) == 0.0)
+    assert np.all(o[0, :, 0, N:] == 0.0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_uniform_scores_give_mean_of_v(causal):
+    N, d = 40, 128
+    q = torch.zeros(1, N, 2, d)
+    k = _bf16((1, N, 1, d), 4)
+    v = _bf16((1, N, 1, d), 5)
+    o, lse = O.attention(q, k, v, causal=causal)
+    vf = v.float().numpy().astype(np.float64)[0, :, 0]
+    for i in range(N):
+        cnt = i + 1 if causal else N
+        ref = vf[:cnt].mean(axis=0)
+        for h in range(2):
+            assert np.abs(o[0, i, h] - ref).max() <= 1e-14
+            assert abs(lse[0, h, i] - math.log(cnt)) <= 1e-14
+
+
+def test_single_key():
+    d = 64
+    q = _bf16((1, 1, 3, d), 6); k = _bf16((1, 1, 1, d), 7); v = _bf16((1, 1, 1, d), 8)
+    o, lse = O.attention(q, k, v)
+    vf = v.float().numpy().astype(np.float64)[0, 0, 0]
+    for h in range(3):
+        assert np.array_equal(o[0, 0, h], vf)
+        dot = float(np.dot(q.float().numpy()[0, 0, h].astype(np.float64), k.float().numpy()[0, 0, 0]))
+        assert abs(lse[0, h, 0] - dot / math.sqrt(d)) <= 1e-13
+
+
+def test_first_causal_row_is_v0():
+    q, k, v = gen.qkv_fixed(2, 33, 4, 2, 64, seed=11)
+    o, lse = O.attention(q, k, v, causal=True)
+    vf = v.float().numpy().astype(np.float64)
+    qf = q.float().numpy().astype(np.float64); kf = k.float().numpy().astype(np.float64)
+    for b in range(2):
+        for h in range(4):
+            assert np.array_equal(o[b, 0, h], vf[b, 0, h // 2])
+            assert abs(lse[b, h, 0] - np.dot(qf[b, 0, h], kf[b, 0, h // 2]) / 8.0) <= 1e-13
+
+
+def test_joint_key_value_permutation_invariance():
+    q, k, v = gen.qkv_fixed(1, 50, 2, 1, 64, seed=12)
+    perm = torch.randperm(50, generator=torch.Generator().manual_seed(1))
+    o1, l1 = O.attention(q, k, v)
+    o2, l2 = O.attention(q, k[:, perm], v[:, perm])
+    assert np.abs(o1 - o2).max() <= 1e-13
+    assert np.abs(l1 - l2).max() <= 1e-13
+
+
+def test_gqa_head_mapping():
+    # query head h must use kv head h // (H/Hkv): swapping kv heads must
+    # permute the output heads in blocks.
+    q, k, v = gen.qkv_fixed(1, 16, 4, 2, 64, seed=13)
+    o1, _ = O.attention(q, k, v)
+    o2, _ = O.attention(q[:, :, [2, 3, 0, 1]], k[:, :, [1, 0]], v[:, :, [1, 0]])
+    assert np.abs(o1[:, :, [2, 3, 0, 1]] - o2).max() <= 1e-14
+
+
+def test_key_shift_moves_lse_only():
+    # s_j -> s_j + scale*q.u for every j: O unchanged, lse shifted by scale*q.u.
+    N, d = 24, 64
+    q = _bf16((1, N, 1, d), 14)
+    k = _bf16((1, N, 1, d), 15)
+    v = _bf16((1, N, 1, d), 16)
+    u = torch.full((d,), 0.25)
+    k2 = (k.float() + u)  # exact in fp32: |k| < 8 and u = 2^-2
+    o1, l1 = O.attention(q, k, v)
+    o2, l2 = O.attention(q, k2, v)
+    shift = q.float().numpy()[0, :, 0].astype(np.float64) @ u.numpy().astype(np.float64) / 8.0
+    assert np.abs(o1 - o2).max() <= 1e-12
+    assert np.abs((l2 - l1)[0, 0] - shift).max() <= 1e-12
+
+
+def test_scale_argument():
+    q, k, v = gen.qkv_fixed(1, 20, 1, 1, 64, seed=17)
+    o1, l1 = O.attention(q, k, v, scale=0.5)
+    o2, l2 = O.attention((q.float() * 0.5), k, v, scale=1.0)
+    assert np.abs(o1 - o2).max() <= 1e-13 and np.abs(l1 - l2).max() <= 1e-13
+
+
+def test_flops_formula():
+    assert O.attention_flops(1, 1, 128, 64, False) == 4 * 128 * 128 * 64
+    assert O.attention_flops(2, 16, 4096, 128, True) == 2 * 2 * 16 * 4096 ** 2 * 128
+
+
+# ---------------------------------------------------------------- Hadamard
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_sylvester_is_hadamard(d):
+    Hm = O.sylvester(d)
+    assert set(np.unique(Hm)) == {-1, 1}
+    assert np.array_equal(Hm @ Hm.T, d * np.eye(d, dtype=np.int64))
+    assert np.array_equal(Hm, Hm.T)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_fwht_equals_matrix_product(d):
+    rng = np.random.default_rng(d)
+    x = rng.integers(-50, 50, size=(5, d)).astype(np.float32)   # exact in fp32
+    assert np.array_equal(O.fwht_f32(x), (x.astype(np.int64) @ O.sylvester(d)).astype(np.float32))
+    y = rng.standard_normal((3, d)).astype(np.float32)
+    assert np.abs(O.fwht_f32(y) - y.astype(np.float64) @ O.sylvester(d)).max() <= 1e-4
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_rotation_preserves_qkT(d):
+    signs = O.hadamard_signs(0, d).astype(np.float64)
+    M = np.diag(signs) @ O.sylvester(d) / math.sqrt(d)
+    assert np.abs(M @ M.T - np.eye(d)).max() <= 1e-13
+    rng = np.random.default_rng(1)
+    Q = rng.standard_normal((64, d)); K = rng.standard_normal((64, d))
+    assert np.abs((Q @ M) @ (K @ M).T - Q @ K.T).max() <= 1e-12
+    # the fp32 statement agrees with the fp64 product up to fp32 rounding
+    xq = Q.astype(np.float32)
+    assert np.abs(O.rotate_f32(xq, signs.astype(np.float32)) - xq.astype(np.float64) @ M).max() <= 2e-5
+
+
+def test_splitmix64_reference_outputs():
+    gamma = 0x9E3779B97F4A7C15
+    for line in open(os.path.join(GOLDEN, "splitmix64.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        k, out = line.split()
+        assert O.splitmix64((int(k) * gamma) % 2 ** 64) == int(out, 16)
+
+
+def test_hadamard_signs_are_balanced_and_seeded():
+    s0 = O.hadamard_signs(0, 256)
+    assert set(np.unique(s0)) == {-1.0, 1.0}
+    assert 80 < (s0 > 0).sum() < 176
+    assert not np.array_equal(s0, O.hadamard_signs(1, 256))
+    # sign c depends on seed + c only (counter based)
+    assert np.array_equal(O.hadamard_signs(5, 64)[1:], O.hadamard_signs(6, 63))
+
+
+# ---------------------------------------------------------------- e4m3
+
+def test_e4m3_table1_values():
+    tab = O.e4m3_table()
+    for line in open(os.path.join(GOLDEN, "e4m3_table1.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        code, val = line.split()
+        got = tab[int(code, 16)]
+        if val == "nan":
+            assert np.isnan(got)
+        else:
+            assert got == float(val) and np.signbit(got) == val.startswith("-")
+
+
+def test_e4m3_table_structure():
+    tab = O.e4m3_table()
+    pos = tab[:0x7F]
+    assert np.all(np.diff(pos) > 0)                      # monotone, no duplicates
+    assert np.array_equal(tab[0x80:0xFF], -pos)          # sign symmetric
+    assert np.isnan(tab).sum() == 2
+    # every normal binade holds 8 values spaced 2^(e-7)/8
+    for e in range(1, 16):
+        vals = pos[e * 8:e * 8 + 8] if e < 15 else pos[120:127]
+        assert np.allclose(np.diff(vals), 2.0 ** (e - 7) / 8)
+
+
+def test_e4m3_encode_roundtrip_and_ties():
+    tab = O.e4m3_table()
+    codes = np.array([c for c in range(256) if not np.isnan(tab[c])])
+    assert np.array_equal(O.e4m3_encode(tab[codes].astype(np.float32)), codes.astype(np.uint8))
+    pos = tab[:0x7F]
+    mids = (pos[:-1] + pos[1:]) / 2                     # exact in fp32
+    enc = O.e4m3_encode(mids.astype(np.float32)).astype(int)
+    lo, hi = np.arange(0, 0x7E), np.arange(1, 0x7F)
+    assert np.array_equal(enc, np.where(lo % 2 == 0, lo, hi))       # ties to even code
+    up = np.nextafter(mids.astype(np.float32), np.float32(np.inf))
+    dn = np.nextafter(mids.astype(np.float32), np.float32(-np.inf))
+    assert np.array_equal(O.e4m3_encode(up).astype(int), hi)
+    assert np.array_equal(O.e4m3_encode(dn).astype(int), lo)
+
+
+def test_e4m3_encode_saturates_and_nan():
+    x = np.array([448.0, 449.0, 464.0, 1e30, np.inf, -np.inf, -1e9, np.nan], dtype=np.float32)
+    assert O.e4m3_encode(x).tolist() == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE, 0x7F]
+
+
+def test_e4m3_encode_brute_force_nearest():
+    rng = np.random.default_rng(0)
+    x = (rng.standard_normal(20000) * np.exp2(rng.integers(-12, 9, 20000))).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    enc = O.e4m3_encode(x)
+    dec = O.e4m3_table()[enc]
+    fin = O.e4m3_table()[np.array([c for c in range(256) if not np.isnan(O.e4m3_table()[c])])]
+    best = np.abs(x[:, None].astype(np.float64) - fin[None, :]).min(axis=1)
+    assert np.array_equal(np.abs(x - dec), best)
+
+
+# ---------------------------------------------------------------- FP8 pre-pass
+
+def _outlier_qkv(B=2, N=256, H=2, Hkv=1, d=64, seed=0):
+    return gen.qkv_fixed(B, N, H, Hkv, d, seed=seed, dist="outlier")
+
+
+@pytest.mark.parametrize("rotate", [False, True])
+def test_prepass_block_scales(rotate):
+    q, k, v = _outlier_qkv(N=300)
+    pre = O.fp8_prepass(q, k, v, mode="block", rotate=rotate, seed=3)
+    B, N, H, d = q.shape
+    qsrc = q.float().numpy()
+    if rotate:
+        qsrc = O.rotate_f32(qsrc, O.hadamard_signs(3, d))
+    assert pre["sq"].shape == (B, H, 3)
+    for b in range(B):
+        for h in range(H):
+            for ib in range(3):
+                blk = qsrc[b, ib * 128:(ib + 1) * 128, h]
+                amax = np.abs(blk).max()
+                assert pre["sq"][b, h, ib] == np.float32(amax / np.float32(448))
+                codes = pre["q8"][b, ib * 128:(ib + 1) * 128, h]
+                assert (codes & 0x7F).max() == 0x7E           # block max hits 448
+                deq = O.e4m3_table()[codes] * pre["sq"][b, h, ib]
+                err = np.abs(deq - blk)
+                # half an e4m3 ulp: 2^-4 relative in the normal range, 2^-10 * s below it
+                assert np.all(err <= np.maximum(np.abs(blk) * 2.0 ** -4, 2.0 ** -10 * pre["sq"][b, h, ib]) * 1.0001)
+    # V: per (b, kv head, channel) over all rows, never rotated
+    vf = v.float().numpy()
+    amax_v = np.abs(vf).max(axis=1)
+    assert np.array_equal(pre["sv"], (amax_v / np.float32(448)).astype(np.float32))
+    assert pre["vt8"].shape == (B, 1, d, N)
+    assert np.array_equal(pre["vt8"].transpose(0, 3, 1, 2), O.e4m3_encode(vf / pre["sv"][:, None]))
+
+
+def test_prepass_zero_block_scale_is_one():
+    q = torch.zeros(1, 128, 1, 64, dtype=torch.bfloat16)
+    pre = O.fp8_prepass(q, q, q, mode="block", rotate=True)
+    assert pre["sq"].ravel().tolist() == [1.0] and np.all((pre["q8"] & 0x7F) == 0)  # +-0
+    assert np.all(pre["sv"] == 1.0)
+
+
+def test_prepass_tensor_mode():
+    q, k, v = _outlier_qkv()
+    pre = O.fp8_prepass(q, k, v, mode="tensor", rotate=False)
+    assert pre["sq"].shape == (1,)
+    assert pre["sq"][0] == np.float32(np.abs(q.float().numpy()).max() / np.float32(448))
+    assert np.array_equal(pre["q8"], O.e4m3_encode(q.float().numpy() / pre["sq"][0]))
+
+
+def test_rotation_spreads_outliers():
+    # incoherent processing: after rotation the block amax relative to the
+    # RMS is far smaller on outlier inputs (the point of the technique).
+    q, _, _ = _outlier_qkv(B=1, N=1024, H=4, d=128, seed=2)
+    x = q.float().numpy()
+    r = O.rotate_f32(x, O.hadamard_signs(0, 128))
+    ratio = lambda a: np.abs(a).max() / np.sqrt((a ** 2).mean())
+    assert ratio(r) < 0.5 * ratio(x)
+
+
+# ---------------------------------------------------------------- FP8 attention emulation
+
+def test_fp8_emulation_unquantised_p_is_exact_attention():
+    q, k, v = _outlier_qkv(B=1, N=200, H=2, Hkv=1, d=64, seed=4)
+    pre = O.fp8_prepass(q, k, v, mode="block", rotate=True, seed=1)
+    dq = O.e4m3_table()[pre["q8"]] * np.repeat(pre["sq"], 128, axis=2)[:, :, :200].transpose(0, 2, 1)[..., None]
+    dk = O.e4m3_table()[pre["k8"]] * np.repeat(pre["sk"], 128, axis=2)[:, :, :200].transpose(0, 2, 1)[..., None]
+    dv = O.e4m3_table()[pre["vt8"]].transpose(0, 3, 1, 2) * pre["sv"][:, None]
+    for causal in (False, True):
+        ref_o, ref_l = O.attention_bruteforce(dq.astype(np.float32), dk.astype(np.float32),
+                                              dv.astype(np.float32), causal=causal)
+        # the dequantised values are exact in fp32 only up to the scale
+        # product's rounding; compare against the fp64 brute force loosely
+        # enough for that and tightly enough to catch a rescaling mistake.
+        for bn in (64, 200):
+            o, l = O.fp8_attention_emulated(pre, causal=causal, block_n=bn, quantize_p=False)
+            o = o.reshape(1, 2, 200, 64).transpose(0, 2, 1, 3)
+            assert np.abs(o - ref_o).max() <= 1e-5
+            assert np.abs(l.reshape(1, 2, 200) - ref_l).max() <= 1e-5
+
+
+def test_fp8_emulation_uniform_scores():
+    q = torch.zeros(1, 128, 1, 64, dtype=torch.bfloat16)
+    _, k, v = _outlier_qkv(B=1, N=128, H=1, Hkv=1, d=64, seed=6)
+    pre = O.fp8_prepass(q, k, v, mode="block", rotate=True)
+    o, l = O.fp8_attention_emulated(pre, block_n=64)
+    dv = O.e4m3_table()[pre["vt8"][0, 0]].T * pre["sv"][0, 0]
+    assert np.abs(o - dv.mean(axis=0)).max() <= 1e-12
+    assert np.abs(l - math.log(128)).max() <= 1e-12
