@@ -1,0 +1,247 @@
+"""Python binding of libattn45.so (the GB300 fused exact attention forward).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/attn45.h``. PyTorch is used for
+device memory and streams. There is no CPU fallback: if the library is not
+built or the device is not a GB300, calls raise.
+
+Functions carry the C names:
+
+* ``attn_fwd(q, k, v, causal=False, scale=None, out=None, lse=None)``
+* ``attn_fwd_varlen(q, k, v, cu_seqlens, causal=False, ...)``
+* ``attn_fp8_prepass(q, k, v, mode="block", rotate=True, hadamard_seed=0)``
+* ``attn_fwd_fp8(pre, causal=False, scale=None, ...)``
+* ``attn_fwd_fp8_auto(q, k, v, workspace=None, ...)``
+* ``attn_get_device_error()``, ``attn_set_wait_timeout_ns(ns)``
+
+``capi()`` returns the raw ctypes handle (pointer-and-size arguments).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "AttnError", "capi", "library_path",
+    "attn_fwd", "attn_fwd_varlen", "attn_fp8_prepass", "attn_fwd_fp8", "attn_fwd_fp8_auto",
+    "attn_fp8_workspace_size", "attn_fp8_vt_ld", "attn_get_device_error", "attn_set_wait_timeout_ns",
+    "attn_debug_timeout_probe", "EXPORTED_SYMBOLS",
+]
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
+_DTYPE = {torch.bfloat16: 0, torch.float16: 1}
+_FP8_MODE = {"tensor": 0, "block": 1}
+
+# Every function include/attn45.h declares.
+EXPORTED_SYMBOLS = (
+    "attn_fwd", "attn_fwd_varlen", "attn_fp8_vt_ld", "attn_fp8_prepass", "attn_fwd_fp8",
+    "attn_fp8_workspace_size", "attn_fwd_fp8_auto", "attn_get_device_error", "attn_set_wait_timeout_ns",
+    "attn_debug_timeout_probe", "attn_status_string", "attn_last_error_message", "attn_version",
+)
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"[{status}] {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def capi(build_if_missing: bool = True):
+    """Load libattn45.so (compiling it first if absent) and declare signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise AttnError(ATTN_ERR_UNSUPPORTED, f"{path} is not built")
+            path = _build.build()
+        lib = ctypes.CDLL(path)
+        P, I, F, U64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t
+        sig = {
+            "attn_fwd": ([P, P, P, P, P, I, I, I, I, I, I, F, I, P], I),
+            "attn_fwd_varlen": ([P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P], I),
+            "attn_fp8_vt_ld": ([I], I),
+            "attn_fp8_prepass": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, U64, P], I),
+            "attn_fwd_fp8": ([P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P], I),
+            "attn_fp8_workspace_size": ([I, I, I, I, I, I], SZ),
+            "attn_fwd_fp8_auto": ([P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, I, I, U64, P], I),
+            "attn_get_device_error": ([P], I),
+            "attn_set_wait_timeout_ns": ([U64], I),
+            "attn_debug_timeout_probe": ([U64, P], I),
+            "attn_status_string": ([I], ctypes.c_char_p),
+            "attn_last_error_message": ([], ctypes.c_char_p),
+            "attn_version": ([], I),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != ATTN_OK:
+        lib = capi()
+        raise AttnError(rc, lib.attn_last_error_message().decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise AttnError(ATTN_ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise AttnError(ATTN_ERR_INVALID_ARG, f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise AttnError(ATTN_ERR_INVALID_ARG, f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise AttnError(ATTN_ERR_INVALID_ARG, f"{name} must have {ndim} dims")
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
+    """O, LSE for q [B,N,H,d], k/v [B,N,Hkv,d] (bf16 or fp16)."""
+    _need(q, "q", ndim=4)
+    _need(k, "k", q.dtype, 4)
+    _need(v, "v", q.dtype, 4)
+    if q.dtype not in _DTYPE:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "q must be bf16 or fp16")
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "k and v must be [B,N,Hkv,d] matching q")
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(out, "out", q.dtype, 4)
+    _need(lse, "lse", torch.float32, 3)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check(capi().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d, int(bool(causal)),
+                           scale, _DTYPE[q.dtype], _stream(stream)))
+    return out, lse
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                    max_seqlen: int = 0, stream=None):
+    """O, LSE for packed q [T,H,d], k/v [T,Hkv,d] with int32 cu_seqlens [nseq+1] on the device."""
+    _need(q, "q", ndim=3)
+    _need(k, "k", q.dtype, 3)
+    _need(v, "v", q.dtype, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    if q.dtype not in _DTYPE:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "q must be bf16 or fp16")
+    T, H, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (T, Hkv, d) or v.shape != k.shape:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "k and v must be [T,Hkv,d] matching q")
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    nseq = cu_seqlens.numel() - 1
+    _check(capi().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens), nseq,
+                                  int(max_seqlen), T, H, Hkv, d, int(bool(causal)), scale, _DTYPE[q.dtype],
+                                  _stream(stream)))
+    return out, lse
+
+
+def attn_fp8_vt_ld(N: int) -> int:
+    return int(capi().attn_fp8_vt_ld(N))
+
+
+def attn_fp8_workspace_size(B, H, Hkv, N, d, mode: str = "block") -> int:
+    return int(capi().attn_fp8_workspace_size(B, H, Hkv, N, d, _FP8_MODE[mode]))
+
+
+def attn_fp8_prepass(q, k, v, mode: str = "block", rotate: bool = True, hadamard_seed: int = 0, stream=None):
+    """e4m3 codes and fp32 scales for bf16 q/k/v [B,N,H(kv),d]; returns a dict."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k, "k", torch.bfloat16, 4)
+    _need(v, "v", torch.bfloat16, 4)
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    dev = q.device
+    ld = attn_fp8_vt_ld(N)
+    nb = (N + 127) // 128
+    u8 = torch.uint8
+    pre = {
+        "q8": torch.empty((B, N, H, d), dtype=u8, device=dev),
+        "k8": torch.empty((B, N, Hkv, d), dtype=u8, device=dev),
+        "vt8": torch.empty((B, Hkv, d, ld), dtype=u8, device=dev),
+        "sq": torch.empty((B, H, nb) if mode == "block" else (1,), dtype=torch.float32, device=dev),
+        "sk": torch.empty((B, Hkv, nb) if mode == "block" else (1,), dtype=torch.float32, device=dev),
+        "sv": torch.empty((B, Hkv, d) if mode == "block" else (1,), dtype=torch.float32, device=dev),
+        "mode": mode, "rotate": rotate, "seed": hadamard_seed,
+    }
+    _check(capi().attn_fp8_prepass(_ptr(q), _ptr(k), _ptr(v), _ptr(pre["q8"]), _ptr(pre["k8"]), _ptr(pre["vt8"]),
+                                   _ptr(pre["sq"]), _ptr(pre["sk"]), _ptr(pre["sv"]), B, H, Hkv, N, d,
+                                   _FP8_MODE[mode], int(bool(rotate)), int(hadamard_seed), _stream(stream)))
+    return pre
+
+
+def attn_fwd_fp8(pre: dict, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
+    """O (bf16) and LSE from attn_fp8_prepass outputs."""
+    q8, k8 = pre["q8"], pre["k8"]
+    B, N, H, d = q8.shape
+    Hkv = k8.shape[2]
+    out = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check(capi().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(pre["vt8"]), _ptr(pre["sq"]), _ptr(pre["sk"]),
+                               _ptr(pre["sv"]), _ptr(out), _ptr(lse), B, H, Hkv, N, d, int(bool(causal)), scale,
+                               _FP8_MODE[pre["mode"]], _stream(stream)))
+    return out, lse
+
+
+def attn_fwd_fp8_auto(q, k, v, causal: bool = False, scale: float | None = None, mode: str = "block",
+                      rotate: bool = True, hadamard_seed: int = 0, workspace=None, out=None, lse=None, stream=None):
+    """Pre-pass + FP8 forward in one call; ``workspace`` is a uint8 CUDA tensor."""
+    _need(q, "q", torch.bfloat16, 4)
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    need = attn_fp8_workspace_size(B, H, Hkv, N, d, mode)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    out = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=q.device) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check(capi().attn_fwd_fp8_auto(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
+                                    int(bool(causal)), scale, _FP8_MODE[mode], int(bool(rotate)),
+                                    int(hadamard_seed), _stream(stream)))
+    return out, lse
+
+
+def attn_get_device_error(stream=None) -> int:
+    """Synchronise ``stream`` and return the device error status (clears it)."""
+    return int(capi().attn_get_device_error(_stream(stream)))
+
+
+def attn_set_wait_timeout_ns(ns: int):
+    _check(capi().attn_set_wait_timeout_ns(int(ns)))
+
+
+def attn_debug_timeout_probe(ns: int, stream=None):
+    _check(capi().attn_debug_timeout_probe(int(ns), _stream(stream)))

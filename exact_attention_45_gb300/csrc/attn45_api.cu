@@ -1,0 +1,305 @@
+// attn45_api.cu -- the C ABI (include/attn45.h): argument checks, TMA tensor
+// map encoding, grid sizing and launches. No allocation happens per call; the
+// only device state the library owns is one error word per device (a
+// __device__ variable, so nothing is allocated for it either).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn45.h"
+#include "attn_common.cuh"
+#include "api_internal.h"
+#include "launchers.h"
+#include "ptx.cuh"
+
+namespace attn45 {
+
+__device__ unsigned int g_err_word;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+unsigned long long g_timeout_ns = 2000000000ull;
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  unsigned int* err = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Current device's info, filled once. Returns ATTN_OK or an error code.
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    d.cc_major = prop.major;
+    d.cc_minor = prop.minor;
+    d.sm_count = prop.multiProcessorCount;
+    d.supported = (prop.major == 10 && prop.minor == 3);
+    void* sym = nullptr;
+    e = cudaGetSymbolAddress(&sym, g_err_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    d.err = static_cast<unsigned int*>(sym);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.ready = true;
+  }
+  if (!d.supported)
+    return fail(ATTN_ERR_UNSUPPORTED, "device %d has compute capability %d.%d; this library needs 10.3 (GB300)",
+                dev, d.cc_major, d.cc_minor);
+  *out = &d;
+  return ATTN_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// 4-D tiled map over a [batch][rows][heads][inner] tensor with dims listed
+// innermost first {inner, heads, rows, batch}; box = {box_inner, 1, box_rows,
+// 1}; 128-byte swizzle, out-of-bounds rows read as zero.
+int make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
+             uint64_t heads, uint64_t rows, uint64_t batch, uint32_t box_inner, uint32_t box_rows) {
+  cuuint64_t dims[4] = {inner, heads, rows, batch};
+  cuuint64_t strides[3] = {inner * elem_bytes, heads * inner * elem_bytes, rows * heads * inner * elem_bytes};
+  cuuint32_t box[4] = {box_inner, 1, box_rows, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, dt, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return ATTN_OK;
+}
+
+int check_common(int H, int Hkv, int d, int causal, float scale, int dtype) {
+  if (H < 1 || Hkv < 1 || H % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "need H >= 1, Hkv >= 1, H %% Hkv == 0 (H=%d Hkv=%d)", H, Hkv);
+  if (d != 64 && d != 128 && d != 256) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not in {64,128,256}", d);
+  if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return fail(ATTN_ERR_INVALID_ARG, "dtype %d unknown", dtype);
+  return ATTN_OK;
+}
+
+cudaError_t launch_f16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const FwdParams& p, bool causal, bool varlen, bool bf16, int grid, cudaStream_t s) {
+  switch (d) {
+    case 64: return launch_fwd_f16_d64(q, k, v, p, causal, varlen, bf16, grid, s);
+    case 128: return launch_fwd_f16_d128(q, k, v, p, causal, varlen, bf16, grid, s);
+    default: return launch_fwd_f16_d256(q, k, v, p, causal, varlen, bf16, grid, s);
+  }
+}
+
+__global__ void timeout_probe_kernel(unsigned long long ns, unsigned int* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, ns, &abort_flag, err);  // nothing ever arrives
+  __syncthreads();
+}
+
+}  // namespace
+
+// Shared with the FP8 translation unit (api_internal.h).
+int api_fail(int code, const char* msg) { return fail(code, "%s", msg); }
+int api_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+unsigned long long api_timeout_ns() { return g_timeout_ns; }
+int api_device(int* sm_count, unsigned int** err) {
+  DeviceInfo* d = nullptr;
+  int rc = device_info(&d);
+  if (rc) return rc;
+  *sm_count = d->sm_count;
+  *err = d->err;
+  return ATTN_OK;
+}
+int api_make_map(CUtensorMap* m, bool u8, const void* base, uint64_t inner, uint64_t heads, uint64_t rows,
+                 uint64_t batch, uint32_t box_inner, uint32_t box_rows) {
+  return make_map(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u8 ? 1 : 2, base,
+                  inner, heads, rows, batch, box_inner, box_rows);
+}
+
+}  // namespace attn45
+
+using namespace attn45;
+
+extern "C" {
+
+int attn_version(void) { return 1; }
+
+const char* attn_status_string(int s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* attn_last_error_message(void) { return g_msg; }
+
+int attn_set_wait_timeout_ns(uint64_t ns) {
+  if (ns < 1000ull || ns > 60000000000ull) return fail(ATTN_ERR_INVALID_ARG, "timeout %llu ns out of range", (unsigned long long)ns);
+  g_timeout_ns = ns;
+  return ATTN_OK;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N,
+             int d, int causal, float scale, int dtype, void* stream) {
+  int rc = check_common(H, Hkv, d, causal, scale, dtype);
+  if (rc) return rc;
+  if (B < 1 || N < 1) return fail(ATTN_ERR_INVALID_ARG, "need B >= 1 and N >= 1 (B=%d N=%d)", B, N);
+  if ((long long)B * N > 0x7fffffffLL || (long long)B * H * ((N + 127) / 128) > 0x7fffffffLL)
+    return fail(ATTN_ERR_INVALID_ARG, "problem too large for int32 indexing");
+  if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v, o must be 16-byte aligned and lse 4-byte aligned");
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  const int bn = f16_block_n(d);
+  const CUtensorMapDataType dt = dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap mq, mk, mv;
+  if ((rc = make_map(&mq, dt, 2, q, d, H, N, B, 64, BLOCK_M))) return rc;
+  if ((rc = make_map(&mk, dt, 2, k, d, Hkv, N, B, 64, bn))) return rc;
+  if ((rc = make_map(&mv, dt, 2, v, d, Hkv, N, B, 64, bn))) return rc;
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.o = o;
+  p.lse = lse;
+  p.nseq = B;
+  p.N = N;
+  p.total = B * N;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.group = H / Hkv;
+  p.ntiles = B * H * ((N + BLOCK_M - 1) / BLOCK_M);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = g_timeout_ns;
+  p.err = dev->err;
+  const int grid = p.ntiles < dev->sm_count ? p.ntiles : dev->sm_count;
+  cudaError_t e = launch_f16(d, mq, mk, mv, p, causal != 0, false, dtype == ATTN_BF16, grid,
+                             static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
+  return ATTN_OK;
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                    int nseq, int max_seqlen, int total, int H, int Hkv, int d, int causal, float scale,
+                    int dtype, void* stream) {
+  (void)max_seqlen;
+  int rc = check_common(H, Hkv, d, causal, scale, dtype);
+  if (rc) return rc;
+  if (nseq < 1 || nseq > MAX_VARLEN_SEQS) return fail(ATTN_ERR_INVALID_ARG, "nseq must be in [1, %d]", MAX_VARLEN_SEQS);
+  if (total < 0) return fail(ATTN_ERR_INVALID_ARG, "total must be >= 0");
+  if ((long long)H * ((long long)total / 128 + nseq + 1) > 0x7fffffffLL)
+    return fail(ATTN_ERR_INVALID_ARG, "problem too large for int32 indexing");
+  if (!cu_seqlens || !aligned(cu_seqlens, 4)) return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens must be a 4-byte aligned device pointer");
+  if (total == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v, o must be 16-byte aligned and lse 4-byte aligned");
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  const int bn = f16_block_n(d);
+  const CUtensorMapDataType dt = dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap mq, mk, mv;
+  if ((rc = make_map(&mq, dt, 2, q, d, H, total, 1, 64, BLOCK_M))) return rc;
+  if ((rc = make_map(&mk, dt, 2, k, d, Hkv, total, 1, 64, bn))) return rc;
+  if ((rc = make_map(&mv, dt, 2, v, d, Hkv, total, 1, 64, bn))) return rc;
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.o = o;
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.nseq = nseq;
+  p.total = total;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.group = H / Hkv;
+  p.ntiles = 0;  // computed on the device from cu_seqlens
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = g_timeout_ns;
+  p.err = dev->err;
+  const long long bound = (long long)H * ((total + BLOCK_M - 1) / BLOCK_M + nseq);
+  const int grid = bound < dev->sm_count ? (int)bound : dev->sm_count;
+  cudaError_t e = launch_f16(d, mq, mk, mv, p, causal != 0, true, dtype == ATTN_BF16, grid,
+                             static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_varlen launch");
+  return ATTN_OK;
+}
+
+int attn_get_device_error(void* stream) {
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_err_word, sizeof(word));
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (word) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+    if (word & DEV_ERR_TIMEOUT) return fail(ATTN_ERR_TIMEOUT, "a device-side wait exceeded its bound");
+  }
+  return ATTN_OK;
+}
+
+int attn_debug_timeout_probe(uint64_t ns, void* stream) {
+  if (ns < 1000ull || ns > 60000000000ull) return fail(ATTN_ERR_INVALID_ARG, "timeout out of range");
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(ns, dev->err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "timeout probe launch");
+  return ATTN_OK;
+}
+
+}  // extern "C"

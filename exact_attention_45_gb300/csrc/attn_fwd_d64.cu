@@ -1,0 +1,10 @@
+// attn_fwd_d64.cu -- BF16/FP16 forward instantiations for head dim 64.
+#include "fwd_launch.cuh"
+
+namespace attn45 {
+cudaError_t launch_fwd_f16_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const FwdParams& p, bool causal, bool varlen, bool bf16, int grid,
+                               cudaStream_t s) {
+  return launch_f16_dispatch<64, f16_block_n(64), 4>(q, k, v, p, causal, varlen, bf16, grid, s);
+}
+}  // namespace attn45

@@ -1,0 +1,158 @@
+/*
+ * attn45.h -- C ABI of the GB300 (sm_103a) fused exact attention forward
+ * library, libattn45.so.
+ *
+ * What is computed ("FlashAttention: Fast and Memory-Efficient Exact
+ * Attention with IO-Awareness", abstract: exact attention, tiled so the score
+ * matrix never goes to HBM; "FlashAttention-3: Fast and Accurate Attention
+ * with Asynchrony and Low-precision", abstract: the same layer with
+ * asynchronous data movement and an FP8 path):
+ *
+ *   O[i,h,:]  = sum_j softmax_j(scale * q[i,h,:] . k[j,hk,:]) v[j,hk,:]
+ *   lse[h,i]  = ln sum_j exp(scale * q[i,h,:] . k[j,hk,:])
+ *
+ * over the keys j of row i's own sequence (j <= i when causal), with kv head
+ * hk = h / (H / Hkv): H/Hkv consecutive query heads share one K/V head
+ * (grouped-query / multi-query attention).
+ *
+ * Conventions for every call
+ *  - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
+ *    aligned, contiguous in the layouts stated per call. The library never
+ *    frees or keeps them.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*,
+ *    NULL = legacy default stream) and never synchronises the host, except
+ *    attn_get_device_error().
+ *  - Head dim d must be 64, 128 or 256; H % Hkv == 0; scale > 0 and finite.
+ *  - Errors are returned as attn_status codes, never thrown or trapped; a
+ *    one-line description of the last failing call on this thread is
+ *    available from attn_last_error_message().
+ *  - Every device-side wait is bounded. If one gives up (a bug, never
+ *    expected), the kernel sets a device error word and exits cleanly;
+ *    attn_get_device_error() reports it as ATTN_ERR_TIMEOUT.
+ *  - Needs a compute capability 10.3 (GB300) device: ATTN_ERR_UNSUPPORTED
+ *    otherwise.
+ */
+#ifndef ATTN45_H
+#define ATTN45_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN45_API __attribute__((visibility("default")))
+#else
+#define ATTN45_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* bad pointer, alignment, shape or value */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not serve (device, head dim) */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  ATTN_ERR_TIMEOUT = 4      /* a device-side bounded wait gave up */
+} attn_status;
+
+typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype;
+
+typedef enum {
+  ATTN_FP8_PER_TENSOR = 0, /* one scale per tensor for Q, K and V */
+  ATTN_FP8_PER_BLOCK = 1   /* Q, K: one scale per (b, head, 128-row block); V: per (b, kv head, channel) */
+} attn_fp8_mode;
+
+/*
+ * attn_fwd -- fixed-length BF16/FP16 forward.
+ *   q   [B, N, H,   d]  dtype (BSHD, contiguous)
+ *   k,v [B, N, Hkv, d]  dtype
+ *   o   [B, N, H,   d]  dtype, written
+ *   lse [B, H, N]       fp32, natural-log logsumexp of the scaled scores, written
+ *   causal: 0 or 1 (row i attends keys j <= i).
+ * B, N >= 1 (B*N*H must fit in int32).
+ */
+ATTN45_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N,
+             int d, int causal, float scale, int dtype, void* stream);
+
+/*
+ * attn_fwd_varlen -- packed variable-length BF16/FP16 forward.
+ *   q [total, H, d], k,v [total, Hkv, d], o [total, H, d] (THD, contiguous);
+ *   lse [H, total] fp32;
+ *   cu_seqlens: DEVICE int32[nseq+1], cu_seqlens[0] = 0, non-decreasing,
+ *   cu_seqlens[nseq] = total; sequence s owns tokens [cu[s], cu[s+1]).
+ *   Causal masking is per sequence (local row i attends local keys j <= i).
+ *   1 <= nseq <= 2048. max_seqlen is accepted for interface symmetry and
+ *   unused. Empty sequences are allowed. Rows of each sequence see only keys
+ *   of that sequence.
+ */
+ATTN45_API int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                    int nseq, int max_seqlen, int total, int H, int Hkv, int d, int causal, float scale,
+                    int dtype, void* stream);
+
+/*
+ * FP8 (e4m3) path. "FlashAttention-3 ...", abstract technique (3): block
+ * quantization plus incoherent processing (Q and K multiplied by a random
+ * orthogonal matrix, which leaves Q K^T unchanged and spreads outliers).
+ *
+ * attn_fp8_prepass -- quantise BF16 Q, K, V (BSHD as in attn_fwd).
+ *   rotate != 0: Q and K rows are first mapped x -> (x * sigma) H_d / sqrt(d)
+ *     (Sylvester Hadamard H_d, butterfly stages of span 1, 2, ..., d/2 in
+ *     fp32; sigma_c = 1 - 2 * (splitmix64(hadamard_seed + c) & 1), the same
+ *     signs for every batch and head). V is never rotated.
+ *   scale = amax / 448 (1 when amax = 0); code = e4m3 RNE-satfinite(x / scale).
+ *   Outputs (device, caller-owned):
+ *     q8 [B,N,H,d], k8 [B,N,Hkv,d] uint8 e4m3 codes;
+ *     vt8 [B,Hkv,d,ldv] uint8: V codes transposed (keys contiguous),
+ *         ldv = attn_fp8_vt_ld(N) (padding columns written as 0);
+ *     mode PER_BLOCK:  sq [B,H,ceil(N/128)], sk [B,Hkv,ceil(N/128)], sv [B,Hkv,d] fp32;
+ *     mode PER_TENSOR: sq, sk, sv each one fp32.
+ *   sv is also used as scratch for the per-channel amax during the call.
+ */
+ATTN45_API int attn_fp8_vt_ld(int N);
+ATTN45_API int attn_fp8_prepass(const void* q, const void* k, const void* v, void* q8, void* k8, void* vt8, float* sq,
+                     float* sk, float* sv, int B, int H, int Hkv, int N, int d, int mode, int rotate,
+                     uint64_t hadamard_seed, void* stream);
+
+/*
+ * attn_fwd_fp8 -- forward on pre-pass outputs (same layouts as above).
+ *   o [B,N,H,d] BF16 and lse [B,H,N] fp32 (of the scaled, dequantised scores).
+ *   P is rounded to e4m3 after multiplication by 256 for the P*V product;
+ *   the row normaliser uses the unrounded P. d must be 128 in this build.
+ */
+ATTN45_API int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* sq, const float* sk,
+                 const float* sv, void* o, float* lse, int B, int H, int Hkv, int N, int d, int causal,
+                 float scale, int mode, void* stream);
+
+/*
+ * attn_fwd_fp8_auto -- pre-pass + FP8 forward in one call, with the
+ * quantised tensors placed in a caller-provided device workspace of at least
+ * attn_fp8_workspace_size() bytes (256-byte aligned).
+ */
+ATTN45_API size_t attn_fp8_workspace_size(int B, int H, int Hkv, int N, int d, int mode);
+ATTN45_API int attn_fwd_fp8_auto(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                      size_t workspace_bytes, int B, int H, int Hkv, int N, int d, int causal, float scale,
+                      int mode, int rotate, uint64_t hadamard_seed, void* stream);
+
+/* Synchronises `stream`, reads and clears the current device's error word.
+ * ATTN_OK, ATTN_ERR_TIMEOUT (a bounded device wait gave up) or ATTN_ERR_CUDA. */
+ATTN45_API int attn_get_device_error(void* stream);
+
+/* Bound for every device-side wait, in nanoseconds (default 2e9). Values
+ * outside [1e3, 6e10] are rejected with ATTN_ERR_INVALID_ARG. */
+ATTN45_API int attn_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook for the bounded-wait machinery: launches one CTA that waits on a
+ * barrier nothing will ever complete, with the given bound. Returns ATTN_OK
+ * once launched; the caller then sees ATTN_ERR_TIMEOUT from
+ * attn_get_device_error(). No fault, trap or hang is involved. */
+ATTN45_API int attn_debug_timeout_probe(uint64_t ns, void* stream);
+
+ATTN45_API const char* attn_status_string(int status);
+ATTN45_API const char* attn_last_error_message(void);
+ATTN45_API int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ATTN45_H */

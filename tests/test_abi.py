@@ -1,0 +1,69 @@
+"""CPU checks of the C ABI: the library builds, loads and exports every
+function include/attn45.h declares; host-side argument checks answer without
+touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "attn45.h")).read()
+    return sorted(set(re.findall(r"ATTN45_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import exact_attention_45_gb300 as A
+    return A.capi()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import exact_attention_45_gb300 as A
+    declared = _header_functions()
+    assert len(declared) >= 13
+    assert sorted(A.EXPORTED_SYMBOLS) == declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert lib.attn_status_string(0) == b"ok"
+    assert lib.attn_status_string(4) == b"device wait timed out"
+    assert lib.attn_version() >= 1
+
+
+def test_host_checks_need_no_gpu(lib):
+    # rejected before any CUDA call is made
+    rc = lib.attn_fwd(None, None, None, None, None, 1, 2, 2, 128, 96, 0, 0.1, 0, None)
+    assert rc == 2 and b"head dim" in lib.attn_last_error_message()
+    rc = lib.attn_fwd(None, None, None, None, None, 1, 3, 2, 128, 64, 0, 0.1, 0, None)
+    assert rc == 1
+    rc = lib.attn_fwd(None, None, None, None, None, 1, 2, 2, 128, 64, 0, -1.0, 0, None)
+    assert rc == 1 and b"scale" in lib.attn_last_error_message()
+    rc = lib.attn_fwd(None, None, None, None, None, 1, 2, 2, 128, 64, 2, 0.1, 0, None)
+    assert rc == 1
+    rc = lib.attn_fwd(None, None, None, None, None, 0, 2, 2, 128, 64, 0, 0.1, 0, None)
+    assert rc == 1
+    rc = lib.attn_fwd(None, None, None, None, None, 1, 2, 2, 128, 64, 0, 0.1, 0, None)
+    assert rc == 1 and b"null" in lib.attn_last_error_message()
+    rc = lib.attn_fwd_varlen(None, None, None, None, None, None, 0, 0, 10, 2, 2, 64, 0, 0.1, 0, None)
+    assert rc == 1
+    assert lib.attn_set_wait_timeout_ns(10) == 1
+    assert lib.attn_set_wait_timeout_ns(2_000_000_000) == 0
+
+
+def test_vt_ld(lib):
+    assert lib.attn_fp8_vt_ld(1) == 128 and lib.attn_fp8_vt_ld(128) == 128 and lib.attn_fp8_vt_ld(129) == 256
+
+
+def test_oracle_and_product_share_no_code():
+    # neither side imports the other
+    for path in ("exact_attention_45_gb300/__init__.py", "exact_attention_45_gb300/build.py"):
+        assert "oracle" not in open(os.path.join(ROOT, path)).read()
+    src = open(os.path.join(ROOT, "oracle", "__init__.py")).read()
+    assert "exact_attention_45_gb300" not in src.split('"""', 2)[2]
+    assert "exact_attention_45_gb300" not in open(os.path.join(ROOT, "oracle", "attn_oracle.c")).read()
