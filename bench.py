@@ -1,0 +1,322 @@
+"""Benchmark of the fused exact attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one forward pass (tile scheduling, Q/K/V tile loads, S = Q K^T,
+masking + online softmax, correction, P V, epilogue) over one batch of
+synthetic BF16 inputs, the workload being BF16 non-causal, head dim 128,
+16 heads, 4 sequences of 4096 tokens (16384 tokens, hidden 2048), N(0,1).
+The metric is attention TFLOP/s = 4*B*H*N^2*d / t (half for causal).
+
+Prints one JSON line (rank 0). With several GPUs (torchrun) each rank runs an
+independent replica of the workload (weak scaling, no collective on the data
+path); the value is the total work of all ranks over the slowest rank's time.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead, on
+a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = {"workload": "attn_fwd bf16 non-causal d128", "B": 4, "N": 4096, "H": 16, "Hkv": 16, "d": 128,
+            "causal": False, "dtype": "bf16", "inputs": "N(0,1) seed 0"}
+METRIC = "attention fwd TFLOP/s (4BHN^2d, 1/2 causal)"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def flops_of(w) -> float:
+    f = 4.0 * w["B"] * w["H"] * w["N"] ** 2 * w["d"]
+    return f / 2 if w["causal"] else f
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            pk = json.load(fh)
+        return {"bf16_tflops": pk["bf16_tflops"], "bf16_tflops_sustained": pk["bf16_tflops_sustained"],
+                "hbm_gbs": pk["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_seconds: float, local_flops: float, group=None):
+    """(max seconds over ranks, total flops over ranks); identity without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_seconds, local_flops
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    f = torch.tensor([local_flops], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(f, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(f.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.out = os.path.join("/tmp", f"attn45_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.out, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.out):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.out):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        os.remove(self.out)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s, p in zip(sm, power) if p > 0.5 * max(power)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "samples": len(sm),
+                "power_w_max": max(power), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ oracle (CPU baseline)
+def cpu_oracle_rate(w, budget_s: float = 12.0, seed: int = 0):
+    """Time the fp64 oracle on a seeded sample of rows of the workload; returns
+    (TFLOP/s extrapolated to the metric's flop count, threads, sample text)."""
+    import numpy as np
+
+    import attn_inputs as gen
+    import oracle as O
+    q, k, v = gen.qkv_fixed(w["B"], w["N"], w["H"], w["Hkv"], w["d"], seed=seed)
+    threads = os.cpu_count() or 1
+    per_row = 4.0 * w["N"] * w["d"] * (0.5 if w["causal"] else 1.0)
+    rows = 256
+    t_used = 0.0
+    while True:
+        rs, rh, ri = gen.sample_rows([w["N"]] * w["B"], w["H"], rows, seed=seed)
+        t0 = time.perf_counter()
+        O.attention(q, k, v, causal=w["causal"], rows=(rs, rh, ri), nthreads=threads)
+        t_used = time.perf_counter() - t0
+        if t_used >= budget_s * 0.5 or rows >= w["B"] * w["H"] * w["N"]:
+            break
+        rows = int(min(rows * max(2.0, budget_s / max(t_used, 1e-3) * 0.8), w["B"] * w["H"] * w["N"]))
+    n = len(rs)
+    rate = per_row * n / t_used / 1e12
+    return rate, threads, f"{n} seeded (b,h,row) query rows of the workload, {t_used:.1f} s"
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import attn_inputs as gen
+    import exact_attention_45_gb300 as A
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    w = dict(WORKLOAD)
+    B, N, H, Hkv, d = w["B"], w["N"], w["H"], w["Hkv"], w["d"]
+    q_h, k_h, v_h = gen.qkv_fixed(B, N, H, Hkv, d, seed=rank)
+    q, k, v = q_h.cuda(), k_h.cuda(), v_h.cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    lib = A.capi()
+    scale = 1.0 / math.sqrt(d)
+
+    def launch():
+        rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv, N, d,
+                          int(w["causal"]), scale, 0, stream.cuda_stream)
+        if rc != 0:
+            raise A.AttnError(rc, lib.attn_last_error_message().decode())
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        launch()
+    torch.cuda.synchronize()
+    if A.attn_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        barrier()
+        for i in range(args.steps):
+            flush.zero_()                      # L2 flushed between timed iterations
+            starts[i].record(stream)
+            launch()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    clocks = clk.summary()
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_s = sum(times_ms) / 1e3
+    local_flops = flops_of(w) * args.steps
+    t_max, total_flops = aggregate(kernel_s, local_flops)
+    value = total_flops / t_max / 1e12
+
+    # end to end through the same C-ABI call with host buffers: pinned H2D of
+    # q, k, v, the kernel, D2H of o and lse, all inside the timed region
+    q_p, k_p, v_p = (t.pin_memory() for t in (q_h, k_h, v_h))
+    o_p = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    l_p = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(q_p, non_blocking=True)
+        k.copy_(k_p, non_blocking=True)
+        v.copy_(v_p, non_blocking=True)
+        launch()
+        o_p.copy_(o, non_blocking=True)
+        l_p.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    e2e_max, e2e_flops = aggregate(e2e_s, local_flops)
+    if A.attn_get_device_error() != 0:
+        raise RuntimeError("device error during timing")
+
+    pk = peaks()
+    avg_launch_s = kernel_s / args.steps
+    achieved = flops_of(w) / avg_launch_s / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_max / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**w, "global_batch": B * world, "seq_len": N, "parallelism": f"replicas{world}",
+                   "l2": "flushed between timed iterations (512 MiB write)"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": None,
+                     "peak_source": f"{pk['source']} bf16 burst (cuBLAS)", "kernel": "attn_fwd_f16_kernel"},
+        "e2e": {"value": round(e2e_flops / e2e_max / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2,
+                "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, threads, sample = cpu_oracle_rate(w, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1 and dist.is_initialized():
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = dict(WORKLOAD)
+    vals = []
+    sample = ""
+    threads = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        cpu_oracle_rate(w, budget_s=2.0)
+    for _ in range(args.steps):
+        rate, threads, sample = cpu_oracle_rate(w, budget_s=args.cpu_budget / max(1, args.steps) * 2)
+        vals.append(rate)
+    value = statistics.mean(vals)
+    per_step_s = flops_of(w) / (value * 1e12)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step_s * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {**w, "global_batch": w["B"], "seq_len": w["N"], "parallelism": "cpu"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample + " per step (extrapolated to the full workload's flops)"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)      # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
