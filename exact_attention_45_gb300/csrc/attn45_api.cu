@@ -120,11 +120,11 @@ int check_common(int H, int Hkv, int d, int causal, float scale, int dtype) {
 }
 
 cudaError_t launch_f16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                       const FwdParams& p, bool causal, bool varlen, bool bf16, int grid, cudaStream_t s) {
+                       const FwdParams& p, bool causal, bool varlen, bool bf16, int sm_count, cudaStream_t s) {
   switch (d) {
-    case 64: return launch_fwd_f16_d64(q, k, v, p, causal, varlen, bf16, grid, s);
-    case 128: return launch_fwd_f16_d128(q, k, v, p, causal, varlen, bf16, grid, s);
-    default: return launch_fwd_f16_d256(q, k, v, p, causal, varlen, bf16, grid, s);
+    case 64: return launch_fwd_f16_d64(q, k, v, p, causal, varlen, bf16, sm_count, s);
+    case 128: return launch_fwd_f16_d128(q, k, v, p, causal, varlen, bf16, sm_count, s);
+    default: return launch_fwd_f16_d256(q, k, v, p, causal, varlen, bf16, sm_count, s);
   }
 }
 
@@ -216,12 +216,10 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.H = H;
   p.Hkv = Hkv;
   p.group = H / Hkv;
-  p.ntiles = B * H * ((N + BLOCK_M - 1) / BLOCK_M);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
   p.err = dev->err;
-  const int grid = p.ntiles < dev->sm_count ? p.ntiles : dev->sm_count;
-  cudaError_t e = launch_f16(d, mq, mk, mv, p, causal != 0, false, dtype == ATTN_BF16, grid,
+  cudaError_t e = launch_f16(d, mq, mk, mv, p, causal != 0, false, dtype == ATTN_BF16, dev->sm_count,
                              static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
   return ATTN_OK;
@@ -264,9 +262,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
   p.err = dev->err;
-  const long long bound = (long long)H * ((total + BLOCK_M - 1) / BLOCK_M + nseq);
-  const int grid = bound < dev->sm_count ? (int)bound : dev->sm_count;
-  cudaError_t e = launch_f16(d, mq, mk, mv, p, causal != 0, true, dtype == ATTN_BF16, grid,
+  cudaError_t e = launch_f16(d, mq, mk, mv, p, causal != 0, true, dtype == ATTN_BF16, dev->sm_count,
                              static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_varlen launch");
   return ATTN_OK;

@@ -1,0 +1,453 @@
+// attn_fwd2_kernel.cuh -- BF16/FP16 forward, two 128-row query tiles per CTA.
+//
+// Same computation as attn_fwd_kernel.cuh, organised so the tensor core never
+// waits for a softmax: a CTA owns a 256-row "super tile" of one (sequence,
+// head), split into tile A (rows 0-127) and tile B (rows 128-255), which share
+// every K/V block loaded into shared memory. Each tile has one TMEM S buffer
+// (P is written back over it) and one TMEM O accumulator. The MMA thread
+// issues, per key block j,
+//     O_A += P_A(j-1) V_{j-1},  S_A(j) = Q_A K_j^T,  O_B += P_B(j-1) V_{j-1},  S_B(j) = Q_B K_j^T
+// so while softmax warpgroup A turns S_A(j) into P_A(j) the tensor core runs
+// tile B's two GEMMs, and the other way round ("FlashAttention-3: Fast and
+// Accurate Attention with Asynchrony and Low-precision", abstract: warp
+// specialisation and block-wise interleaving of matmul and softmax; here the
+// interleaving is between two tiles through TMEM instead of Hopper registers).
+//
+// Online softmax ("Related papers: FlashAttention-4" page, online-softmax
+// teaser: running maximum and normaliser): the running maximum m is only
+// raised when a block's maximum exceeds it by more than 2^8; otherwise the
+// stale m keeps being used, P stays <= 2^8 and neither O nor l is rescaled.
+// The final O / l and logsumexp are unchanged by this (both use the same m).
+//
+// Warps 0-3: softmax/correction/epilogue of tile A; warps 4-7: tile B (thread
+// r of a warpgroup owns row r = TMEM lane r); warp 8: TMA; warp 9: MMA.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include "attn_common.cuh"
+#include "attn_fwd_kernel.cuh"
+#include "ptx.cuh"
+
+namespace attn45 {
+
+constexpr int SUPER_M = 2 * BLOCK_M;          // query rows per CTA work unit
+constexpr float LAZY_RESCALE_LOG2 = 8.0f;     // raise m only past this margin
+
+template <int D, int BN, int STAGES>
+struct Pair2Traits {
+  static constexpr int NC = D / 64;
+  static constexpr int Q_CHUNK = BLOCK_M * 128;
+  static constexpr int KV_CHUNK = BN * 128;
+  static constexpr int Q_BYTES = BLOCK_M * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int OFF_Q = 0;                        // Q_A then Q_B
+  static constexpr int OFF_K = 2 * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr int OFF_BARS = OFF_V + STAGES * KV_BYTES;
+  static constexpr int BARS_BYTES = 512;
+  static constexpr int OFF_PREFIX = OFF_BARS + BARS_BYTES;
+  static constexpr int SMEM_FIXED = OFF_PREFIX + 1024;
+  static constexpr int TMEM_S = 0;                       // + BN * tile
+  static constexpr int TMEM_O = 2 * BN;                  // + D * tile
+  static constexpr int TMEM_COLS = 512;
+  static_assert(2 * BN + 2 * D <= TMEM_COLS, "TMEM budget");
+};
+
+struct Bars2 {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Bars2) <= 512, "barrier block");
+
+struct Tile2 {
+  int seq, h, sblk, n, tok0, tma_row0, tma_b;
+};
+
+// Fixed length. Non-causal: head-major (all super tiles of one (b,h) are
+// adjacent, so CTAs running together share that head's K/V in L2). Causal:
+// longest first (super-tile index descending), heads fastest.
+template <bool CAUSAL>
+__device__ __forceinline__ Tile2 tile2_fixed(const FwdParams& p, int t) {
+  const int nsb = ceil_div(p.N, SUPER_M);
+  Tile2 T;
+  int bh;
+  if (CAUSAL) {
+    const int cnt = p.nseq * p.H;
+    T.sblk = nsb - 1 - t / cnt;
+    bh = t % cnt;
+  } else {
+    bh = t / nsb;
+    T.sblk = t % nsb;
+  }
+  T.seq = bh / p.H;
+  T.h = bh % p.H;
+  T.n = p.N;
+  T.tok0 = T.seq * p.N;
+  T.tma_row0 = 0;
+  T.tma_b = T.seq;
+  return T;
+}
+
+// Varlen: prefix[s] = H * sum_{s'<s} ceil(n_s'/256); inside a sequence,
+// super tiles run longest first with heads fastest.
+__device__ __forceinline__ Tile2 tile2_varlen(const FwdParams& p, const int* prefix, int t) {
+  int lo = 0, hi = p.nseq - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  Tile2 T;
+  T.seq = lo;
+  const int r = t - prefix[lo];
+  const int a = __ldg(p.cu_seqlens + lo), b = __ldg(p.cu_seqlens + lo + 1);
+  T.n = b - a;
+  T.sblk = ceil_div(T.n, SUPER_M) - 1 - r / p.H;
+  T.h = r % p.H;
+  T.tok0 = a;
+  T.tma_row0 = a;
+  T.tma_b = 0;
+  return T;
+}
+
+__device__ __forceinline__ void build_varlen_prefix2(const FwdParams& p, int* prefix) {
+  for (int s = threadIdx.x; s < p.nseq; s += blockDim.x) {
+    const int n = __ldg(p.cu_seqlens + s + 1) - __ldg(p.cu_seqlens + s);
+    prefix[s + 1] = (n > 0 ? ceil_div(n, SUPER_M) : 0) * p.H;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int base = 0; base < p.nseq; base += 32) {
+      const int s = base + lane;
+      int v = s < p.nseq ? prefix[s + 1] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += u;
+      }
+      if (s < p.nseq) prefix[s + 1] = v + carry;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) prefix[0] = 0;
+  }
+  __syncthreads();
+}
+
+// Key blocks tile x (0 = A, 1 = B) of a super tile visits; 0 if it has no rows.
+template <bool CAUSAL, int BN>
+__device__ __forceinline__ int tile2_blocks(const Tile2& tl, int x) {
+  const int r0 = tl.sblk * SUPER_M + x * BLOCK_M;
+  if (r0 >= tl.n) return 0;
+  int kend = tl.n;
+  if (CAUSAL) kend = min(kend, r0 + BLOCK_M);
+  return ceil_div(kend, BN);
+}
+
+template <int D, int BN, int STAGES, bool CAUSAL, bool VARLEN, bool BF16>
+__global__ void __launch_bounds__(320, 1)
+attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using T = Pair2Traits<D, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sQ = smem + T::OFF_Q;
+  uint8_t* sK = smem + T::OFF_K;
+  uint8_t* sV = smem + T::OFF_V;
+  Bars2* bars = reinterpret_cast<Bars2*>(smem + T::OFF_BARS);
+  int* prefix = reinterpret_cast<int*>(smem + T::OFF_PREFIX);
+  volatile int* abort_flag = &bars->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars->s_full[x], 1);
+      mbar_init(&bars->p_full[x], 128);
+      mbar_init(&bars->o_done[x], 1);
+    }
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&bars->tmem_base, T::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  int ntiles = p.ntiles;
+  if constexpr (VARLEN) {
+    build_varlen_prefix2(p, prefix);
+    ntiles = prefix[p.nseq];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const uint64_t tmo = p.timeout_ns;
+
+  auto get_tile = [&](int t) -> Tile2 {
+    if constexpr (VARLEN) return tile2_varlen(p, prefix, t);
+    else return tile2_fixed<CAUSAL>(p, t);
+  };
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int kv_it = 0, tile_i = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tile_i) {
+        const Tile2 tl = get_tile(t);
+        const int hk = tl.h / p.group;
+        const int nkv = max(tile2_blocks<CAUSAL, BN>(tl, 0), tile2_blocks<CAUSAL, BN>(tl, 1));
+        ok = mbar_wait(&bars->q_empty, (tile_i & 1) ^ 1, tmo, abort_flag, p.err);
+        if (!ok) break;
+        mbar_expect_tx(&bars->q_full, 2 * T::Q_BYTES);
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+          for (int c = 0; c < T::NC; ++c)
+            tma_load_4d(&tmQ, &bars->q_full, sQ + x * T::Q_BYTES + c * T::Q_CHUNK, c * 64, tl.h,
+                        tl.tma_row0 + tl.sblk * SUPER_M + x * BLOCK_M, tl.tma_b);
+        for (int j = 0; j < nkv; ++j, ++kv_it) {
+          const int st = kv_it % STAGES;
+          const uint32_t ph = (kv_it / STAGES) & 1;
+          const int krow = tl.tma_row0 + j * BN;
+          ok = mbar_wait(&bars->k_empty[st], ph ^ 1, tmo, abort_flag, p.err);
+          if (!ok) break;
+          mbar_expect_tx(&bars->k_full[st], T::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < T::NC; ++c)
+            tma_load_4d(&tmK, &bars->k_full[st], sK + st * T::KV_BYTES + c * T::KV_CHUNK, c * 64, hk, krow,
+                        tl.tma_b);
+          ok = mbar_wait(&bars->v_empty[st], ph ^ 1, tmo, abort_flag, p.err);
+          if (!ok) { ++kv_it; break; }
+          mbar_expect_tx(&bars->v_full[st], T::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < T::NC; ++c)
+            tma_load_4d(&tmV, &bars->v_full[st], sV + st * T::KV_BYTES + c * T::KV_CHUNK, c * 64, hk, krow,
+                        tl.tma_b);
+        }
+      }
+      const int last = kv_it;
+      for (int it = (last > STAGES ? last - STAGES : 0); it < last; ++it) {
+        const int st = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        mbar_wait_drain(&bars->k_full[st], ph, tmo, p.err);
+        mbar_wait_drain(&bars->v_full[st], ph, tmo, p.err);
+      }
+      if (tile_i > 0) mbar_wait_drain(&bars->q_full, (tile_i - 1) & 1, tmo, p.err);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_kind_f16(BLOCK_M, BN, BF16, false);
+      constexpr uint32_t idesc_o = idesc_kind_f16(BLOCK_M, D, BF16, true);
+      const uint32_t qa = smem_u32(sQ);
+      const uint32_t ka = smem_u32(sK);
+      const uint32_t va = smem_u32(sV);
+      int kv_it = 0, tile_i = 0;
+      int p_cnt[2] = {0, 0};
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tile_i) {
+        const Tile2 tl = get_tile(t);
+        const int nblk[2] = {tile2_blocks<CAUSAL, BN>(tl, 0), tile2_blocks<CAUSAL, BN>(tl, 1)};
+        const int nkv = max(nblk[0], nblk[1]);
+        ok = mbar_wait(&bars->q_full, tile_i & 1, tmo, abort_flag, p.err);
+        if (!ok) break;
+        for (int j = 0; j <= nkv && ok; ++j) {
+          const int st = kv_it % STAGES;               // stage of block j
+          const int pst = (kv_it + STAGES - 1) % STAGES;  // stage of block j-1
+          bool v_ready = false, k_ready = false;
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            // O_x += P_x(j-1) V_{j-1}
+            if (j >= 1 && j - 1 < nblk[x]) {
+              ok = mbar_wait(&bars->p_full[x], p_cnt[x] & 1, tmo, abort_flag, p.err);
+              if (!ok) break;
+              ++p_cnt[x];
+              if (!v_ready) {
+                ok = mbar_wait(&bars->v_full[pst], ((kv_it - 1) / STAGES) & 1, tmo, abort_flag, p.err);
+                if (!ok) break;
+                v_ready = true;
+              }
+              tc_fence_after();
+              const uint32_t a_tmem = tmem + T::TMEM_S + x * BN;
+              const uint32_t vbase = va + pst * T::KV_BYTES;
+#pragma unroll
+              for (int k = 0; k < BN / 16; ++k)
+                umma_f16_ts(tmem + T::TMEM_O + x * D, a_tmem + k * 8,
+                            sdesc_mnmajor_sw128(vbase + k * 2048, T::KV_CHUNK), idesc_o, (j > 1 || k > 0) ? 1u : 0u);
+              umma_commit(&bars->o_done[x]);
+            }
+            // S_x(j) = Q_x K_j^T
+            if (j < nblk[x]) {
+              if (!k_ready) {
+                ok = mbar_wait(&bars->k_full[st], (kv_it / STAGES) & 1, tmo, abort_flag, p.err);
+                if (!ok) break;
+                k_ready = true;
+                tc_fence_after();
+              }
+              const uint32_t qx = qa + x * T::Q_BYTES;
+              const uint32_t kb = ka + st * T::KV_BYTES;
+#pragma unroll
+              for (int k = 0; k < D / 16; ++k) {
+                const uint32_t qo = (k >> 2) * T::Q_CHUNK + (k & 3) * 32;
+                const uint32_t ko = (k >> 2) * T::KV_CHUNK + (k & 3) * 32;
+                umma_f16_ss(tmem + T::TMEM_S + x * BN, sdesc_kmajor_sw128(qx + qo), sdesc_kmajor_sw128(kb + ko),
+                            idesc_s, k > 0 ? 1u : 0u);
+              }
+              umma_commit(&bars->s_full[x]);
+            }
+          }
+          if (!ok) break;
+          if (j >= 1) umma_commit(&bars->v_empty[pst]);
+          if (j < nkv) {
+            umma_commit(&bars->k_empty[st]);
+            if (j == nkv - 1) umma_commit(&bars->q_empty);
+            ++kv_it;
+          }
+        }
+      }
+      umma_commit(&bars->mma_done);
+      mbar_wait_drain(&bars->mma_done, 0, tmo, p.err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------- softmax / correction / epilogue
+    const int x = warp >> 2;                           // 0 = tile A, 1 = tile B
+    const int r = threadIdx.x & 127;                   // row within the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t ts = tmem + lane_off + T::TMEM_S + x * BN;
+    const uint32_t to = tmem + lane_off + T::TMEM_O + x * D;
+    const float sl2 = p.scale_log2;
+    int s_cnt = 0, pv_total = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      const Tile2 tl = get_tile(t);
+      const int nblk = tile2_blocks<CAUSAL, BN>(tl, x);
+      if (nblk == 0) continue;                        // tile B past the sequence end
+      const int row0 = tl.sblk * SUPER_M + x * BLOCK_M;  // first row of this tile
+      const int i_row = row0 + r;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nblk; ++j) {
+        ok = mbar_wait(&bars->s_full[x], s_cnt & 1, tmo, abort_flag, p.err);
+        ++s_cnt;
+        if (!ok) break;
+        tc_fence_after();
+        float s[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(ts + c * 32, u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(u[i]);
+        }
+        const int col0 = j * BN;
+        if ((col0 + BN > tl.n) || (CAUSAL && col0 + BN - 1 > row0)) {
+          int limit = tl.n - col0;
+          if (CAUSAL) limit = min(limit, i_row - col0 + 1);
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c >= limit) s[c] = -INFINITY;
+        }
+        float mx0 = s[0], mx1 = s[1];
+#pragma unroll
+        for (int c = 2; c < BN; c += 2) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+        }
+        const float mx = fmaxf(mx0, mx1) * sl2;
+        // raise the running max only when it moved by more than 2^8
+        const bool raise = mx > m + LAZY_RESCALE_LOG2;
+        const float m_new = raise ? mx : m;
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = raise ? ex2_approx(m - m_use) : 1.f;
+        float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < BN; c += 2) {
+          s[c] = ex2_approx(fmaf(s[c], sl2, -m_use));
+          s[c + 1] = ex2_approx(fmaf(s[c + 1], sl2, -m_use));
+          sum0 += s[c];
+          sum1 += s[c + 1];
+        }
+        l = l * alpha + (sum0 + sum1);
+        m = m_new;
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t u[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = pack2(s[c * 64 + 2 * i], s[c * 64 + 2 * i + 1], BF16);
+          tmem_st32(ts + c * 32, u);
+        }
+        // correction: O_x += P(j-1) V has completed (it was issued before
+        // S_x(j), whose completion we just observed), so O_x is stable.
+        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld32(to + c * 32, u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+            tmem_st32(to + c * 32, u);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[x]);
+      }
+      if (!ok) break;
+      pv_total += nblk;
+      ok = mbar_wait(&bars->o_done[x], (pv_total - 1) & 1, tmo, abort_flag, p.err);
+      if (!ok) break;
+      tc_fence_after();
+      const bool valid = i_row < tl.n;
+      const float inv_l = 1.f / l;
+      const size_t tok = (size_t)tl.tok0 + (size_t)(valid ? i_row : 0);
+      uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.o) + (tok * p.H + tl.h) * D);
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(to + c * 32, u);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l, BF16);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            orow[c * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (valid) {
+        const float lse = (m + lg2_approx(l)) * 0.69314718055994530942f;
+        if constexpr (VARLEN) p.lse[(size_t)tl.h * p.total + tok] = lse;
+        else p.lse[((size_t)tl.seq * p.H + tl.h) * p.N + i_row] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, T::TMEM_COLS);
+}
+
+}  // namespace attn45
