@@ -275,6 +275,59 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_sweep(args):
+    """TFLOP/s of every BF16 configuration of the benchmark set (one GPU):
+    the hidden-2048 sweep (d=64/H=32 and d=128/H=16, N = 512..16384,
+    B*N = 16384), d=256/H=8 for N = 1024..16384, causal and not, and the GQA
+    varlen causal batch. One JSON object per line on stdout."""
+    import torch
+
+    import attn_inputs as gen
+    import exact_attention_45_gb300 as A
+    torch.cuda.set_device(0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    pk = peaks()
+    cases = [(d, H, N, c) for d, H in ((64, 32), (128, 16)) for N in (512, 1024, 2048, 4096, 8192, 16384)
+             for c in (False, True)]
+    cases += [(256, 8, N, c) for N in (1024, 2048, 4096, 8192, 16384) for c in (False, True)]
+
+    def timeit(fn, reps):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ts) / 1e3
+
+    for d, H, N, causal in cases:
+        B = 16384 // N
+        q, k, v = (t.cuda() for t in gen.qkv_fixed(B, N, H, H, d, seed=0))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        t = timeit(lambda: A.attn_fwd(q, k, v, causal=causal, out=o, lse=lse), args.sweep_reps)
+        fl = 4.0 * B * H * N * N * d / (2 if causal else 1)
+        print(json.dumps({"d": d, "H": H, "N": N, "B": B, "causal": causal, "ms": round(t * 1e3, 4),
+                          "tflops": round(fl / t / 1e12, 1), "frac": round(fl / t / 1e12 / pk["bf16_tflops"], 4)}),
+              flush=True)
+    lengths = gen.varlen_lengths(8, 1024, 32768, seed=0)
+    q, k, v, cu = gen.qkv_varlen(lengths, 32, 8, 128, seed=0)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    dcu = torch.as_tensor(cu, dtype=torch.int32, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((32, q.shape[0]), dtype=torch.float32, device="cuda")
+    t = timeit(lambda: A.attn_fwd_varlen(q, k, v, dcu, causal=True, out=o, lse=lse), args.sweep_reps)
+    fl = sum(4.0 * 32 * int(n) ** 2 * 128 / 2 for n in lengths)
+    print(json.dumps({"varlen_gqa": [int(n) for n in lengths], "H": 32, "Hkv": 8, "d": 128, "causal": True,
+                      "ms": round(t * 1e3, 4), "tflops": round(fl / t / 1e12, 1),
+                      "frac": round(fl / t / 1e12 / pk["bf16_tflops"], 4)}), flush=True)
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -310,9 +363,13 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="time every BF16 configuration instead")
+    ap.add_argument("--sweep-reps", type=int, default=20)
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)      # at least 3 untimed warm-up steps
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

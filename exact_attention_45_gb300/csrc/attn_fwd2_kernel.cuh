@@ -149,7 +149,7 @@ __device__ __forceinline__ int tile2_blocks(const Tile2& tl, int x) {
 }
 
 template <int D, int BN, int STAGES, bool CAUSAL, bool VARLEN, bool BF16>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __maxnreg__(200)
 attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using T = Pair2Traits<D, BN, STAGES>;
@@ -352,13 +352,13 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         ++s_cnt;
         if (!ok) break;
         tc_fence_after();
+        static_assert(BN == 128, "softmax path assumes 128-column S tiles");
         float s[BN];
+        {
+          uint32_t u[BN];
+          tmem_ld128(ts, u);
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t u[32];
-          tmem_ld32(ts + c * 32, u);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(u[i]);
+          for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(u[i]);
         }
         const int col0 = j * BN;
         if ((col0 + BN > tl.n) || (CAUSAL && col0 + BN - 1 > row0)) {
@@ -368,26 +368,43 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           for (int c = 0; c < BN; ++c)
             if (c >= limit) s[c] = -INFINITY;
         }
-        float mx0 = s[0], mx1 = s[1];
+        float mxa = fmaxf(s[0], s[1]), mxb = fmaxf(s[2], s[3]);
+        float mxc = fmaxf(s[4], s[5]), mxd = fmaxf(s[6], s[7]);
 #pragma unroll
-        for (int c = 2; c < BN; c += 2) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
+        for (int c = 8; c < BN; c += 8) {
+          mxa = fmaxf(mxa, fmaxf(s[c], s[c + 1]));
+          mxb = fmaxf(mxb, fmaxf(s[c + 2], s[c + 3]));
+          mxc = fmaxf(mxc, fmaxf(s[c + 4], s[c + 5]));
+          mxd = fmaxf(mxd, fmaxf(s[c + 6], s[c + 7]));
         }
-        const float mx = fmaxf(mx0, mx1) * sl2;
+        const float mx = fmaxf(fmaxf(mxa, mxb), fmaxf(mxc, mxd)) * sl2;
         // raise the running max only when it moved by more than 2^8
         const bool raise = mx > m + LAZY_RESCALE_LOG2;
         const float m_new = raise ? mx : m;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = raise ? ex2_approx(m - m_use) : 1.f;
-        float sum0 = 0.f, sum1 = 0.f;
+        // p = 2^(s * scale * log2(e) - m): the affine step and the row sum run
+        // as packed f32x2 operations, the exponentials on the MUFU unit
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        const uint64_t negm2 = f2_pack(-m_use, -m_use);
+        uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-        for (int c = 0; c < BN; c += 2) {
-          s[c] = ex2_approx(fmaf(s[c], sl2, -m_use));
-          s[c + 1] = ex2_approx(fmaf(s[c + 1], sl2, -m_use));
-          sum0 += s[c];
-          sum1 += s[c + 1];
+        for (int c = 0; c < BN; c += 4) {
+          float a0, a1, b0, b1;
+          f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, negm2), a0, a1);
+          f2_unpack(f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, negm2), b0, b1);
+          s[c] = ex2_approx(a0);
+          s[c + 1] = ex2_approx(a1);
+          s[c + 2] = ex2_approx(b0);
+          s[c + 3] = ex2_approx(b1);
+          acc0 = f2_add(acc0, f2_pack(s[c], s[c + 1]));
+          acc1 = f2_add(acc1, f2_pack(s[c + 2], s[c + 3]));
         }
+        float sum0, sum1, sum2, sum3;
+        f2_unpack(acc0, sum0, sum1);
+        f2_unpack(acc1, sum2, sum3);
+        sum0 = (sum0 + sum1) + (sum2 + sum3);
+        sum1 = 0.f;
         l = l * alpha + (sum0 + sum1);
         m = m_new;
 #pragma unroll
@@ -401,12 +418,13 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         // S_x(j), whose completion we just observed), so O_x is stable.
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t u[32];
-            tmem_ld32(to + c * 32, u);
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t u[64];
+            tmem_ld64(to + c * 64, u);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-            tmem_st32(to + c * 32, u);
+            for (int i = 0; i < 64; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+            tmem_st32(to + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+            tmem_st32(to + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
           }
         }
         tmem_st_wait();
@@ -423,17 +441,17 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       const size_t tok = (size_t)tl.tok0 + (size_t)(valid ? i_row : 0);
       uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.o) + (tok * p.H + tl.h) * D);
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(to + c * 32, u);
-        uint32_t w[16];
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t u[64];
+        tmem_ld64(to + c * 64, u);
+        uint32_t w[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < 32; ++i)
           w[i] = pack2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l, BF16);
         if (valid) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            orow[c * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int i = 0; i < 8; ++i)
+            orow[c * 8 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
       if (valid) {
