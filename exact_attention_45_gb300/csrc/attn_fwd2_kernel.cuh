@@ -20,7 +20,10 @@
 // The final O / l and logsumexp are unchanged by this (both use the same m).
 //
 // Warps 0-3: softmax/correction/epilogue of tile A; warps 4-7: tile B (thread
-// r of a warpgroup owns row r = TMEM lane r); warp 8: TMA; warp 9: MMA.
+// r of a warpgroup owns row r = TMEM lane r); warp 8: TMA; warp 9: MMA;
+// warps 10-11 idle. The block launches at 168 registers per thread; the
+// producer warpgroup (8-11) gives registers back (72 each) and the two
+// softmax warpgroups take 208 each: 2*128*208 + 128*72 = 62464 <= 384*168.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -149,7 +152,7 @@ __device__ __forceinline__ int tile2_blocks(const Tile2& tl, int x) {
 }
 
 template <int D, int BN, int STAGES, bool CAUSAL, bool VARLEN, bool BF16>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(384, 1)
 attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using T = Pair2Traits<D, BN, STAGES>;
@@ -208,6 +211,9 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     else return tile2_fixed<CAUSAL>(p, t);
   };
 
+  if (warp >= 8) {
+    regs_dec<72>();
+  }
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -330,8 +336,9 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       mbar_wait_drain(&bars->mma_done, 0, tmo, p.err);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------- softmax / correction / epilogue
+    regs_inc<208>();
     const int x = warp >> 2;                           // 0 = tile A, 1 = tile B
     const int r = threadIdx.x & 127;                   // row within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;

@@ -45,7 +45,7 @@ cudaError_t launch_f16_pair(const CUtensorMap& q, const CUtensorMap& k, const CU
   const int smem = T::SMEM_FIXED + (VARLEN ? 4 * (p.nseq + 1) : 0);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 320, smem, stream>>>(q, k, v, p);
+  kern<<<grid, 384, smem, stream>>>(q, k, v, p);
   return cudaGetLastError();
 }
 

@@ -254,6 +254,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 #undef ATTN45_W8
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Per-warpgroup register budget changes (all four warps of a warpgroup must
+// execute the same one).
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ math
 // Packed fp32 pairs (f32x2 arithmetic, one instruction for two lanes of work).
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
