@@ -11,7 +11,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/attn45.h"
+#include "attn45.h"
 #include "attn_common.cuh"
 #include "api_internal.h"
 #include "launchers.h"
@@ -153,6 +153,19 @@ int api_device(int* sm_count, unsigned int** err) {
   if (rc) return rc;
   *sm_count = d->sm_count;
   *err = d->err;
+  return ATTN_OK;
+}
+int api_make_map_rows(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t batch,
+                      uint32_t box_inner, uint32_t box_rows) {
+  // u8 [batch][rows][inner] as {inner, rows, batch, 1}, box {box_inner, box_rows, 1, 1}
+  cuuint64_t dims[4] = {inner, rows, batch, 1};
+  cuuint64_t strides[3] = {inner, rows * inner, batch * rows * inner};
+  cuuint32_t box[4] = {box_inner, box_rows, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return ATTN_OK;
 }
 int api_make_map(CUtensorMap* m, bool u8, const void* base, uint64_t inner, uint64_t heads, uint64_t rows,

@@ -1,31 +1,175 @@
-// attn_fp8_api.cu -- C ABI of the FP8 path (pre-pass and FP8 forward).
-#include "../../include/attn45.h"
+// attn_fp8_api.cu -- C ABI of the FP8 path: pre-pass (rotation + block
+// quantisation), FP8 forward, and the two combined over a caller workspace.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+
 #include "api_internal.h"
+#include "attn45.h"
+#include "fp8_launchers.h"
+#include "fp8_prepass.h"
 
 using namespace attn45;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// SplitMix64 (Vigna): first output of the generator whose state is x.
+uint64_t splitmix64(uint64_t x) {
+  uint64_t z = x + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Fp8Layout {
+  size_t q8, k8, vt8, sq, sk, sv, total;
+};
+
+Fp8Layout fp8_layout(int B, int H, int Hkv, int N, int d, int mode) {
+  const size_t nb = (size_t)((N + 127) / 128);
+  const size_t ldv = (size_t)attn_fp8_vt_ld(N);
+  Fp8Layout L;
+  size_t off = 0;
+  L.q8 = off; off += up256((size_t)B * N * H * d);
+  L.k8 = off; off += up256((size_t)B * N * Hkv * d);
+  L.vt8 = off; off += up256((size_t)B * Hkv * d * ldv);
+  const bool blk = mode == ATTN_FP8_PER_BLOCK;
+  L.sq = off; off += up256(4 * (blk ? (size_t)B * H * nb : 1));
+  L.sk = off; off += up256(4 * (blk ? (size_t)B * Hkv * nb : 1));
+  L.sv = off; off += up256(4 * (blk ? (size_t)B * Hkv * d : 1));
+  L.total = off;
+  return L;
+}
+
+int check_shape(int B, int H, int Hkv, int N, int d, int mode) {
+  if (B < 1 || N < 1 || H < 1 || Hkv < 1 || H % Hkv != 0)
+    return api_fail(ATTN_ERR_INVALID_ARG, "need B, N, H, Hkv >= 1 and H % Hkv == 0");
+  if (d != 64 && d != 128 && d != 256) return api_fail(ATTN_ERR_UNSUPPORTED, "head dim not in {64,128,256}");
+  if (mode != ATTN_FP8_PER_TENSOR && mode != ATTN_FP8_PER_BLOCK)
+    return api_fail(ATTN_ERR_INVALID_ARG, "unknown FP8 scaling mode");
+  if ((long long)B * N * (H > Hkv ? H : Hkv) > 0x7fffffffLL || (long long)(B * (long long)H + 2LL * B * Hkv) * ((N + 127) / 128) > 0x7fffffffLL)
+    return api_fail(ATTN_ERR_INVALID_ARG, "problem too large for int32 indexing");
+  return ATTN_OK;
+}
+
+}  // namespace
 
 extern "C" {
 
 int attn_fp8_vt_ld(int N) { return N <= 0 ? 0 : ((N + 127) / 128) * 128; }
 
 size_t attn_fp8_workspace_size(int B, int H, int Hkv, int N, int d, int mode) {
-  (void)B; (void)H; (void)Hkv; (void)N; (void)d; (void)mode;
-  return 0;
+  if (check_shape(B, H, Hkv, N, d, mode)) return 0;
+  return fp8_layout(B, H, Hkv, N, d, mode).total;
 }
 
-int attn_fp8_prepass(const void*, const void*, const void*, void*, void*, void*, float*, float*, float*, int, int,
-                     int, int, int, int, int, uint64_t, void*) {
-  return api_fail(ATTN_ERR_UNSUPPORTED, "FP8 pre-pass not built yet");
+int attn_fp8_prepass(const void* q, const void* k, const void* v, void* q8, void* k8, void* vt8, float* sq,
+                     float* sk, float* sv, int B, int H, int Hkv, int N, int d, int mode, int rotate,
+                     uint64_t hadamard_seed, void* stream) {
+  int rc = check_shape(B, H, Hkv, N, d, mode);
+  if (rc) return rc;
+  if (rotate != 0 && rotate != 1) return api_fail(ATTN_ERR_INVALID_ARG, "rotate must be 0 or 1");
+  if (!q || !k || !v || !q8 || !k8 || !vt8 || !sq || !sk || !sv) return api_fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q8, 16) || !aligned(k8, 16) ||
+      !aligned(vt8, 16) || !aligned(sq, 4) || !aligned(sk, 4) || !aligned(sv, 4))
+    return api_fail(ATTN_ERR_INVALID_ARG, "tensors must be 16-byte aligned, scales 4-byte aligned");
+  int sm = 0;
+  unsigned int* err = nullptr;
+  if ((rc = api_device(&sm, &err))) return rc;
+  PrepassArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.q8 = static_cast<uint8_t*>(q8);
+  a.k8 = static_cast<uint8_t*>(k8);
+  a.vt8 = static_cast<uint8_t*>(vt8);
+  a.sq = sq;
+  a.sk = sk;
+  a.sv = sv;
+  a.B = B;
+  a.N = N;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.nblk = (N + 127) / 128;
+  a.ldv = attn_fp8_vt_ld(N);
+  a.block_mode = mode == ATTN_FP8_PER_BLOCK;
+  a.rotate = rotate;
+  a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
+  for (int c = 0; c < d; ++c)
+    if (splitmix64(hadamard_seed + (uint64_t)c) & 1ull) a.sign_bits[c >> 5] |= 1u << (c & 31);
+  cudaError_t e = launch_fp8_prepass(a, d, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return api_cuda_fail(e, "attn_fp8_prepass launch");
+  return ATTN_OK;
 }
 
-int attn_fwd_fp8(const void*, const void*, const void*, const float*, const float*, const float*, void*, float*,
-                 int, int, int, int, int, int, float, int, void*) {
-  return api_fail(ATTN_ERR_UNSUPPORTED, "FP8 forward not built yet");
+int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* sq, const float* sk,
+                 const float* sv, void* o, float* lse, int B, int H, int Hkv, int N, int d, int causal,
+                 float scale, int mode, void* stream) {
+  int rc = check_shape(B, H, Hkv, N, d, mode);
+  if (rc) return rc;
+  if (d != 128) return api_fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward is built for head dim 128");
+  if (causal != 0 && causal != 1) return api_fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return api_fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (!q8 || !k8 || !vt8 || !sq || !sk || !sv || !o || !lse) return api_fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(vt8, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(sq, 4) || !aligned(sk, 4) || !aligned(sv, 4))
+    return api_fail(ATTN_ERR_INVALID_ARG, "tensors must be 16-byte aligned, scales and lse 4-byte aligned");
+  int sm = 0;
+  unsigned int* err = nullptr;
+  if ((rc = api_device(&sm, &err))) return rc;
+  const int ldv = attn_fp8_vt_ld(N);
+  CUtensorMap mq, mk, mv;
+  if ((rc = api_make_map(&mq, true, q8, d, H, N, B, 128, 128))) return rc;
+  if ((rc = api_make_map(&mk, true, k8, d, Hkv, N, B, 128, 128))) return rc;
+  // V^T codes: [B*Hkv][d][ldv] read as boxes of (128 keys) x (d channel rows)
+  if ((rc = api_make_map_rows(&mv, vt8, ldv, d, (uint64_t)B * Hkv, 128, d))) return rc;
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.o = o;
+  p.lse = lse;
+  p.sq = sq;
+  p.sk = sk;
+  p.sv = sv;
+  p.nseq = B;
+  p.N = N;
+  p.total = B * N;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.group = H / Hkv;
+  p.vt_ld = ldv;
+  p.fp8_block = mode == ATTN_FP8_PER_BLOCK;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out_mult = 1.0f / 256.0f;
+  p.timeout_ns = api_timeout_ns();
+  p.err = err;
+  cudaError_t e = launch_fwd_fp8_d128(mq, mk, mv, p, causal != 0, sm, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return api_cuda_fail(e, "attn_fwd_fp8 launch");
+  return ATTN_OK;
 }
 
-int attn_fwd_fp8_auto(const void*, const void*, const void*, void*, float*, void*, size_t, int, int, int, int, int,
-                      int, float, int, int, uint64_t, void*) {
-  return api_fail(ATTN_ERR_UNSUPPORTED, "FP8 forward not built yet");
+int attn_fwd_fp8_auto(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                      size_t workspace_bytes, int B, int H, int Hkv, int N, int d, int causal, float scale,
+                      int mode, int rotate, uint64_t hadamard_seed, void* stream) {
+  int rc = check_shape(B, H, Hkv, N, d, mode);
+  if (rc) return rc;
+  const Fp8Layout L = fp8_layout(B, H, Hkv, N, d, mode);
+  if (!workspace || !aligned(workspace, 256)) return api_fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (workspace_bytes < L.total) return api_fail(ATTN_ERR_INVALID_ARG, "workspace smaller than attn_fp8_workspace_size()");
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  float* sq = reinterpret_cast<float*>(w + L.sq);
+  float* sk = reinterpret_cast<float*>(w + L.sk);
+  float* sv = reinterpret_cast<float*>(w + L.sv);
+  rc = attn_fp8_prepass(q, k, v, w + L.q8, w + L.k8, w + L.vt8, sq, sk, sv, B, H, Hkv, N, d, mode, rotate,
+                        hadamard_seed, stream);
+  if (rc) return rc;
+  return attn_fwd_fp8(w + L.q8, w + L.k8, w + L.vt8, sq, sk, sv, o, lse, B, H, Hkv, N, d, causal, scale, mode,
+                      stream);
 }
 
 }  // extern "C"

@@ -1,0 +1,326 @@
+// attn_fp8_prepass.cu -- FP8 (e4m3) pre-pass: incoherent processing of Q and
+// K fused with block quantisation, and per-channel quantisation of V written
+// transposed (keys contiguous) for the P V product.
+//
+// "FlashAttention-3: Fast and Accurate Attention with Asynchrony and
+// Low-precision", abstract technique (3): block quantization, and incoherent
+// processing that multiplies Q and K by a random orthogonal matrix so that
+// outlier features spread over all channels while Q K^T stays unchanged.
+// The orthogonal matrix is M = diag(sigma) H_d / sqrt(d): H_d the Sylvester
+// Hadamard matrix applied by the fast Walsh-Hadamard butterflies (spans 1, 2,
+// ..., d/2, each stage one fp32 add or subtract per element), sigma_c =
+// 1 - 2*(splitmix64(seed + c) & 1) computed on the host.
+//
+// Scales are amax / 448 (448 = largest finite e4m3), 1 for an all-zero group;
+// codes are e4m3(RNE, saturating) of x / scale with the division one IEEE
+// fp32 rounding, so results are reproducible bit for bit.
+//
+// HBM-bound: every kernel reads its bf16 input once per pass with 16-byte
+// vector loads and writes codes with coalesced 4-byte stores.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fp8_prepass.h"
+
+namespace attn45 {
+
+namespace {
+
+constexpr int ROWS = 128;        // rows per quantisation block
+constexpr int THREADS = 256;     // 8 warps x 16 rows
+constexpr int ROWS_PER_WARP = ROWS / (THREADS / 32);
+constexpr float E4M3_MAX = 448.0f;
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+__device__ __forceinline__ float scale_from_amax(float amax) {
+  return amax == 0.f ? 1.f : __fdiv_rn(amax, E4M3_MAX);
+}
+
+// Loads E = d/32 consecutive bf16 of one row for this lane.
+template <int E>
+__device__ __forceinline__ void load_row(const __nv_bfloat16* src, float (&x)[E]) {
+  if constexpr (E == 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+  } else if constexpr (E == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(src);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+  } else {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src));
+    x[0] = f.x;
+    x[1] = f.y;
+  }
+}
+
+// In-place x -> (x * sigma) H_d * fl32(1/sqrt(d)) for the row spread over a
+// warp (lane holds elements E*lane .. E*lane+E-1). Butterfly pair (i, i+h)
+// with bit h of i clear becomes (x_i + x_{i+h}, x_i - x_{i+h}).
+template <int E>
+__device__ __forceinline__ void rotate_row(float (&x)[E], uint32_t sign_bits_lane, float inv_sqrt_d, int lane) {
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if ((sign_bits_lane >> e) & 1u) x[e] = -x[e];
+  // spans inside the lane
+#pragma unroll
+  for (int h = 1; h < E; h <<= 1) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if ((e & h) == 0) {
+        const float a = x[e], b = x[e + h];
+        x[e] = __fadd_rn(a, b);
+        x[e + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+  // spans across lanes: partner lane holds element i ^ h at the same slot
+#pragma unroll
+  for (int hl = 1; hl < 32; hl <<= 1) {
+    const bool upper = (lane & hl) != 0;   // this lane holds the i + h side
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float other = __shfl_xor_sync(0xffffffffu, x[e], hl);
+      x[e] = upper ? __fsub_rn(other, x[e]) : __fadd_rn(x[e], other);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) x[e] = __fmul_rn(x[e], inv_sqrt_d);
+}
+
+template <int E>
+__device__ __forceinline__ void store_codes(uint8_t* dst, const float (&x)[E], float s) {
+  float y[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) y[e] = __fdiv_rn(x[e], s);
+  if constexpr (E == 8) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(e4m3x4(y[0], y[1], y[2], y[3]), e4m3x4(y[4], y[5], y[6], y[7]));
+  } else if constexpr (E == 4) {
+    *reinterpret_cast<uint32_t*>(dst) = e4m3x4(y[0], y[1], y[2], y[3]);
+  } else {
+    uint16_t c;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(y[1]), "f"(y[0]));
+    *reinterpret_cast<uint16_t*>(dst) = c;
+  }
+}
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  const int warp = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[warp] = v;
+  __syncthreads();
+  float m = red[0];
+#pragma unroll
+  for (int w = 1; w < THREADS / 32; ++w) m = fmaxf(m, red[w]);
+  return m;
+}
+
+// Q or K row block: rows [blk*128, blk*128+128) of (b, head).
+// phase 0, block mode : rotate, block amax -> scale, codes, scale written.
+// phase 0, tensor mode: rotate, block amax -> atomicMax into amax_out[0].
+// phase 1, tensor mode: rotate, codes with the tensor amax in amax_out[0].
+template <int E>
+__device__ void qk_block(const PrepassArgs& a, bool is_q, int b, int head, int blk, int phase) {
+  __shared__ float red[THREADS / 32];
+  const int Hx = is_q ? a.H : a.Hkv;
+  const __nv_bfloat16* src = is_q ? a.q : a.k;
+  uint8_t* dst = is_q ? a.q8 : a.k8;
+  float* sc = is_q ? a.sq : a.sk;
+  const int d = E * 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sign_lane = (a.sign_bits[(E * lane) >> 5] >> ((E * lane) & 31)) & ((1u << E) - 1u);
+  float x[ROWS_PER_WARP][E];
+  float amax = 0.f;
+#pragma unroll
+  for (int rr = 0; rr < ROWS_PER_WARP; ++rr) {
+    const int n = blk * ROWS + warp * ROWS_PER_WARP + rr;
+    if (n < a.N) {
+      const size_t row = ((size_t)b * a.N + n) * Hx + head;
+      load_row<E>(src + row * d + E * lane, x[rr]);
+      if (a.rotate) rotate_row<E>(x[rr], sign_lane, a.inv_sqrt_d, lane);
+#pragma unroll
+      for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[rr][e]));
+    }
+  }
+  float s;
+  if (a.block_mode) {
+    amax = block_max(amax, red);
+    s = scale_from_amax(amax);
+    if (threadIdx.x == 0) sc[((size_t)b * Hx + head) * a.nblk + blk] = s;
+  } else if (phase == 0) {
+    amax = block_max(amax, red);
+    if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(sc), __float_as_uint(amax));
+    return;
+  } else {
+    s = scale_from_amax(__uint_as_float(*reinterpret_cast<volatile unsigned int*>(sc)));
+  }
+#pragma unroll
+  for (int rr = 0; rr < ROWS_PER_WARP; ++rr) {
+    const int n = blk * ROWS + warp * ROWS_PER_WARP + rr;
+    if (n < a.N) {
+      const size_t row = ((size_t)b * a.N + n) * Hx + head;
+      store_codes<E>(dst + row * d + E * lane, x[rr], s);
+    }
+  }
+}
+
+// V row block of (b, kv head). phase 0: per-channel (block mode) or whole
+// tensor amax -> atomicMax into sv. phase 1: codes with those amax values,
+// written transposed into vt8[b][head][c][n] through shared memory.
+template <int E>
+__device__ void v_block(const PrepassArgs& a, int b, int head, int blk, int phase) {
+  constexpr int D = E * 32;
+  constexpr int TP = ROWS + 4;                      // padded row of the transposed tile
+  __shared__ __align__(16) uint8_t tile[D * TP];
+  __shared__ float red[THREADS / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float x[ROWS_PER_WARP][E];
+  float amax_c[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) amax_c[e] = 0.f;
+#pragma unroll
+  for (int rr = 0; rr < ROWS_PER_WARP; ++rr) {
+    const int n = blk * ROWS + warp * ROWS_PER_WARP + rr;
+    if (n < a.N) {
+      const size_t row = ((size_t)b * a.N + n) * a.Hkv + head;
+      load_row<E>(a.v + row * D + E * lane, x[rr]);
+#pragma unroll
+      for (int e = 0; e < E; ++e) amax_c[e] = fmaxf(amax_c[e], fabsf(x[rr][e]));
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[rr][e] = 0.f;
+    }
+  }
+  float* sv = a.sv;
+  if (phase == 0) {
+    if (a.block_mode) {
+      // per channel: reduce over the 8 warps through shared memory
+      __shared__ float part[THREADS / 32][D];
+#pragma unroll
+      for (int e = 0; e < E; ++e) part[warp][E * lane + e] = amax_c[e];
+      __syncthreads();
+      if (threadIdx.x < D) {
+        float m = part[0][threadIdx.x];
+#pragma unroll
+        for (int w = 1; w < THREADS / 32; ++w) m = fmaxf(m, part[w][threadIdx.x]);
+        atomicMax(reinterpret_cast<unsigned int*>(sv + ((size_t)b * a.Hkv + head) * D + threadIdx.x),
+                  __float_as_uint(m));
+      }
+    } else {
+      float m = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) m = fmaxf(m, amax_c[e]);
+      m = block_max(m, red);
+      if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(sv), __float_as_uint(m));
+    }
+    return;
+  }
+  float s[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const unsigned int bits = a.block_mode
+        ? *reinterpret_cast<volatile unsigned int*>(sv + ((size_t)b * a.Hkv + head) * D + E * lane + e)
+        : *reinterpret_cast<volatile unsigned int*>(sv);
+    s[e] = scale_from_amax(__uint_as_float(bits));
+  }
+  // codes into the transposed tile: tile[c][n_local]
+#pragma unroll
+  for (int rr = 0; rr < ROWS_PER_WARP; ++rr) {
+    const int nl = warp * ROWS_PER_WARP + rr;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      uint16_t c2;
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+          : "=h"(c2)
+          : "f"(__fdiv_rn(x[rr][e + 1], s[e + 1])), "f"(__fdiv_rn(x[rr][e], s[e])));
+      tile[(E * lane + e) * TP + nl] = (uint8_t)(c2 & 0xFF);
+      tile[(E * lane + e + 1) * TP + nl] = (uint8_t)(c2 >> 8);
+    }
+  }
+  __syncthreads();
+  // rows of vt8: 128 keys = 32 lanes x 4 bytes; pad keys (n >= N) hold code 0
+  const size_t base = ((size_t)b * a.Hkv + head) * D;
+  for (int c = warp; c < D; c += THREADS / 32) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[c * TP + 4 * lane]);
+    *reinterpret_cast<uint32_t*>(a.vt8 + (base + c) * a.ldv + (size_t)blk * ROWS + 4 * lane) = w;
+  }
+}
+
+template <int E>
+__global__ void __launch_bounds__(THREADS) prepass_kernel(const PrepassArgs a, int phase) {
+  // blocks: [Q blocks][K blocks][V blocks], each B * heads * nblk
+  int id = blockIdx.x;
+  const int nq = a.B * a.H * a.nblk, nk = a.B * a.Hkv * a.nblk;
+  if (id < nq) {
+    if (phase == 1 && a.block_mode) return;   // Q done in phase 0
+    const int blk = id % a.nblk, bh = id / a.nblk;
+    qk_block<E>(a, true, bh / a.H, bh % a.H, blk, phase);
+    return;
+  }
+  id -= nq;
+  if (id < nk) {
+    if (phase == 1 && a.block_mode) return;
+    const int blk = id % a.nblk, bh = id / a.nblk;
+    qk_block<E>(a, false, bh / a.Hkv, bh % a.Hkv, blk, phase);
+    return;
+  }
+  id -= nk;
+  const int blk = id % a.nblk, bh = id / a.nblk;
+  v_block<E>(a, bh / a.Hkv, bh % a.Hkv, blk, phase);
+}
+
+// Turns the amax values left in the scale outputs into scales.
+__global__ void finalize_kernel(float* sq, float* sk, float* sv, int nsv, int tensor_mode) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < nsv) sv[i] = scale_from_amax(sv[i]);
+  if (tensor_mode && i == 0) {
+    sq[0] = scale_from_amax(sq[0]);
+    sk[0] = scale_from_amax(sk[0]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, cudaStream_t s) {
+  const size_t nsv = a.block_mode ? (size_t)a.B * a.Hkv * d : 1;
+  cudaError_t e = cudaMemsetAsync(a.sv, 0, nsv * sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  if (!a.block_mode) {
+    if ((e = cudaMemsetAsync(a.sq, 0, sizeof(float), s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(a.sk, 0, sizeof(float), s)) != cudaSuccess) return e;
+  }
+  const int blocks = (a.B * a.H + 2 * a.B * a.Hkv) * a.nblk;
+  for (int phase = 0; phase < 2; ++phase) {
+    switch (d) {
+      case 64: prepass_kernel<2><<<blocks, THREADS, 0, s>>>(a, phase); break;
+      case 128: prepass_kernel<4><<<blocks, THREADS, 0, s>>>(a, phase); break;
+      default: prepass_kernel<8><<<blocks, THREADS, 0, s>>>(a, phase); break;
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  finalize_kernel<<<(int)((nsv + 255) / 256), 256, 0, s>>>(a.sq, a.sk, a.sv, (int)nsv, a.block_mode ? 0 : 1);
+  return cudaGetLastError();
+}
+
+}  // namespace attn45

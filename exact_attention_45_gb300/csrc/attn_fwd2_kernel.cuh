@@ -36,13 +36,16 @@ namespace attn45 {
 constexpr int SUPER_M = 2 * BLOCK_M;          // query rows per CTA work unit
 constexpr float LAZY_RESCALE_LOG2 = 8.0f;     // raise m only past this margin
 
-template <int D, int BN, int STAGES>
+// Element kinds of the two-tile kernel.
+enum : int { KIND_FP16 = 0, KIND_BF16 = 1, KIND_E4M3 = 2 };
+
+template <int D, int BN, int STAGES, int ELEM = 2>
 struct Pair2Traits {
-  static constexpr int NC = D / 64;
+  static constexpr int NC = D * ELEM / 128;              // 128-byte chunks per Q/K row
   static constexpr int Q_CHUNK = BLOCK_M * 128;
   static constexpr int KV_CHUNK = BN * 128;
-  static constexpr int Q_BYTES = BLOCK_M * D * 2;
-  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int Q_BYTES = BLOCK_M * D * ELEM;
+  static constexpr int KV_BYTES = BN * D * ELEM;          // one K block, or one V (V^T) block
   static constexpr int OFF_Q = 0;                        // Q_A then Q_B
   static constexpr int OFF_K = 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
@@ -151,11 +154,27 @@ __device__ __forceinline__ int tile2_blocks(const Tile2& tl, int x) {
   return ceil_div(kend, BN);
 }
 
-template <int D, int BN, int STAGES, bool CAUSAL, bool VARLEN, bool BF16>
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// KIND_BF16 / KIND_FP16: Q, K, V in that type, V tiles MN-major (rows of
+// keys). KIND_E4M3: e4m3 codes with scales (FP8 path): S = Q8 K8^T is
+// dequantised by the per-block scalar sq * sk folded into the softmax scale,
+// P is multiplied by 256 and rounded to e4m3 for O += P V^T with V given
+// transposed (rows of channels, K-major), and the epilogue applies the V
+// channel scale and 1/256.
+template <int D, int BN, int STAGES, bool CAUSAL, bool VARLEN, int KIND>
 __global__ void __launch_bounds__(384, 1)
-attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using T = Pair2Traits<D, BN, STAGES>;
+attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  constexpr bool FP8 = KIND == KIND_E4M3;
+  constexpr bool BF16 = KIND == KIND_BF16;
+  constexpr int ELEM = FP8 ? 1 : 2;
+  using T = Pair2Traits<D, BN, STAGES, ELEM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sQ = smem + T::OFF_Q;
@@ -230,7 +249,7 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         for (int x = 0; x < 2; ++x)
 #pragma unroll
           for (int c = 0; c < T::NC; ++c)
-            tma_load_4d(&tmQ, &bars->q_full, sQ + x * T::Q_BYTES + c * T::Q_CHUNK, c * 64, tl.h,
+            tma_load_4d(&tmQ, &bars->q_full, sQ + x * T::Q_BYTES + c * T::Q_CHUNK, c * (128 / ELEM), tl.h,
                         tl.tma_row0 + tl.sblk * SUPER_M + x * BLOCK_M, tl.tma_b);
         for (int j = 0; j < nkv; ++j, ++kv_it) {
           const int st = kv_it % STAGES;
@@ -241,15 +260,20 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           mbar_expect_tx(&bars->k_full[st], T::KV_BYTES);
 #pragma unroll
           for (int c = 0; c < T::NC; ++c)
-            tma_load_4d(&tmK, &bars->k_full[st], sK + st * T::KV_BYTES + c * T::KV_CHUNK, c * 64, hk, krow,
-                        tl.tma_b);
+            tma_load_4d(&tmK, &bars->k_full[st], sK + st * T::KV_BYTES + c * T::KV_CHUNK, c * (128 / ELEM), hk,
+                        krow, tl.tma_b);
           ok = mbar_wait(&bars->v_empty[st], ph ^ 1, tmo, abort_flag, p.err);
           if (!ok) { ++kv_it; break; }
           mbar_expect_tx(&bars->v_full[st], T::KV_BYTES);
+          if constexpr (FP8) {
+            // V^T block: 128 keys x D channel rows of (batch, kv head)
+            tma_load_4d(&tmV, &bars->v_full[st], sV + st * T::KV_BYTES, j * BN, 0, tl.seq * p.Hkv + hk, 0);
+          } else {
 #pragma unroll
-          for (int c = 0; c < T::NC; ++c)
-            tma_load_4d(&tmV, &bars->v_full[st], sV + st * T::KV_BYTES + c * T::KV_CHUNK, c * 64, hk, krow,
-                        tl.tma_b);
+            for (int c = 0; c < T::NC; ++c)
+              tma_load_4d(&tmV, &bars->v_full[st], sV + st * T::KV_BYTES + c * T::KV_CHUNK, c * 64, hk, krow,
+                          tl.tma_b);
+          }
         }
       }
       const int last = kv_it;
@@ -264,8 +288,10 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_kind_f16(BLOCK_M, BN, BF16, false);
-      constexpr uint32_t idesc_o = idesc_kind_f16(BLOCK_M, D, BF16, true);
+      constexpr uint32_t idesc_s = FP8 ? idesc_kind_f8_e4m3(BLOCK_M, BN) : idesc_kind_f16(BLOCK_M, BN, BF16, false);
+      constexpr uint32_t idesc_o = FP8 ? idesc_kind_f8_e4m3(BLOCK_M, D) : idesc_kind_f16(BLOCK_M, D, BF16, true);
+      constexpr int PV_STEPS = BN * ELEM / 32;               // 32-byte K steps of P V
+      constexpr int S_STEPS = D * ELEM / 32;                 // 32-byte K steps of Q K^T
       const uint32_t qa = smem_u32(sQ);
       const uint32_t ka = smem_u32(sK);
       const uint32_t va = smem_u32(sV);
@@ -298,9 +324,16 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
               const uint32_t a_tmem = tmem + T::TMEM_S + x * BN;
               const uint32_t vbase = va + pst * T::KV_BYTES;
 #pragma unroll
-              for (int k = 0; k < BN / 16; ++k)
-                umma_f16_ts(tmem + T::TMEM_O + x * D, a_tmem + k * 8,
-                            sdesc_mnmajor_sw128(vbase + k * 2048, T::KV_CHUNK), idesc_o, (j > 1 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < PV_STEPS; ++k) {
+                // each K step is 8 TMEM columns of P (16 x 16-bit or 32 x 8-bit)
+                if constexpr (FP8)
+                  umma_f8_ts(tmem + T::TMEM_O + x * D, a_tmem + k * 8, sdesc_kmajor_sw128(vbase + k * 32), idesc_o,
+                             (j > 1 || k > 0) ? 1u : 0u);
+                else
+                  umma_f16_ts(tmem + T::TMEM_O + x * D, a_tmem + k * 8,
+                              sdesc_mnmajor_sw128(vbase + k * 2048, T::KV_CHUNK), idesc_o,
+                              (j > 1 || k > 0) ? 1u : 0u);
+              }
               umma_commit(&bars->o_done[x]);
             }
             // S_x(j) = Q_x K_j^T
@@ -314,11 +347,15 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
               const uint32_t qx = qa + x * T::Q_BYTES;
               const uint32_t kb = ka + st * T::KV_BYTES;
 #pragma unroll
-              for (int k = 0; k < D / 16; ++k) {
+              for (int k = 0; k < S_STEPS; ++k) {
                 const uint32_t qo = (k >> 2) * T::Q_CHUNK + (k & 3) * 32;
                 const uint32_t ko = (k >> 2) * T::KV_CHUNK + (k & 3) * 32;
-                umma_f16_ss(tmem + T::TMEM_S + x * BN, sdesc_kmajor_sw128(qx + qo), sdesc_kmajor_sw128(kb + ko),
-                            idesc_s, k > 0 ? 1u : 0u);
+                if constexpr (FP8)
+                  umma_f8_ss(tmem + T::TMEM_S + x * BN, sdesc_kmajor_sw128(qx + qo), sdesc_kmajor_sw128(kb + ko),
+                             idesc_s, k > 0 ? 1u : 0u);
+                else
+                  umma_f16_ss(tmem + T::TMEM_S + x * BN, sdesc_kmajor_sw128(qx + qo), sdesc_kmajor_sw128(kb + ko),
+                              idesc_s, k > 0 ? 1u : 0u);
               }
               umma_commit(&bars->s_full[x]);
             }
@@ -344,7 +381,9 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t ts = tmem + lane_off + T::TMEM_S + x * BN;
     const uint32_t to = tmem + lane_off + T::TMEM_O + x * D;
-    const float sl2 = p.scale_log2;
+    // raise m only past this margin (FP8: P * 256 must stay <= 448, so m
+    // follows the block maxima exactly)
+    constexpr float lazy = FP8 ? 0.f : LAZY_RESCALE_LOG2;
     int s_cnt = 0, pv_total = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
@@ -353,8 +392,16 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       if (nblk == 0) continue;                        // tile B past the sequence end
       const int row0 = tl.sblk * SUPER_M + x * BLOCK_M;  // first row of this tile
       const int i_row = row0 + r;
+      const int hk = tl.h / p.group;
+      const int nb128 = ceil_div(tl.n, BLOCK_M);      // 128-row scale blocks (FP8)
+      float sq_x = 1.f;
+      if constexpr (FP8)
+        sq_x = p.fp8_block ? __ldg(p.sq + ((size_t)tl.seq * p.H + tl.h) * nb128 + (row0 >> 7)) : __ldg(p.sq);
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nblk; ++j) {
+        float sl2 = p.scale_log2;
+        if constexpr (FP8)
+          sl2 *= sq_x * (p.fp8_block ? __ldg(p.sk + ((size_t)tl.seq * p.Hkv + hk) * nb128 + j) : __ldg(p.sk));
         ok = mbar_wait(&bars->s_full[x], s_cnt & 1, tmo, abort_flag, p.err);
         ++s_cnt;
         if (!ok) break;
@@ -386,7 +433,7 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         const float mx = fmaxf(fmaxf(mxa, mxb), fmaxf(mxc, mxd)) * sl2;
         // raise the running max only when it moved by more than 2^8
-        const bool raise = mx > m + LAZY_RESCALE_LOG2;
+        const bool raise = mx > m + lazy;
         const float m_new = raise ? mx : m;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = raise ? ex2_approx(m - m_use) : 1.f;
@@ -414,12 +461,22 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         sum1 = 0.f;
         l = l * alpha + (sum0 + sum1);
         m = m_new;
-#pragma unroll
-        for (int c = 0; c < BN / 64; ++c) {
+        if constexpr (FP8) {
+          // P * 256 as e4m3, four per TMEM column
+          static_assert(BN == 128, "P tile is one 32-column store");
           uint32_t u[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = pack2(s[c * 64 + 2 * i], s[c * 64 + 2 * i + 1], BF16);
-          tmem_st32(ts + c * 32, u);
+          for (int i = 0; i < 32; ++i)
+            u[i] = pack_e4m3x4(s[4 * i] * 256.f, s[4 * i + 1] * 256.f, s[4 * i + 2] * 256.f, s[4 * i + 3] * 256.f);
+          tmem_st32(ts, u);
+        } else {
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c) {
+            uint32_t u[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = pack2(s[c * 64 + 2 * i], s[c * 64 + 2 * i + 1], BF16);
+            tmem_st32(ts + c * 32, u);
+          }
         }
         // correction: O_x += P(j-1) V has completed (it was issued before
         // S_x(j), whose completion we just observed), so O_x is stable.
@@ -444,17 +501,29 @@ attn_fwd2_f16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       if (!ok) break;
       tc_fence_after();
       const bool valid = i_row < tl.n;
-      const float inv_l = 1.f / l;
+      const float inv_l = FP8 ? p.out_mult / l : 1.f / l;
       const size_t tok = (size_t)tl.tok0 + (size_t)(valid ? i_row : 0);
       uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.o) + (tok * p.H + tl.h) * D);
+      const float* svp = FP8 ? (p.fp8_block ? p.sv + ((size_t)tl.seq * p.Hkv + hk) * D : p.sv) : nullptr;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t u[64];
         tmem_ld64(to + c * 64, u);
         uint32_t w[32];
+        if constexpr (FP8) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          w[i] = pack2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l, BF16);
+          for (int i = 0; i < 32; ++i) {
+            const int ch = c * 64 + 2 * i;
+            const float s0 = p.fp8_block ? __ldg(svp + ch) : __ldg(svp);
+            const float s1 = p.fp8_block ? __ldg(svp + ch + 1) : s0;
+            w[i] = pack2(__uint_as_float(u[2 * i]) * (s0 * inv_l), __uint_as_float(u[2 * i + 1]) * (s1 * inv_l),
+                         true);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            w[i] = pack2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l, BF16);
+        }
         if (valid) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)

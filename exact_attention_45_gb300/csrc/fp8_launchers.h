@@ -1,0 +1,12 @@
+// fp8_launchers.h -- host entry of the FP8 forward kernel (head dim 128).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include "attn_common.cuh"
+
+namespace attn45 {
+// q, k: e4m3 maps {d, heads, N, B} with 128 x 128-byte boxes; v: V^T map
+// {ldv, d, B*Hkv, 1} with 128-key x d-row boxes.
+cudaError_t launch_fwd_fp8_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                const FwdParams& p, bool causal, int sm_count, cudaStream_t s);
+}  // namespace attn45

@@ -35,12 +35,12 @@ cudaError_t launch_f16_single(const CUtensorMap& q, const CUtensorMap& k, const 
 }
 
 // Two 128-row query tiles per CTA (head dims 64 and 128).
-template <int D, int BN, int ST, bool CAUSAL, bool VARLEN, bool BF16>
-cudaError_t launch_f16_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, FwdParams p,
-                            int sm_count, cudaStream_t stream) {
+template <int D, int BN, int ST, bool CAUSAL, bool VARLEN, int KIND>
+cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, FwdParams p,
+                        int sm_count, cudaStream_t stream) {
   static_assert(BN == f16_block_n(D), "tensor-map box height and kernel BN must agree");
-  using T = Pair2Traits<D, BN, ST>;
-  auto kern = attn_fwd2_f16_kernel<D, BN, ST, CAUSAL, VARLEN, BF16>;
+  using T = Pair2Traits<D, BN, ST, KIND == KIND_E4M3 ? 1 : 2>;
+  auto kern = attn_fwd2_kernel<D, BN, ST, CAUSAL, VARLEN, KIND>;
   const int grid = persistent_grid(p, VARLEN, SUPER_M, sm_count, &p.ntiles);
   const int smem = T::SMEM_FIXED + (VARLEN ? 4 * (p.nseq + 1) : 0);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -52,7 +52,7 @@ cudaError_t launch_f16_pair(const CUtensorMap& q, const CUtensorMap& k, const CU
 template <int D, int BN, int ST, bool PAIR, bool CA, bool VL, bool BF>
 cudaError_t launch_f16_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p,
                            int sm_count, cudaStream_t s) {
-  if constexpr (PAIR) return launch_f16_pair<D, BN, ST, CA, VL, BF>(q, k, v, p, sm_count, s);
+  if constexpr (PAIR) return launch_pair<D, BN, ST, CA, VL, BF ? KIND_BF16 : KIND_FP16>(q, k, v, p, sm_count, s);
   else return launch_f16_single<D, BN, ST, CA, VL, BF>(q, k, v, p, sm_count, s);
 }
 
