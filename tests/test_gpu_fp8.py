@@ -62,8 +62,13 @@ def _emulated_check(B, N, H, Hkv, causal, mode, rotate, seed, rows=None):
         l_g = l_h[rows[0], rows[1], rows[2]]
     err = o_g - o_ref
     assert np.isfinite(o_h).all()
-    # bf16 output rounding plus rare e4m3 rounding flips of P (GPU fp32 vs fp64)
-    assert np.abs(err).max() <= 2e-2 and np.sqrt((err ** 2).mean()) <= 2e-3, (np.abs(err).max(), np.sqrt((err ** 2).mean()))
+    # bf16 output rounding (relative, up to 2^-9 |O|; outlier V makes |O| large)
+    # plus rare e4m3 rounding flips of P where the GPU's fp32 scores and the
+    # oracle's fp64 scores straddle a rounding boundary
+    bound = 1e-2 + 4e-3 * np.abs(o_ref)
+    worst = float((np.abs(err) / bound).max())
+    rms = float(np.sqrt((err ** 2).mean()))
+    assert worst <= 1.0 and rms <= 2e-3, (worst, rms)
     assert np.abs(l_g - l_ref).max() <= 2e-3
 
 
