@@ -59,9 +59,11 @@ struct Pair2Traits {
   static_assert(2 * BN + 2 * D <= TMEM_COLS, "TMEM budget");
 };
 
+// Ring slot j of a super tile holds K_j and V_{j-1} (slots 0..nkv), so each
+// key block costs one full and one empty barrier.
 struct Bars2 {
-  uint64_t q_full, q_empty;
-  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t q_full, q_empty;                 // q_empty: one arrival per MMA warp
+  uint64_t slot_full[4], slot_empty[4];     // slot_empty: one arrival per MMA warp
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -189,19 +191,17 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->q_empty, 2);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->slot_full[s], 1);
+      mbar_init(&bars->slot_empty[s], 2);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars->s_full[x], 1);
       mbar_init(&bars->p_full[x], 128);
       mbar_init(&bars->o_done[x], 1);
     }
-    mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->mma_done, 2);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -236,7 +236,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int kv_it = 0, tile_i = 0;
+      int slot_it = 0, tile_i = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tile_i) {
         const Tile2 tl = get_tile(t);
@@ -251,122 +251,100 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           for (int c = 0; c < T::NC; ++c)
             tma_load_4d(&tmQ, &bars->q_full, sQ + x * T::Q_BYTES + c * T::Q_CHUNK, c * (128 / ELEM), tl.h,
                         tl.tma_row0 + tl.sblk * SUPER_M + x * BLOCK_M, tl.tma_b);
-        for (int j = 0; j < nkv; ++j, ++kv_it) {
-          const int st = kv_it % STAGES;
-          const uint32_t ph = (kv_it / STAGES) & 1;
-          const int krow = tl.tma_row0 + j * BN;
-          ok = mbar_wait(&bars->k_empty[st], ph ^ 1, tmo, abort_flag, p.err);
+        // slot j: K_j (j < nkv) and V_{j-1} (j >= 1)
+        for (int j = 0; j <= nkv; ++j, ++slot_it) {
+          const int st = slot_it % STAGES;
+          ok = mbar_wait(&bars->slot_empty[st], ((slot_it / STAGES) & 1) ^ 1, tmo, abort_flag, p.err);
           if (!ok) break;
-          mbar_expect_tx(&bars->k_full[st], T::KV_BYTES);
-#pragma unroll
-          for (int c = 0; c < T::NC; ++c)
-            tma_load_4d(&tmK, &bars->k_full[st], sK + st * T::KV_BYTES + c * T::KV_CHUNK, c * (128 / ELEM), hk,
-                        krow, tl.tma_b);
-          ok = mbar_wait(&bars->v_empty[st], ph ^ 1, tmo, abort_flag, p.err);
-          if (!ok) { ++kv_it; break; }
-          mbar_expect_tx(&bars->v_full[st], T::KV_BYTES);
-          if constexpr (FP8) {
-            // V^T block: 128 keys x D channel rows of (batch, kv head)
-            tma_load_4d(&tmV, &bars->v_full[st], sV + st * T::KV_BYTES, j * BN, 0, tl.seq * p.Hkv + hk, 0);
-          } else {
+          mbar_expect_tx(&bars->slot_full[st], (j < nkv ? T::KV_BYTES : 0) + (j >= 1 ? T::KV_BYTES : 0));
+          if (j < nkv) {
 #pragma unroll
             for (int c = 0; c < T::NC; ++c)
-              tma_load_4d(&tmV, &bars->v_full[st], sV + st * T::KV_BYTES + c * T::KV_CHUNK, c * 64, hk, krow,
-                          tl.tma_b);
+              tma_load_4d(&tmK, &bars->slot_full[st], sK + st * T::KV_BYTES + c * T::KV_CHUNK, c * (128 / ELEM),
+                          hk, tl.tma_row0 + j * BN, tl.tma_b);
+          }
+          if (j >= 1) {
+            if constexpr (FP8) {
+              // V^T block: 128 keys x D channel rows of (batch, kv head)
+              tma_load_4d(&tmV, &bars->slot_full[st], sV + st * T::KV_BYTES, (j - 1) * BN, 0, tl.seq * p.Hkv + hk, 0);
+            } else {
+#pragma unroll
+              for (int c = 0; c < T::NC; ++c)
+                tma_load_4d(&tmV, &bars->slot_full[st], sV + st * T::KV_BYTES + c * T::KV_CHUNK, c * 64, hk,
+                            tl.tma_row0 + (j - 1) * BN, tl.tma_b);
+            }
           }
         }
       }
-      const int last = kv_it;
-      for (int it = (last > STAGES ? last - STAGES : 0); it < last; ++it) {
-        const int st = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        mbar_wait_drain(&bars->k_full[st], ph, tmo, p.err);
-        mbar_wait_drain(&bars->v_full[st], ph, tmo, p.err);
-      }
+      // never leave with copies in flight
+      for (int it = (slot_it > STAGES ? slot_it - STAGES : 0); it < slot_it; ++it)
+        mbar_wait_drain(&bars->slot_full[it % STAGES], (it / STAGES) & 1, tmo, p.err);
       if (tile_i > 0) mbar_wait_drain(&bars->q_full, (tile_i - 1) & 1, tmo, p.err);
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------- MMA issuers, one per tile
+    // Each warp's lane 0 issues its tile's GEMMs in order O_x += P_x(j-1) V,
+    // S_x(j) = Q_x K_j^T; the two tiles' chains are independent, so while one
+    // waits for its softmax the other keeps the tensor core busy.
     if (lane == 0) {
+      const int x = warp - 9;
       constexpr uint32_t idesc_s = FP8 ? idesc_kind_f8_e4m3(BLOCK_M, BN) : idesc_kind_f16(BLOCK_M, BN, BF16, false);
       constexpr uint32_t idesc_o = FP8 ? idesc_kind_f8_e4m3(BLOCK_M, D) : idesc_kind_f16(BLOCK_M, D, BF16, true);
       constexpr int PV_STEPS = BN * ELEM / 32;               // 32-byte K steps of P V
       constexpr int S_STEPS = D * ELEM / 32;                 // 32-byte K steps of Q K^T
-      const uint32_t qa = smem_u32(sQ);
+      const uint32_t qx = smem_u32(sQ) + x * T::Q_BYTES;
       const uint32_t ka = smem_u32(sK);
       const uint32_t va = smem_u32(sV);
-      int kv_it = 0, tile_i = 0;
-      int p_cnt[2] = {0, 0};
+      const uint32_t s_tmem = tmem + T::TMEM_S + x * BN;
+      const uint32_t o_tmem = tmem + T::TMEM_O + x * D;
+      int slot_it = 0, tile_i = 0, p_cnt = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tile_i) {
         const Tile2 tl = get_tile(t);
-        const int nblk[2] = {tile2_blocks<CAUSAL, BN>(tl, 0), tile2_blocks<CAUSAL, BN>(tl, 1)};
-        const int nkv = max(nblk[0], nblk[1]);
+        const int nx = tile2_blocks<CAUSAL, BN>(tl, x);
+        const int nkv = max(tile2_blocks<CAUSAL, BN>(tl, 0), tile2_blocks<CAUSAL, BN>(tl, 1));
         ok = mbar_wait(&bars->q_full, tile_i & 1, tmo, abort_flag, p.err);
         if (!ok) break;
-        for (int j = 0; j <= nkv && ok; ++j) {
-          const int st = kv_it % STAGES;               // stage of block j
-          const int pst = (kv_it + STAGES - 1) % STAGES;  // stage of block j-1
-          bool v_ready = false, k_ready = false;
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            // O_x += P_x(j-1) V_{j-1}
-            if (j >= 1 && j - 1 < nblk[x]) {
-              ok = mbar_wait(&bars->p_full[x], p_cnt[x] & 1, tmo, abort_flag, p.err);
-              if (!ok) break;
-              ++p_cnt[x];
-              if (!v_ready) {
-                ok = mbar_wait(&bars->v_full[pst], ((kv_it - 1) / STAGES) & 1, tmo, abort_flag, p.err);
-                if (!ok) break;
-                v_ready = true;
-              }
-              tc_fence_after();
-              const uint32_t a_tmem = tmem + T::TMEM_S + x * BN;
-              const uint32_t vbase = va + pst * T::KV_BYTES;
-#pragma unroll
-              for (int k = 0; k < PV_STEPS; ++k) {
-                // each K step is 8 TMEM columns of P (16 x 16-bit or 32 x 8-bit)
-                if constexpr (FP8)
-                  umma_f8_ts(tmem + T::TMEM_O + x * D, a_tmem + k * 8, sdesc_kmajor_sw128(vbase + k * 32), idesc_o,
-                             (j > 1 || k > 0) ? 1u : 0u);
-                else
-                  umma_f16_ts(tmem + T::TMEM_O + x * D, a_tmem + k * 8,
-                              sdesc_mnmajor_sw128(vbase + k * 2048, T::KV_CHUNK), idesc_o,
-                              (j > 1 || k > 0) ? 1u : 0u);
-              }
-              umma_commit(&bars->o_done[x]);
-            }
-            // S_x(j) = Q_x K_j^T
-            if (j < nblk[x]) {
-              if (!k_ready) {
-                ok = mbar_wait(&bars->k_full[st], (kv_it / STAGES) & 1, tmo, abort_flag, p.err);
-                if (!ok) break;
-                k_ready = true;
-                tc_fence_after();
-              }
-              const uint32_t qx = qa + x * T::Q_BYTES;
-              const uint32_t kb = ka + st * T::KV_BYTES;
-#pragma unroll
-              for (int k = 0; k < S_STEPS; ++k) {
-                const uint32_t qo = (k >> 2) * T::Q_CHUNK + (k & 3) * 32;
-                const uint32_t ko = (k >> 2) * T::KV_CHUNK + (k & 3) * 32;
-                if constexpr (FP8)
-                  umma_f8_ss(tmem + T::TMEM_S + x * BN, sdesc_kmajor_sw128(qx + qo), sdesc_kmajor_sw128(kb + ko),
-                             idesc_s, k > 0 ? 1u : 0u);
-                else
-                  umma_f16_ss(tmem + T::TMEM_S + x * BN, sdesc_kmajor_sw128(qx + qo), sdesc_kmajor_sw128(kb + ko),
-                              idesc_s, k > 0 ? 1u : 0u);
-              }
-              umma_commit(&bars->s_full[x]);
-            }
-          }
+        for (int j = 0; j <= nkv; ++j, ++slot_it) {
+          const int st = slot_it % STAGES;
+          ok = mbar_wait(&bars->slot_full[st], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);
           if (!ok) break;
-          if (j >= 1) umma_commit(&bars->v_empty[pst]);
-          if (j < nkv) {
-            umma_commit(&bars->k_empty[st]);
-            if (j == nkv - 1) umma_commit(&bars->q_empty);
-            ++kv_it;
+          if (j >= 1 && j - 1 < nx) {
+            ok = mbar_wait(&bars->p_full[x], p_cnt & 1, tmo, abort_flag, p.err);
+            ++p_cnt;
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t vbase = va + st * T::KV_BYTES;
+#pragma unroll
+            for (int k = 0; k < PV_STEPS; ++k) {
+              // each K step is 8 TMEM columns of P (16 x 16-bit or 32 x 8-bit)
+              if constexpr (FP8)
+                umma_f8_ts(o_tmem, s_tmem + k * 8, sdesc_kmajor_sw128(vbase + k * 32), idesc_o,
+                           (j > 1 || k > 0) ? 1u : 0u);
+              else
+                umma_f16_ts(o_tmem, s_tmem + k * 8, sdesc_mnmajor_sw128(vbase + k * 2048, T::KV_CHUNK), idesc_o,
+                            (j > 1 || k > 0) ? 1u : 0u);
+            }
+            if (j == nx) umma_commit(&bars->o_done[x]);     // last P V of this tile
+          } else {
+            tc_fence_after();
           }
+          if (j < nx) {
+            const uint32_t kb = ka + st * T::KV_BYTES;
+#pragma unroll
+            for (int k = 0; k < S_STEPS; ++k) {
+              const uint32_t qo = (k >> 2) * T::Q_CHUNK + (k & 3) * 32;
+              const uint32_t ko = (k >> 2) * T::KV_CHUNK + (k & 3) * 32;
+              if constexpr (FP8)
+                umma_f8_ss(s_tmem, sdesc_kmajor_sw128(qx + qo), sdesc_kmajor_sw128(kb + ko), idesc_s, k > 0 ? 1u : 0u);
+              else
+                umma_f16_ss(s_tmem, sdesc_kmajor_sw128(qx + qo), sdesc_kmajor_sw128(kb + ko), idesc_s,
+                            k > 0 ? 1u : 0u);
+            }
+            umma_commit(&bars->s_full[x]);
+          }
+          umma_commit(&bars->slot_empty[st]);
+          if (j == nkv - 1) umma_commit(&bars->q_empty);
         }
       }
       umma_commit(&bars->mma_done);
@@ -384,7 +362,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     // raise m only past this margin (FP8: P * 256 must stay <= 448, so m
     // follows the block maxima exactly)
     constexpr float lazy = FP8 ? 0.f : LAZY_RESCALE_LOG2;
-    int s_cnt = 0, pv_total = 0;
+    int s_cnt = 0, o_tiles = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       const Tile2 tl = get_tile(t);
@@ -496,8 +474,8 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         mbar_arrive(&bars->p_full[x]);
       }
       if (!ok) break;
-      pv_total += nblk;
-      ok = mbar_wait(&bars->o_done[x], (pv_total - 1) & 1, tmo, abort_flag, p.err);
+      ok = mbar_wait(&bars->o_done[x], o_tiles & 1, tmo, abort_flag, p.err);
+      ++o_tiles;
       if (!ok) break;
       tc_fence_after();
       const bool valid = i_row < tl.n;
