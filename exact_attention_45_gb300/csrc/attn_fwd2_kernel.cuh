@@ -62,8 +62,8 @@ struct Pair2Traits {
 // Ring slot j of a super tile holds K_j and V_{j-1} (slots 0..nkv), so each
 // key block costs one full and one empty barrier.
 struct Bars2 {
-  uint64_t q_full, q_empty;                 // q_empty: one arrival per MMA warp
-  uint64_t slot_full[4], slot_empty[4];     // slot_empty: one arrival per MMA warp
+  uint64_t q_full, q_empty;
+  uint64_t slot_full[4], slot_empty[4];
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -191,17 +191,20 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 2);
+    mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars->slot_full[s], 1);
-      mbar_init(&bars->slot_empty[s], 2);
+      mbar_init(&bars->slot_empty[s], 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars->s_full[x], 1);
-      mbar_init(&bars->p_full[x], 128);
       mbar_init(&bars->o_done[x], 1);
     }
-    mbar_init(&bars->mma_done, 2);
+    // tile A's P-ready barrier also carries "slot j has landed" from the
+    // watcher warp, so the MMA thread waits once for both
+    mbar_init(&bars->p_full[0], 129);
+    mbar_init(&bars->p_full[1], 128);
+    mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -281,74 +284,112 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         mbar_wait_drain(&bars->slot_full[it % STAGES], (it / STAGES) & 1, tmo, p.err);
       if (tile_i > 0) mbar_wait_drain(&bars->q_full, (tile_i - 1) & 1, tmo, p.err);
     }
-  } else if (warp == 9 || warp == 10) {
-    // ------------------------------------------------- MMA issuers, one per tile
-    // Each warp's lane 0 issues its tile's GEMMs in order O_x += P_x(j-1) V,
-    // S_x(j) = Q_x K_j^T; the two tiles' chains are independent, so while one
-    // waits for its softmax the other keeps the tensor core busy.
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    // One thread issues, in this order per key block j,
+    //   O_A += P_A(j-1) V_{j-1}, S_A(j) = Q_A K_j^T, O_B += P_B(j-1) V_{j-1}, S_B(j)
+    // so tile A's softmax of block j overlaps tile B's two GEMMs and vice
+    // versa. The issuing thread waits as little as possible (a wait on a
+    // barrier costs the tensor pipe idle time even when it is already
+    // complete): once per block for tile A (its P and the slot's data, see
+    // the watcher) and once for tile B.
     if (lane == 0) {
-      const int x = warp - 9;
       constexpr uint32_t idesc_s = FP8 ? idesc_kind_f8_e4m3(BLOCK_M, BN) : idesc_kind_f16(BLOCK_M, BN, BF16, false);
       constexpr uint32_t idesc_o = FP8 ? idesc_kind_f8_e4m3(BLOCK_M, D) : idesc_kind_f16(BLOCK_M, D, BF16, true);
       constexpr int PV_STEPS = BN * ELEM / 32;               // 32-byte K steps of P V
       constexpr int S_STEPS = D * ELEM / 32;                 // 32-byte K steps of Q K^T
-      const uint32_t qx = smem_u32(sQ) + x * T::Q_BYTES;
+      const uint32_t qa = smem_u32(sQ);
       const uint32_t ka = smem_u32(sK);
       const uint32_t va = smem_u32(sV);
-      const uint32_t s_tmem = tmem + T::TMEM_S + x * BN;
-      const uint32_t o_tmem = tmem + T::TMEM_O + x * D;
-      int slot_it = 0, tile_i = 0, p_cnt = 0;
+      int slot_it = 0, tile_i = 0;
+      int p_cnt0 = 0, p_cnt1 = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tile_i) {
         const Tile2 tl = get_tile(t);
-        const int nx = tile2_blocks<CAUSAL, BN>(tl, x);
-        const int nkv = max(tile2_blocks<CAUSAL, BN>(tl, 0), tile2_blocks<CAUSAL, BN>(tl, 1));
+        const int nb[2] = {tile2_blocks<CAUSAL, BN>(tl, 0), tile2_blocks<CAUSAL, BN>(tl, 1)};
+        const int nkv = max(nb[0], nb[1]);
         ok = mbar_wait(&bars->q_full, tile_i & 1, tmo, abort_flag, p.err);
         if (!ok) break;
-        for (int j = 0; j <= nkv; ++j, ++slot_it) {
+        for (int j = 0; j <= nkv && ok; ++j, ++slot_it) {
           const int st = slot_it % STAGES;
-          ok = mbar_wait(&bars->slot_full[st], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);
+          const uint32_t vbase = va + st * T::KV_BYTES;
+          const uint32_t kb = ka + st * T::KV_BYTES;
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (!ok) continue;
+            const bool pv = j >= 1 && j - 1 < nb[x];
+            int& pc = x == 0 ? p_cnt0 : p_cnt1;
+            if (pv) {
+              ok = mbar_wait(&bars->p_full[x], pc & 1, tmo, abort_flag, p.err);
+              ++pc;
+            } else if (x == 0) {
+              ok = mbar_wait(&bars->slot_full[st], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);
+            }
+            if (!ok) continue;
+            tc_fence_after();
+            const uint32_t s_tmem = tmem + T::TMEM_S + x * BN;
+            if (pv) {
+              const uint32_t o_tmem = tmem + T::TMEM_O + x * D;
+#pragma unroll
+              for (int k = 0; k < PV_STEPS; ++k) {
+                // each K step is 8 TMEM columns of P (16 x 16-bit or 32 x 8-bit)
+                if constexpr (FP8)
+                  umma_f8_ts(o_tmem, s_tmem + k * 8, sdesc_kmajor_sw128(vbase + k * 32), idesc_o,
+                             (j > 1 || k > 0) ? 1u : 0u);
+                else
+                  umma_f16_ts(o_tmem, s_tmem + k * 8, sdesc_mnmajor_sw128(vbase + k * 2048, T::KV_CHUNK), idesc_o,
+                              (j > 1 || k > 0) ? 1u : 0u);
+              }
+              if (j == nb[x]) umma_commit(&bars->o_done[x]);   // last P V of this tile
+            }
+            if (j < nb[x]) {
+              const uint32_t qx = qa + x * T::Q_BYTES;
+#pragma unroll
+              for (int k = 0; k < S_STEPS; ++k) {
+                const uint32_t qo = (k >> 2) * T::Q_CHUNK + (k & 3) * 32;
+                const uint32_t ko = (k >> 2) * T::KV_CHUNK + (k & 3) * 32;
+                if constexpr (FP8)
+                  umma_f8_ss(s_tmem, sdesc_kmajor_sw128(qx + qo), sdesc_kmajor_sw128(kb + ko), idesc_s,
+                             k > 0 ? 1u : 0u);
+                else
+                  umma_f16_ss(s_tmem, sdesc_kmajor_sw128(qx + qo), sdesc_kmajor_sw128(kb + ko), idesc_s,
+                              k > 0 ? 1u : 0u);
+              }
+              umma_commit(&bars->s_full[x]);
+            }
+          }
           if (!ok) break;
-          if (j >= 1 && j - 1 < nx) {
-            ok = mbar_wait(&bars->p_full[x], p_cnt & 1, tmo, abort_flag, p.err);
-            ++p_cnt;
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t vbase = va + st * T::KV_BYTES;
-#pragma unroll
-            for (int k = 0; k < PV_STEPS; ++k) {
-              // each K step is 8 TMEM columns of P (16 x 16-bit or 32 x 8-bit)
-              if constexpr (FP8)
-                umma_f8_ts(o_tmem, s_tmem + k * 8, sdesc_kmajor_sw128(vbase + k * 32), idesc_o,
-                           (j > 1 || k > 0) ? 1u : 0u);
-              else
-                umma_f16_ts(o_tmem, s_tmem + k * 8, sdesc_mnmajor_sw128(vbase + k * 2048, T::KV_CHUNK), idesc_o,
-                            (j > 1 || k > 0) ? 1u : 0u);
-            }
-            if (j == nx) umma_commit(&bars->o_done[x]);     // last P V of this tile
-          } else {
-            tc_fence_after();
-          }
-          if (j < nx) {
-            const uint32_t kb = ka + st * T::KV_BYTES;
-#pragma unroll
-            for (int k = 0; k < S_STEPS; ++k) {
-              const uint32_t qo = (k >> 2) * T::Q_CHUNK + (k & 3) * 32;
-              const uint32_t ko = (k >> 2) * T::KV_CHUNK + (k & 3) * 32;
-              if constexpr (FP8)
-                umma_f8_ss(s_tmem, sdesc_kmajor_sw128(qx + qo), sdesc_kmajor_sw128(kb + ko), idesc_s, k > 0 ? 1u : 0u);
-              else
-                umma_f16_ss(s_tmem, sdesc_kmajor_sw128(qx + qo), sdesc_kmajor_sw128(kb + ko), idesc_s,
-                            k > 0 ? 1u : 0u);
-            }
-            umma_commit(&bars->s_full[x]);
-          }
           umma_commit(&bars->slot_empty[st]);
           if (j == nkv - 1) umma_commit(&bars->q_empty);
         }
       }
       umma_commit(&bars->mma_done);
       mbar_wait_drain(&bars->mma_done, 0, tmo, p.err);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ slot watcher
+    // For every slot j >= 1 that tile A consumes together with P_A(j-1), wait
+    // until its K/V data has landed and add one arrival to tile A's P-ready
+    // barrier (after the barrier's previous phase completed, so the arrival
+    // lands in the phase of block j-1).
+    if (lane == 0) {
+      int slot_it = 0, arrivals = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const Tile2 tl = get_tile(t);
+        const int na = tile2_blocks<CAUSAL, BN>(tl, 0);
+        const int nkv = max(na, tile2_blocks<CAUSAL, BN>(tl, 1));
+        for (int j = 0; j <= nkv; ++j, ++slot_it) {
+          if (j >= 1 && j - 1 < na) {
+            ok = mbar_wait(&bars->slot_full[slot_it % STAGES], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);
+            if (ok && arrivals > 0) ok = mbar_wait(&bars->p_full[0], (arrivals - 1) & 1, tmo, abort_flag, p.err);
+            if (!ok) break;
+            mbar_arrive(&bars->p_full[0]);
+            ++arrivals;
+          }
+        }
+      }
     }
     __syncwarp();
   } else if (warp < 8) {
