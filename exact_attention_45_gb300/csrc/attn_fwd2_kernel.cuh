@@ -381,9 +381,14 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const int na = tile2_blocks<CAUSAL, BN>(tl, 0);
         const int nkv = max(na, tile2_blocks<CAUSAL, BN>(tl, 1));
         for (int j = 0; j <= nkv; ++j, ++slot_it) {
+          // Every slot is waited for, in order, even those this warp does not
+          // report: a parity wait is only unambiguous while the waiter is at
+          // most one phase behind, and skipping slots of a short ring would
+          // let it run two phases ahead of a slot still in flight.
+          ok = mbar_wait(&bars->slot_full[slot_it % STAGES], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);
+          if (!ok) break;
           if (j >= 1 && j - 1 < na) {
-            ok = mbar_wait(&bars->slot_full[slot_it % STAGES], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);
-            if (ok && arrivals > 0) ok = mbar_wait(&bars->p_full[0], (arrivals - 1) & 1, tmo, abort_flag, p.err);
+            if (arrivals > 0) ok = mbar_wait(&bars->p_full[0], (arrivals - 1) & 1, tmo, abort_flag, p.err);
             if (!ok) break;
             mbar_arrive(&bars->p_full[0]);
             ++arrivals;
