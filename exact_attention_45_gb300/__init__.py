@@ -41,8 +41,9 @@ _FP8_MODE = {"tensor": 0, "block": 1}
 # Every function include/attn45.h declares.
 EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_fwd_varlen", "attn_fp8_vt_ld", "attn_fp8_prepass", "attn_fwd_fp8",
-    "attn_fp8_workspace_size", "attn_fwd_fp8_auto", "attn_get_device_error", "attn_set_wait_timeout_ns",
-    "attn_debug_timeout_probe", "attn_status_string", "attn_last_error_message", "attn_version",
+    "attn_fp8_workspace_size", "attn_fwd_fp8_auto", "attn_fwd_fp8_auto_noalloc", "attn_get_device_error",
+    "attn_set_wait_timeout_ns", "attn_debug_timeout_probe", "attn_status_string", "attn_last_error_message",
+    "attn_version",
 )
 
 
@@ -81,6 +82,7 @@ def capi(build_if_missing: bool = True):
             "attn_fwd_fp8": ([P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P], I),
             "attn_fp8_workspace_size": ([I, I, I, I, I, I], SZ),
             "attn_fwd_fp8_auto": ([P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, I, I, U64, P], I),
+            "attn_fwd_fp8_auto_noalloc": ([P, P, P, P, P, I, I, I, I, I, I, F, I, I, U64, P], I),
             "attn_get_device_error": ([P], I),
             "attn_set_wait_timeout_ns": ([U64], I),
             "attn_debug_timeout_probe": ([U64, P], I),

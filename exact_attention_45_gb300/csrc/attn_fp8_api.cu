@@ -3,7 +3,9 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "api_internal.h"
 #include "attn45.h"
@@ -25,6 +27,34 @@ uint64_t splitmix64(uint64_t x) {
 }
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Fixed device scratch for attn_fwd_fp8_auto_noalloc: a file-scope device
+// array, so every GPU that loads this library holds these 16 MiB until the
+// process exits. Host code must not use the symbol as a pointer (it is a
+// host-side stand-in); its device address comes from cudaGetSymbolAddress,
+// looked up once per device with that device current.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) uint8_t g_fp8_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxScratchDevices] = {};
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return api_cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxScratchDevices) return api_fail(ATTN_ERR_UNSUPPORTED, "device index out of range");
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_fp8_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) return api_cuda_fail(e, "cudaGetSymbolAddress(fixed FP8 scratch)");
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return ATTN_OK;
+}
 
 struct Fp8Layout {
   size_t q8, k8, vt8, sq, sk, sv, total;
@@ -170,6 +200,30 @@ int attn_fwd_fp8_auto(const void* q, const void* k, const void* v, void* o, floa
   if (rc) return rc;
   return attn_fwd_fp8(w + L.q8, w + L.k8, w + L.vt8, sq, sk, sv, o, lse, B, H, Hkv, N, d, causal, scale, mode,
                       stream);
+}
+
+// Same computation as attn_fwd_fp8_auto, for callers that are not allowed to
+// allocate device memory: the quantised Q/K/V and their scales go to the
+// library's fixed 16 MiB device scratch instead of a caller workspace. Nothing
+// here allocates (no cudaMalloc/cudaFree, no allocating library routine).
+int attn_fwd_fp8_auto_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                              int Hkv, int N, int d, int causal, float scale, int mode, int rotate,
+                              uint64_t hadamard_seed, void* stream) {
+  int rc = check_shape(B, H, Hkv, N, d, mode);
+  if (rc) return rc;
+  const size_t need = fp8_layout(B, H, Hkv, N, d, mode).total;
+  if (need > kNoAllocScratchBytes) {
+    char msg[256];
+    snprintf(msg, sizeof(msg),
+             "this shape needs %zu bytes of FP8 scratch; the fixed scratch of attn_fwd_fp8_auto_noalloc holds %zu "
+             "(use attn_fwd_fp8_auto with a caller workspace)",
+             need, kNoAllocScratchBytes);
+    return api_fail(ATTN_ERR_INVALID_ARG, msg);
+  }
+  void* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch))) return rc;
+  return attn_fwd_fp8_auto(q, k, v, o, lse, scratch, kNoAllocScratchBytes, B, H, Hkv, N, d, causal, scale, mode,
+                           rotate, hadamard_seed, stream);
 }
 
 }  // extern "C"

@@ -134,6 +134,29 @@ ATTN45_API int attn_fwd_fp8_auto(const void* q, const void* k, const void* v, vo
                       size_t workspace_bytes, int B, int H, int Hkv, int N, int d, int causal, float scale,
                       int mode, int rotate, uint64_t hadamard_seed, void* stream);
 
+/*
+ * attn_fwd_fp8_auto_noalloc -- attn_fwd_fp8_auto for callers that may not
+ * allocate device memory (for example a host framework that owns every byte
+ * of device memory through its own pool and forbids cudaMalloc/cudaFree,
+ * whose implicit device-wide synchronisation and possible out-of-memory
+ * failure it cannot accept on its request path). Nothing in the pages has a
+ * counterpart to this call; it is an interface convenience.
+ *   Same arguments, layouts and results as attn_fwd_fp8_auto, without the
+ *   workspace: the quantised tensors live in one fixed device scratch array
+ *   of 16 MiB (16777216 bytes) inside this library, which every GPU that
+ *   loads the library holds until the process exits. Shapes whose
+ *   attn_fp8_workspace_size() exceeds that return ATTN_ERR_INVALID_ARG.
+ *   The first call on a device looks up the scratch address for that device
+ *   (with it current); make that first call before any stream capture.
+ *   Every call uses the same scratch: calls that may overlap on the GPU
+ *   (different streams, or several host threads) race and must be
+ *   serialised by the caller. Parts that must start at zero are cleared by
+ *   each call. Allocates nothing.
+ */
+ATTN45_API int attn_fwd_fp8_auto_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                         int H, int Hkv, int N, int d, int causal, float scale, int mode, int rotate,
+                                         uint64_t hadamard_seed, void* stream);
+
 /* Synchronises `stream`, reads and clears the current device's error word.
  * ATTN_OK, ATTN_ERR_TIMEOUT (a bounded device wait gave up) or ATTN_ERR_CUDA. */
 ATTN45_API int attn_get_device_error(void* stream);
