@@ -319,7 +319,7 @@ def fp8_measure(steps: int, warmup: int, seed: int = 0):
     pk = peaks()
     fp8_peak = 2.0 * pk["bf16_tflops"]     # e4m3 dense rate = 2x bf16 (nominal 4.5 vs 2.25 PFLOP/s)
     elems = B * N * H * d
-    pre_bytes = 3 * elems * 2 + elems * 2 + 3 * elems   # read Q,K,V; V read again; write 3 code tensors
+    pre_bytes = 3 * elems * 2 + 3 * elems   # read Q, K, V once, write the three code tensors
     return {
         "inputs": "N(0,1) + N(0,100) w.p. 0.001, seed 0", "mode": "per-block scales + Hadamard rotation",
         "fwd_tflops": round(fl / t_fwd / 1e12, 2), "fwd_ms": round(t_fwd * 1e3, 4),
