@@ -320,7 +320,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             const bool pv = j >= 1 && j - 1 < nb[x];
             int& pc = x == 0 ? p_cnt0 : p_cnt1;
             if (pv) {
-              ok = mbar_wait_relaxed(&bars->p_full[x], pc & 1, tmo, abort_flag, p.err);
+              ok = mbar_wait(&bars->p_full[x], pc & 1, tmo, abort_flag, p.err);
               ++pc;
             } else if (x == 0) {
               ok = mbar_wait(&bars->slot_full[st], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);

@@ -71,37 +71,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
-// Same as mbar_wait with a relaxed (not acquire) probe: on sm_103a it leaves
-// the tensor pipe idle for ~60 instead of ~110 cycles when issued between
-// MMAs. Callers order what follows with a tcgen05 after_thread_sync fence.
-__device__ __forceinline__ bool mbar_try_wait_relaxed(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.relaxed.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_relaxed(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
-                                                  volatile int* abort, unsigned int* err) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait_relaxed(a, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait_relaxed(a, parity)) return true;
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > timeout_ns) {
-      *abort = 1;
-      atomicOr(err, DEV_ERR_TIMEOUT);
-      return false;
-    }
-  }
-}
-
 // Bounded wait used while shutting down: ignores the abort flag so that copies
 // already in flight are still waited for, but gives up after `timeout_ns`.
 __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
