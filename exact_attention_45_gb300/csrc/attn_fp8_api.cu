@@ -133,7 +133,18 @@ int attn_fp8_prepass(const void* q, const void* k, const void* v, void* q8, void
   a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
   for (int c = 0; c < d; ++c)
     if (splitmix64(hadamard_seed + (uint64_t)c) & 1ull) a.sign_bits[c >> 5] |= 1u << (c & 31);
-  cudaError_t e = launch_fp8_prepass(a, d, static_cast<cudaStream_t>(stream));
+  a.timeout_ns = api_timeout_ns();
+  a.err = err;
+  Prepass128Maps maps;
+  const Prepass128Maps* mp = nullptr;
+  if (d == 128) {
+    if ((rc = api_make_map(&maps.in_q, false, q, d, H, N, B, 64, 128))) return rc;
+    if ((rc = api_make_map(&maps.in_k, false, k, d, Hkv, N, B, 64, 128))) return rc;
+    if ((rc = api_make_map(&maps.out_q, true, q8, d, H, N, B, 128, 128))) return rc;
+    if ((rc = api_make_map(&maps.out_k, true, k8, d, Hkv, N, B, 128, 128))) return rc;
+    mp = &maps;
+  }
+  cudaError_t e = launch_fp8_prepass(a, d, mp, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return api_cuda_fail(e, "attn_fp8_prepass launch");
   return ATTN_OK;
 }

@@ -15,8 +15,11 @@
 // codes are e4m3(RNE, saturating) of x / scale with the division one IEEE
 // fp32 rounding, so results are reproducible bit for bit.
 //
-// HBM-bound: every kernel reads its bf16 input once per pass with 16-byte
-// vector loads and writes codes with coalesced 4-byte stores.
+// HBM-bound. For head dim 128 (the FP8 forward's), Q and K blocks use
+// qk128_kernel: the 128-row block is staged by TMA, each thread rotates one
+// whole row in registers (all butterfly stages without shuffles, packed f32x2
+// adds) and the codes leave by a TMA store. Other head dims and V use the
+// warp-per-rows kernel below.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -24,6 +27,7 @@
 #include <cstdint>
 
 #include "fp8_prepass.h"
+#include "ptx.cuh"
 
 namespace attn45 {
 
@@ -44,6 +48,26 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
 __device__ __forceinline__ float scale_from_amax(float amax) {
   return amax == 0.f ? 1.f : __fdiv_rn(amax, E4M3_MAX);
 }
+
+// Correctly rounded x / s from the correctly rounded reciprocal r = RN(1/s):
+// q0 = RN(x r), e = x - q0 s (exact with one FMA), q = RN(q0 + e r)
+// (Markstein's division correction, as used for IEEE division on IA-64).
+// Valid for normal s and r; callers check that once per scale.
+struct Divider {
+  float s, r;
+  bool fast;
+  __device__ __forceinline__ Divider() : s(1.f), r(1.f), fast(true) {}
+  __device__ __forceinline__ explicit Divider(float s_) : s(s_) {
+    r = __frcp_rn(s_);
+    fast = isfinite(r) && fabsf(s_) >= 1.17549435e-38f && fabsf(r) >= 1.17549435e-38f;
+  }
+  __device__ __forceinline__ float div(float x) const {
+    if (!fast) return __fdiv_rn(x, s);
+    const float q0 = __fmul_rn(x, r);
+    const float e = __fmaf_rn(-q0, s, x);
+    return __fmaf_rn(e, r, q0);
+  }
+};
 
 // Loads E = d/32 consecutive bf16 of one row for this lane.
 template <int E>
@@ -108,10 +132,10 @@ __device__ __forceinline__ void rotate_row(float (&x)[E], uint32_t sign_bits_lan
 }
 
 template <int E>
-__device__ __forceinline__ void store_codes(uint8_t* dst, const float (&x)[E], float s) {
+__device__ __forceinline__ void store_codes(uint8_t* dst, const float (&x)[E], const Divider& dv) {
   float y[E];
 #pragma unroll
-  for (int e = 0; e < E; ++e) y[e] = __fdiv_rn(x[e], s);
+  for (int e = 0; e < E; ++e) y[e] = dv.div(x[e]);
   if constexpr (E == 8) {
     *reinterpret_cast<uint2*>(dst) = make_uint2(e4m3x4(y[0], y[1], y[2], y[3]), e4m3x4(y[4], y[5], y[6], y[7]));
   } else if constexpr (E == 4) {
@@ -175,12 +199,13 @@ __device__ void qk_block(const PrepassArgs& a, bool is_q, int b, int head, int b
   } else {
     s = scale_from_amax(__uint_as_float(*reinterpret_cast<volatile unsigned int*>(sc)));
   }
+  const Divider dv(s);
 #pragma unroll
   for (int rr = 0; rr < ROWS_PER_WARP; ++rr) {
     const int n = blk * ROWS + warp * ROWS_PER_WARP + rr;
     if (n < a.N) {
       const size_t row = ((size_t)b * a.N + n) * Hx + head;
-      store_codes<E>(dst + row * d + E * lane, x[rr], s);
+      store_codes<E>(dst + row * d + E * lane, x[rr], dv);
     }
   }
 }
@@ -244,6 +269,9 @@ __device__ void v_block(const PrepassArgs& a, int b, int head, int blk, int phas
         : *reinterpret_cast<volatile unsigned int*>(sv);
     s[e] = scale_from_amax(__uint_as_float(bits));
   }
+  Divider dv[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) dv[e] = Divider(s[e]);
   // codes into the transposed tile: tile[c][n_local]
 #pragma unroll
   for (int rr = 0; rr < ROWS_PER_WARP; ++rr) {
@@ -253,7 +281,7 @@ __device__ void v_block(const PrepassArgs& a, int b, int head, int blk, int phas
       uint16_t c2;
       asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
           : "=h"(c2)
-          : "f"(__fdiv_rn(x[rr][e + 1], s[e + 1])), "f"(__fdiv_rn(x[rr][e], s[e])));
+          : "f"(dv[e + 1].div(x[rr][e + 1])), "f"(dv[e].div(x[rr][e])));
       tile[(E * lane + e) * TP + nl] = (uint8_t)(c2 & 0xFF);
       tile[(E * lane + e + 1) * TP + nl] = (uint8_t)(c2 >> 8);
     }
@@ -268,9 +296,9 @@ __device__ void v_block(const PrepassArgs& a, int b, int head, int blk, int phas
 }
 
 template <int E>
-__global__ void __launch_bounds__(THREADS) prepass_kernel(const PrepassArgs a, int phase) {
+__global__ void __launch_bounds__(THREADS) prepass_kernel(const PrepassArgs a, int phase, int block_offset) {
   // blocks: [Q blocks][K blocks][V blocks], each B * heads * nblk
-  int id = blockIdx.x;
+  int id = blockIdx.x + block_offset;
   const int nq = a.B * a.H * a.nblk, nk = a.B * a.Hkv * a.nblk;
   if (id < nq) {
     if (phase == 1 && a.block_mode) return;   // Q done in phase 0
@@ -290,6 +318,148 @@ __global__ void __launch_bounds__(THREADS) prepass_kernel(const PrepassArgs a, i
   v_block<E>(a, bh / a.Hkv, bh % a.Hkv, blk, phase);
 }
 
+
+// ---------------------------------------------------------------- head dim 128
+// One CTA = one 128-row block of Q or K; thread r owns row r.
+constexpr int QK128_SMEM = 1024 + 2 * 16384 + 16384;   // alignment + bf16 tile + code tile
+
+__device__ __forceinline__ void butterfly_pairs(float (&x)[128], int h) {
+  // stage with span h >= 2: pairs (i, i+h) and (i+1, i+1+h) share one f32x2 op
+#pragma unroll
+  for (int i = 0; i < 128; i += 2) {
+    if ((i & h) == 0) {
+      const uint64_t a = f2_pack(x[i], x[i + 1]);
+      const uint64_t b = f2_pack(x[i + h], x[i + h + 1]);
+      f2_unpack(f2_add(a, b), x[i], x[i + 1]);
+      f2_unpack(f2_sub(a, b), x[i + h], x[i + h + 1]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(128) qk128_kernel(const __grid_constant__ CUtensorMap in_q,
+                                                    const __grid_constant__ CUtensorMap in_k,
+                                                    const __grid_constant__ CUtensorMap out_q,
+                                                    const __grid_constant__ CUtensorMap out_k, const PrepassArgs a,
+                                                    int phase) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* tile = raw + ((1024 - (smem_u32(raw) & 1023)) & 1023);   // 2 x [128 rows][128 B], swizzled
+  uint8_t* codes = tile + 2 * 16384;                                  // [128 rows][128 B], swizzled
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  __shared__ float red[4];
+  __shared__ uint32_t xmask[64];
+  const int nq = a.B * a.H * a.nblk;
+  int id = blockIdx.x;
+  const bool is_q = id < nq;
+  if (!is_q) id -= nq;
+  const int Hx = is_q ? a.H : a.Hkv;
+  const int blk = id % a.nblk, bh = id / a.nblk;
+  const int b = bh / Hx, head = bh % Hx;
+  float* sc = is_q ? a.sq : a.sk;
+  const int r = threadIdx.x;
+  if (r == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (r < 64) {
+    // sign flips as XOR masks on bf16 pairs (elements 2r, 2r+1)
+    const uint32_t w = a.sign_bits[(2 * r) >> 5] >> ((2 * r) & 31);
+    xmask[r] = a.rotate ? (((w & 1u) << 15) | (((w >> 1) & 1u) << 31)) : 0u;
+  }
+  __syncthreads();
+  if (r == 0) {
+    const CUtensorMap* m = is_q ? &in_q : &in_k;
+    mbar_expect_tx(&bar, 2 * 16384);
+    tma_load_4d(m, &bar, tile, 0, head, blk * ROWS, b);
+    tma_load_4d(m, &bar, tile + 16384, 64, head, blk * ROWS, b);
+  }
+  mbar_wait(&bar, 0, a.timeout_ns, &abort_flag, a.err);
+  // row r: element e lives in chunk e/64, 16-byte piece (e%64)/8 swizzled by r%8
+  float x[128];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 v = *reinterpret_cast<const uint4*>(tile + c * 16384 + r * 128 + ((j ^ (r & 7)) << 4));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e = c * 64 + j * 8 + 2 * i;
+        const uint32_t u = w[i] ^ xmask[e >> 1];
+        x[e] = __uint_as_float(u << 16);
+        x[e + 1] = __uint_as_float(u & 0xFFFF0000u);
+      }
+    }
+  }
+  if (a.rotate) {
+    // span 1 inside each register pair, then spans 2..64 as packed pairs
+#pragma unroll
+    for (int i = 0; i < 128; i += 2) {
+      const float p0 = x[i], p1 = x[i + 1];
+      x[i] = __fadd_rn(p0, p1);
+      x[i + 1] = __fsub_rn(p0, p1);
+    }
+    butterfly_pairs(x, 2);
+    butterfly_pairs(x, 4);
+    butterfly_pairs(x, 8);
+    butterfly_pairs(x, 16);
+    butterfly_pairs(x, 32);
+    butterfly_pairs(x, 64);
+    const uint64_t c2 = f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
+#pragma unroll
+    for (int i = 0; i < 128; i += 2) f2_unpack(f2_mul(f2_pack(x[i], x[i + 1]), c2), x[i], x[i + 1]);
+  }
+  const bool valid = blk * ROWS + r < a.N;      // rows past N (zero filled) do not count
+  float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
+  if (valid) {
+#pragma unroll
+    for (int i = 0; i < 128; i += 4) {
+      m0 = fmaxf(m0, fabsf(x[i]));
+      m1 = fmaxf(m1, fabsf(x[i + 1]));
+      m2 = fmaxf(m2, fabsf(x[i + 2]));
+      m3 = fmaxf(m3, fabsf(x[i + 3]));
+    }
+  }
+  float amax = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+  float s;
+  const bool need_block_max = a.block_mode || phase == 0;
+  if (need_block_max) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if ((r & 31) == 0) red[r >> 5] = amax;
+    __syncthreads();
+    amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  }
+  if (a.block_mode) {
+    s = scale_from_amax(amax);
+    if (r == 0) sc[((size_t)b * Hx + head) * a.nblk + blk] = s;
+  } else if (phase == 0) {
+    if (r == 0) atomicMax(reinterpret_cast<unsigned int*>(sc), __float_as_uint(amax));
+    return;
+  } else {
+    s = scale_from_amax(__uint_as_float(*reinterpret_cast<volatile unsigned int*>(sc)));
+  }
+  const Divider dv(s);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = j * 16 + i * 4;
+      w[i] = e4m3x4(dv.div(x[e]), dv.div(x[e + 1]), dv.div(x[e + 2]), dv.div(x[e + 3]));
+    }
+    *reinterpret_cast<uint4*>(codes + r * 128 + ((j ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (r == 0) {
+    tma_store_4d(is_q ? &out_q : &out_k, codes, 0, head, blk * ROWS, b);
+    tma_store_commit();
+    tma_store_wait_all();
+  }
+}
+
 // Turns the amax values left in the scale outputs into scales.
 __global__ void finalize_kernel(float* sq, float* sk, float* sv, int nsv, int tensor_mode) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -302,7 +472,7 @@ __global__ void finalize_kernel(float* sq, float* sk, float* sv, int nsv, int te
 
 }  // namespace
 
-cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, cudaStream_t s) {
+cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps* maps, cudaStream_t s) {
   const size_t nsv = a.block_mode ? (size_t)a.B * a.Hkv * d : 1;
   cudaError_t e = cudaMemsetAsync(a.sv, 0, nsv * sizeof(float), s);
   if (e != cudaSuccess) return e;
@@ -310,12 +480,27 @@ cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, cudaStream_t s) {
     if ((e = cudaMemsetAsync(a.sq, 0, sizeof(float), s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(a.sk, 0, sizeof(float), s)) != cudaSuccess) return e;
   }
-  const int blocks = (a.B * a.H + 2 * a.B * a.Hkv) * a.nblk;
+  const int nqk = (a.B * a.H + a.B * a.Hkv) * a.nblk;
+  const int nv = a.B * a.Hkv * a.nblk;
+  const bool fast_qk = d == 128 && maps != nullptr;
+  if (fast_qk) {
+    e = cudaFuncSetAttribute(qk128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QK128_SMEM);
+    if (e != cudaSuccess) return e;
+  }
   for (int phase = 0; phase < 2; ++phase) {
-    switch (d) {
-      case 64: prepass_kernel<2><<<blocks, THREADS, 0, s>>>(a, phase); break;
-      case 128: prepass_kernel<4><<<blocks, THREADS, 0, s>>>(a, phase); break;
-      default: prepass_kernel<8><<<blocks, THREADS, 0, s>>>(a, phase); break;
+    if (fast_qk) {
+      if (phase == 0 || !a.block_mode) {
+        qk128_kernel<<<nqk, 128, QK128_SMEM, s>>>(maps->in_q, maps->in_k, maps->out_q, maps->out_k, a, phase);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      }
+      prepass_kernel<4><<<nv, THREADS, 0, s>>>(a, phase, nqk);   // V blocks only
+    } else {
+      const int blocks = nqk + nv;
+      switch (d) {
+        case 64: prepass_kernel<2><<<blocks, THREADS, 0, s>>>(a, phase, 0); break;
+        case 128: prepass_kernel<4><<<blocks, THREADS, 0, s>>>(a, phase, 0); break;
+        default: prepass_kernel<8><<<blocks, THREADS, 0, s>>>(a, phase, 0); break;
+      }
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

@@ -1,6 +1,7 @@
 // fp8_prepass.h -- arguments of the FP8 pre-pass kernels.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -14,9 +15,19 @@ struct PrepassArgs {
   int block_mode, rotate;
   float inv_sqrt_d;                // fl32(1/sqrt(d))
   uint32_t sign_bits[8];           // bit c set <=> sigma_c = -1 (d <= 256)
+  unsigned long long timeout_ns;   // bound for device waits
+  unsigned int* err;               // device error word
 };
 
-// memsets of the scale outputs, two passes of the pre-pass kernel, finalise.
-cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, cudaStream_t s);
+// Tensor maps of the head-dim-128 Q/K path: bf16 inputs {128, heads, N, B}
+// with 64 x 128-row boxes, e4m3 outputs {128, heads, N, B} with 128 x 128-row
+// boxes, 128-byte swizzle.
+struct Prepass128Maps {
+  CUtensorMap in_q, in_k, out_q, out_k;
+};
+
+// memsets of the scale outputs, two passes of the pre-pass kernels, finalise.
+// maps: required for the fast head-dim-128 path (nullptr selects the generic one).
+cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps* maps, cudaStream_t s);
 
 }  // namespace attn45
