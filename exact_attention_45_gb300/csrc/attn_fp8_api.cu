@@ -140,6 +140,7 @@ int attn_fp8_prepass(const void* q, const void* k, const void* v, void* q8, void
   if (d == 128) {
     if ((rc = api_make_map(&maps.in_q, false, q, d, H, N, B, 64, 128))) return rc;
     if ((rc = api_make_map(&maps.in_k, false, k, d, Hkv, N, B, 64, 128))) return rc;
+    if ((rc = api_make_map(&maps.in_v, false, v, d, Hkv, N, B, 64, 128))) return rc;
     if ((rc = api_make_map(&maps.out_q, true, q8, d, H, N, B, 128, 128))) return rc;
     if ((rc = api_make_map(&maps.out_k, true, k8, d, Hkv, N, B, 128, 128))) return rc;
     mp = &maps;

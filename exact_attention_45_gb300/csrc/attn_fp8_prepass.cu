@@ -460,6 +460,80 @@ __global__ void __launch_bounds__(128) qk128_kernel(const __grid_constant__ CUte
   }
 }
 
+
+// V block (b, kv head, 128 rows) for head dim 128; thread c owns channel c.
+// phase 0: per-channel (block mode) or whole-tensor amax -> atomicMax into sv.
+// phase 1: codes x / scale_c written transposed: vt8[b][head][c][n0 .. n0+127].
+constexpr int V128_SMEM = 1024 + 2 * 16384;
+
+__global__ void __launch_bounds__(128) v128_kernel(const __grid_constant__ CUtensorMap in_v, const PrepassArgs a,
+                                                   int phase) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* tile = raw + ((1024 - (smem_u32(raw) & 1023)) & 1023);   // 2 x [128 rows][64 ch] bf16, swizzled
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  __shared__ float red[4];
+  const int blk = blockIdx.x % a.nblk, bh = blockIdx.x / a.nblk;
+  const int b = bh / a.Hkv, head = bh % a.Hkv;
+  const int c = threadIdx.x;
+  if (c == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (c == 0) {
+    mbar_expect_tx(&bar, 2 * 16384);
+    tma_load_4d(&in_v, &bar, tile, 0, head, blk * ROWS, b);
+    tma_load_4d(&in_v, &bar, tile + 16384, 64, head, blk * ROWS, b);
+  }
+  mbar_wait(&bar, 0, a.timeout_ns, &abort_flag, a.err);
+  // channel c of row n: chunk c/64, 16-byte piece ((c%64)/8) ^ (n%8), element c%8
+  const uint8_t* col = tile + (c >> 6) * 16384 + (c & 7) * 2;
+  const int piece = (c & 63) >> 3;
+  const int nvalid = min(ROWS, a.N - blk * ROWS);
+  float* sv_c = a.block_mode ? a.sv + ((size_t)b * a.Hkv + head) * 128 + c : a.sv;
+  if (phase == 0) {
+    float m0 = 0.f, m1 = 0.f;
+#pragma unroll 8
+    for (int n = 0; n < ROWS; n += 2) {
+      const float v0 = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(col + n * 128 + ((piece ^ (n & 7)) << 4)) << 16);
+      const float v1 = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(col + (n + 1) * 128 + ((piece ^ ((n + 1) & 7)) << 4)) << 16);
+      if (n < nvalid) m0 = fmaxf(m0, fabsf(v0));
+      if (n + 1 < nvalid) m1 = fmaxf(m1, fabsf(v1));
+    }
+    float m = fmaxf(m0, m1);
+    if (a.block_mode) {
+      atomicMax(reinterpret_cast<unsigned int*>(sv_c), __float_as_uint(m));
+    } else {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      if ((c & 31) == 0) red[c >> 5] = m;
+      __syncthreads();
+      if (c == 0) atomicMax(reinterpret_cast<unsigned int*>(sv_c), __float_as_uint(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]))));
+    }
+    return;
+  }
+  const Divider dv(scale_from_amax(__uint_as_float(*reinterpret_cast<volatile unsigned int*>(sv_c))));
+  uint4* dst = reinterpret_cast<uint4*>(a.vt8 + (((size_t)b * a.Hkv + head) * 128 + c) * a.ldv + (size_t)blk * ROWS);
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {             // 16 rows -> 16 codes -> one 16-byte store
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float y[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int n = g * 16 + i * 4 + t;
+        const float v = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(col + n * 128 + ((piece ^ (n & 7)) << 4)) << 16);
+        y[t] = n < nvalid ? dv.div(v) : 0.f;    // pad keys past N hold code 0
+      }
+      w[i] = e4m3x4(y[0], y[1], y[2], y[3]);
+    }
+    dst[g] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 // Turns the amax values left in the scale outputs into scales.
 __global__ void finalize_kernel(float* sq, float* sk, float* sv, int nsv, int tensor_mode) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -486,6 +560,8 @@ cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps
   if (fast_qk) {
     e = cudaFuncSetAttribute(qk128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QK128_SMEM);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(v128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, V128_SMEM);
+    if (e != cudaSuccess) return e;
   }
   for (int phase = 0; phase < 2; ++phase) {
     if (fast_qk) {
@@ -493,7 +569,7 @@ cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps
         qk128_kernel<<<nqk, 128, QK128_SMEM, s>>>(maps->in_q, maps->in_k, maps->out_q, maps->out_k, a, phase);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
       }
-      prepass_kernel<4><<<nv, THREADS, 0, s>>>(a, phase, nqk);   // V blocks only
+      v128_kernel<<<nv, 128, V128_SMEM, s>>>(maps->in_v, a, phase);
     } else {
       const int blocks = nqk + nv;
       switch (d) {

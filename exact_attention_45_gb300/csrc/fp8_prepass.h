@@ -19,11 +19,11 @@ struct PrepassArgs {
   unsigned int* err;               // device error word
 };
 
-// Tensor maps of the head-dim-128 Q/K path: bf16 inputs {128, heads, N, B}
+// Tensor maps of the head-dim-128 path: bf16 inputs (Q, K, V) {128, heads, N, B}
 // with 64 x 128-row boxes, e4m3 outputs {128, heads, N, B} with 128 x 128-row
 // boxes, 128-byte swizzle.
 struct Prepass128Maps {
-  CUtensorMap in_q, in_k, out_q, out_k;
+  CUtensorMap in_q, in_k, in_v, out_q, out_k;
 };
 
 // memsets of the scale outputs, two passes of the pre-pass kernels, finalise.
