@@ -145,7 +145,7 @@ int attn_fp8_prepass(const void* q, const void* k, const void* v, void* q8, void
     if ((rc = api_make_map(&maps.out_k, true, k8, d, Hkv, N, B, 128, 128))) return rc;
     mp = &maps;
   }
-  cudaError_t e = launch_fp8_prepass(a, d, mp, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_fp8_prepass(a, d, mp, sm, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return api_cuda_fail(e, "attn_fp8_prepass launch");
   return ATTN_OK;
 }

@@ -28,6 +28,7 @@ struct Prepass128Maps {
 
 // memsets of the scale outputs, two passes of the pre-pass kernels, finalise.
 // maps: required for the fast head-dim-128 path (nullptr selects the generic one).
-cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps* maps, cudaStream_t s);
+cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps* maps, int sm_count,
+                               cudaStream_t s);
 
 }  // namespace attn45
