@@ -321,12 +321,12 @@ __global__ void __launch_bounds__(THREADS) prepass_kernel(const PrepassArgs a, i
 
 // ---------------------------------------------------------------- head dim 128
 // One CTA = one 128-row block of Q or K; thread r owns row r.
-constexpr int QK128_SMEM = 1024 + 2 * 32768 + 2 * 16384;   // alignment + 2 bf16 tiles + 2 code tiles
+constexpr int QK128_SMEM = 1024 + 2 * 16384 + 16384;   // alignment + bf16 tile + code tile
 
-__device__ __forceinline__ void butterfly_pairs(float (&x)[128], int h) {
+__device__ __forceinline__ void butterfly_pairs64(float (&x)[64], int h) {
   // stage with span h >= 2: pairs (i, i+h) and (i+1, i+1+h) share one f32x2 op
 #pragma unroll
-  for (int i = 0; i < 128; i += 2) {
+  for (int i = 0; i < 64; i += 2) {
     if ((i & h) == 0) {
       const uint64_t a = f2_pack(x[i], x[i + 1]);
       const uint64_t b = f2_pack(x[i + h], x[i + h + 1]);
@@ -336,170 +336,150 @@ __device__ __forceinline__ void butterfly_pairs(float (&x)[128], int h) {
   }
 }
 
-struct QKBlock {
-  bool is_q;
-  int b, head, blk, Hx;
-};
-
-__device__ __forceinline__ QKBlock qk_decode(const PrepassArgs& a, int id) {
-  const int nq = a.B * a.H * a.nblk;
-  QKBlock k;
-  k.is_q = id < nq;
-  if (!k.is_q) id -= nq;
-  k.Hx = k.is_q ? a.H : a.Hkv;
-  k.blk = id % a.nblk;
-  const int bh = id / a.nblk;
-  k.b = bh / k.Hx;
-  k.head = bh % k.Hx;
-  return k;
-}
-
-// Persistent: CTA i handles blocks i, i + grid, ...; the TMA load of the next
-// block is issued before the current one is processed (two input tiles), and
-// code tiles alternate so a TMA store may still be reading the previous one.
-__global__ void __launch_bounds__(128) qk128_kernel(const __grid_constant__ CUtensorMap in_q,
+// One CTA = one 128-row block of Q or K, 256 threads: lanes 2i and 2i+1 of a
+// warp hold elements 0-63 and 64-127 of one row (row = warp * 16 + lane / 2).
+// Spans 1..32 run inside a thread; span 64 pairs the two halves by a shuffle.
+__global__ void __launch_bounds__(256, 3) qk128_kernel(const __grid_constant__ CUtensorMap in_q,
                                                     const __grid_constant__ CUtensorMap in_k,
                                                     const __grid_constant__ CUtensorMap out_q,
                                                     const __grid_constant__ CUtensorMap out_k, const PrepassArgs a,
                                                     int phase) {
   extern __shared__ uint8_t raw[];
-  uint8_t* base = raw + ((1024 - (smem_u32(raw) & 1023)) & 1023);
-  uint8_t* tiles = base;                  // 2 x (2 x [128 rows][128 B]) bf16, swizzled
-  uint8_t* codes = base + 2 * 32768;      // 2 x [128 rows][128 B] e4m3, swizzled
-  __shared__ uint64_t full[2];
+  uint8_t* tile = raw + ((1024 - (smem_u32(raw) & 1023)) & 1023);   // 2 x [128 rows][128 B], swizzled
+  uint8_t* codes = tile + 2 * 16384;                                  // [128 rows][128 B], swizzled
+  __shared__ uint64_t bar;
   __shared__ int abort_flag;
-  __shared__ float red[2][4];
+  __shared__ float red[8];
   __shared__ uint32_t xmask[64];
-  const int nblocks = (a.B * a.H + a.B * a.Hkv) * a.nblk;
-  const int r = threadIdx.x;
-  if (r == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+  const int nq = a.B * a.H * a.nblk;
+  int id = blockIdx.x;
+  const bool is_q = id < nq;
+  if (!is_q) id -= nq;
+  const int Hx = is_q ? a.H : a.Hkv;
+  const int blk = id % a.nblk, bh = id / a.nblk;
+  const int b = bh / Hx, head = bh % Hx;
+  float* sc = is_q ? a.sq : a.sk;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int r = warp * 16 + (lane >> 1);      // row in the block
+  const int half = lane & 1;                  // elements [64*half, 64*half + 64)
+  if (t == 0) {
+    mbar_init(&bar, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
-  if (r < 64) {
-    // sign flips as XOR masks on bf16 pairs (elements 2r, 2r+1)
-    const uint32_t w = a.sign_bits[(2 * r) >> 5] >> ((2 * r) & 31);
-    xmask[r] = a.rotate ? (((w & 1u) << 15) | (((w >> 1) & 1u) << 31)) : 0u;
+  if (t < 64) {
+    // sign flips as XOR masks on bf16 pairs (elements 2t, 2t+1)
+    const uint32_t w = a.sign_bits[(2 * t) >> 5] >> ((2 * t) & 31);
+    xmask[t] = a.rotate ? (((w & 1u) << 15) | (((w >> 1) & 1u) << 31)) : 0u;
   }
   __syncthreads();
-  auto issue_load = [&](int id, int buf) {
-    const QKBlock k = qk_decode(a, id);
-    const CUtensorMap* m = k.is_q ? &in_q : &in_k;
-    uint8_t* t = tiles + buf * 32768;
-    mbar_expect_tx(&full[buf], 32768);
-    tma_load_4d(m, &full[buf], t, 0, k.head, k.blk * ROWS, k.b);
-    tma_load_4d(m, &full[buf], t + 16384, 64, k.head, k.blk * ROWS, k.b);
-  };
-  if (r == 0 && (int)blockIdx.x < nblocks) issue_load(blockIdx.x, 0);
-  int it = 0;
-  for (int id = blockIdx.x; id < nblocks; id += gridDim.x, ++it) {
-    const int buf = it & 1;
-    const QKBlock k = qk_decode(a, id);
-    float* sc = k.is_q ? a.sq : a.sk;
-    if (!mbar_wait(&full[buf], (it >> 1) & 1, a.timeout_ns, &abort_flag, a.err)) {
-      // give up, but not with copies in flight: the one for this round and
-      // the prefetch of the next (if it was issued) are drained (bounded)
-      if (r == 0) {
-        mbar_wait_drain(&full[buf], (it >> 1) & 1, a.timeout_ns, a.err);
-        if (id + (int)gridDim.x < nblocks && it > 0) mbar_wait_drain(&full[buf ^ 1], ((it + 1) >> 1) & 1, a.timeout_ns, a.err);
-      }
-      break;
-    }
-    // row r: element e lives in chunk e/64, 16-byte piece (e%64)/8 swizzled by r%8
-    const uint8_t* tile = tiles + buf * 32768;
-    float x[128];
+  if (t == 0) {
+    const CUtensorMap* m = is_q ? &in_q : &in_k;
+    mbar_expect_tx(&bar, 2 * 16384);
+    tma_load_4d(m, &bar, tile, 0, head, blk * ROWS, b);
+    tma_load_4d(m, &bar, tile + 16384, 64, head, blk * ROWS, b);
+  }
+  mbar_wait(&bar, 0, a.timeout_ns, &abort_flag, a.err);
+  // element e (0..63 of this half) of row r: chunk `half`, piece e/8 swizzled by r%8
+  float x[64];
+  const uint8_t* src = tile + half * 16384 + r * 128;
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
+  for (int j = 0; j < 8; ++j) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src + ((j ^ (r & 7)) << 4));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint4 v = *reinterpret_cast<const uint4*>(tile + c * 16384 + r * 128 + ((j ^ (r & 7)) << 4));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int e = c * 64 + j * 8 + 2 * i;
-          const uint32_t u = w[i] ^ xmask[e >> 1];
-          x[e] = __uint_as_float(u << 16);
-          x[e + 1] = __uint_as_float(u & 0xFFFF0000u);
-        }
-      }
-    }
-    // every thread has its row: the other tile (read in the previous round)
-    // and this one are free once all threads pass this barrier
-    __syncthreads();
-    if (r == 0 && id + (int)gridDim.x < nblocks) issue_load(id + gridDim.x, buf ^ 1);
-    if (a.rotate) {
-      // span 1 inside each register pair, then spans 2..64 as packed pairs
-#pragma unroll
-      for (int i = 0; i < 128; i += 2) {
-        const float p0 = x[i], p1 = x[i + 1];
-        x[i] = __fadd_rn(p0, p1);
-        x[i + 1] = __fsub_rn(p0, p1);
-      }
-      butterfly_pairs(x, 2);
-      butterfly_pairs(x, 4);
-      butterfly_pairs(x, 8);
-      butterfly_pairs(x, 16);
-      butterfly_pairs(x, 32);
-      butterfly_pairs(x, 64);
-      const uint64_t c2 = f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
-#pragma unroll
-      for (int i = 0; i < 128; i += 2) f2_unpack(f2_mul(f2_pack(x[i], x[i + 1]), c2), x[i], x[i + 1]);
-    }
-    const bool valid = k.blk * ROWS + r < a.N;      // rows past N (zero filled) do not count
-    float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
-    if (valid) {
-#pragma unroll
-      for (int i = 0; i < 128; i += 4) {
-        m0 = fmaxf(m0, fabsf(x[i]));
-        m1 = fmaxf(m1, fabsf(x[i + 1]));
-        m2 = fmaxf(m2, fabsf(x[i + 2]));
-        m3 = fmaxf(m3, fabsf(x[i + 3]));
-      }
-    }
-    float amax = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-    if (a.block_mode || phase == 0) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      if ((r & 31) == 0) red[buf][r >> 5] = amax;
-      __syncthreads();
-      amax = fmaxf(fmaxf(red[buf][0], red[buf][1]), fmaxf(red[buf][2], red[buf][3]));
-    }
-    if (!a.block_mode && phase == 0) {
-      if (r == 0) atomicMax(reinterpret_cast<unsigned int*>(sc), __float_as_uint(amax));
-      continue;
-    }
-    float s;
-    if (a.block_mode) {
-      s = scale_from_amax(amax);
-      if (r == 0) sc[((size_t)k.b * k.Hx + k.head) * a.nblk + k.blk] = s;
-    } else {
-      s = scale_from_amax(__uint_as_float(*reinterpret_cast<volatile unsigned int*>(sc)));
-    }
-    // the code tile written two rounds ago must have been read by its store
-    if (r == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-    __syncthreads();
-    uint8_t* ct = codes + buf * 16384;
-    const Divider dv(s);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int e = j * 16 + i * 4;
-        w[i] = e4m3x4(dv.div(x[e]), dv.div(x[e + 1]), dv.div(x[e + 2]), dv.div(x[e + 3]));
-      }
-      *reinterpret_cast<uint4*>(ct + r * 128 + ((j ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (r == 0) {
-      tma_store_4d(k.is_q ? &out_q : &out_k, ct, 0, k.head, k.blk * ROWS, k.b);
-      tma_store_commit();
+    for (int i = 0; i < 4; ++i) {
+      const int e = j * 8 + 2 * i;
+      const uint32_t u = w[i] ^ xmask[(half * 64 + e) >> 1];
+      x[e] = __uint_as_float(u << 16);
+      x[e + 1] = __uint_as_float(u & 0xFFFF0000u);
     }
   }
-  if (r == 0) tma_store_wait_all();
+  if (a.rotate) {
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) {
+      const float p0 = x[i], p1 = x[i + 1];
+      x[i] = __fadd_rn(p0, p1);
+      x[i + 1] = __fsub_rn(p0, p1);
+    }
+    butterfly_pairs64(x, 2);
+    butterfly_pairs64(x, 4);
+    butterfly_pairs64(x, 8);
+    butterfly_pairs64(x, 16);
+    butterfly_pairs64(x, 32);
+    // span 64: (x_i, x_{i+64}) -> (x_i + x_{i+64}, x_i - x_{i+64}); half 0 holds x_i
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[i], 1);
+      x[i] = half ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
+    }
+    const uint64_t c2 = f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) f2_unpack(f2_mul(f2_pack(x[i], x[i + 1]), c2), x[i], x[i + 1]);
+  }
+  const bool valid = blk * ROWS + r < a.N;      // rows past N (zero filled) do not count
+  float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
+  if (valid) {
+#pragma unroll
+    for (int i = 0; i < 64; i += 4) {
+      m0 = fmaxf(m0, fabsf(x[i]));
+      m1 = fmaxf(m1, fabsf(x[i + 1]));
+      m2 = fmaxf(m2, fabsf(x[i + 2]));
+      m3 = fmaxf(m3, fabsf(x[i + 3]));
+    }
+  }
+  float amax = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+  if (a.block_mode || phase == 0) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+  }
+  float s;
+  if (a.block_mode) {
+    s = scale_from_amax(amax);
+    if (t == 0) sc[((size_t)b * Hx + head) * a.nblk + blk] = s;
+  } else if (phase == 0) {
+    if (t == 0) atomicMax(reinterpret_cast<unsigned int*>(sc), __float_as_uint(amax));
+    return;
+  } else {
+    s = scale_from_amax(__uint_as_float(*reinterpret_cast<volatile unsigned int*>(sc)));
+  }
+  const Divider dv(s);
+  if (dv.fast) {
+    // Markstein correction, hoisted branch
+    const uint64_t r2 = f2_pack(dv.r, dv.r), ns2 = f2_pack(-dv.s, -dv.s);
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) {
+      const uint64_t xv = f2_pack(x[i], x[i + 1]);
+      const uint64_t q0 = f2_mul(xv, r2);
+      const uint64_t e = f2_fma(q0, ns2, xv);
+      f2_unpack(f2_fma(e, r2, q0), x[i], x[i + 1]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) x[i] = __fdiv_rn(x[i], dv.s);
+  }
+  uint8_t* dst = codes + r * 128;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = j * 16;
+    const uint4 w = make_uint4(e4m3x4(x[e], x[e + 1], x[e + 2], x[e + 3]), e4m3x4(x[e + 4], x[e + 5], x[e + 6], x[e + 7]),
+                               e4m3x4(x[e + 8], x[e + 9], x[e + 10], x[e + 11]),
+                               e4m3x4(x[e + 12], x[e + 13], x[e + 14], x[e + 15]));
+    const int piece = half * 4 + j;
+    *reinterpret_cast<uint4*>(dst + ((piece ^ (r & 7)) << 4)) = w;
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (t == 0) {
+    tma_store_4d(is_q ? &out_q : &out_k, codes, 0, head, blk * ROWS, b);
+    tma_store_commit();
+    tma_store_wait_all();
+  }
 }
 
 // V block (b, kv head, 128 rows) for head dim 128; thread c owns channel c.
@@ -608,8 +588,7 @@ cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps
   for (int phase = 0; phase < 2; ++phase) {
     if (fast_qk) {
       if (phase == 0 || !a.block_mode) {
-        const int grid = nqk < 2 * sm_count ? nqk : 2 * sm_count;
-        qk128_kernel<<<grid, 128, QK128_SMEM, s>>>(maps->in_q, maps->in_k, maps->out_q, maps->out_k, a, phase);
+        qk128_kernel<<<nqk, 256, QK128_SMEM, s>>>(maps->in_q, maps->in_k, maps->out_q, maps->out_k, a, phase);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
       }
       v128_kernel<<<nv, 128, V128_SMEM, s>>>(maps->in_v, a, phase);
