@@ -40,7 +40,7 @@ __all__ = [
     "splitmix64", "hadamard_signs", "sylvester", "fwht_f32", "rotate_f32",
     "E4M3_MAX", "e4m3_decode", "e4m3_encode", "e4m3_table",
     "fp8_quant_block_rows", "fp8_prepass", "fp8_attention_emulated",
-    "P_FP8_MULT", "Q_BLOCK", "K_BLOCK",
+    "P_FP8_MULT", "P_FP8_LAZY_LOG2", "Q_BLOCK", "K_BLOCK",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -202,7 +202,9 @@ def attention_flops(B: int, H: int, N: int, d: int, causal: bool) -> float:
 _M64 = (1 << 64) - 1
 Q_BLOCK = 128      # rows of Q per quantisation block (one scale per block)
 K_BLOCK = 128      # rows of K per quantisation block
-P_FP8_MULT = 256.0  # P in [0,1] is multiplied by 2^8 before its e4m3 cast
+P_FP8_LAZY_LOG2 = 4.0  # FP8 P: the running maximum is raised only when a block
+                       # maximum exceeds it by more than this (log2 units)
+P_FP8_MULT = 16.0      # = 2^(8 - P_FP8_LAZY_LOG2): P <= 2^4 maps to codes <= 256
 
 
 def splitmix64(x: int) -> int:
@@ -383,13 +385,18 @@ def fp8_attention_emulated(pre: dict, causal: bool = False, scale: float | None 
     softmax: stream score tiles, keep a running maximum and normaliser), over
     key blocks of ``block_n`` in order, in fp64:
       t_j   = (Q8 K8^T)_ij * scale * log2(e) * sq(row block) * sk(key block)
-      m'    = max(m, max_j t_j);  p_j = 2^(t_j - m')
-      l     = l * 2^(m - m') + sum_j p_j            (l from unquantised p)
-      acc   = acc * 2^(m - m') + sum_j e4m3(256 p_j) * V8_j
-      O     = acc * sv / (256 l),  lse = (m + log2 l) * ln 2
-    The P quantisation (multiplier 256, l from unquantised p) is our reading;
-    parity unpinned beyond the special cases tested (a single key block equals
-    a direct evaluation; uniform scores give the mean of dequantised V).
+      b     = max_j t_j;  m' = b if b > m + tau else m     (tau = P_FP8_LAZY_LOG2)
+      p_j   = 2^(t_j - m')                               (so p_j <= 2^tau)
+      l     = l * 2^(m - m') + sum_j p_j                 (l from unquantised p)
+      acc   = acc * 2^(m - m') + sum_j e4m3(M p_j) * V8_j  (M = P_FP8_MULT = 2^(8-tau))
+      O     = acc * sv / (M l),  lse = (m + log2 l) * ln 2
+    The lazy maximum is the same online softmax with a stale reference point:
+    O and lse do not depend on m in exact arithmetic, only the e4m3 grid P
+    lands on does. The P quantisation (lazy margin 2^4, multiplier 2^4, l from
+    unquantised p) is our reading; parity unpinned beyond the special cases
+    tested (a single key block equals a direct evaluation; blocks after one
+    that holds the row maximum reproduce the single-block result; uniform
+    scores give the mean of dequantised V).
     ``rows`` = (b, h, i) arrays; default all rows. Returns o [R,d], lse [R].
     ``quantize_p=False`` keeps p unquantised (then the result is the exact
     softmax attention of the dequantised inputs, for any ``block_n``).
@@ -426,7 +433,8 @@ def fp8_attention_emulated(pre: dict, causal: bool = False, scale: float | None 
             ks = np.array([sk[b, hk, j // K_BLOCK] if block else sk[0] for j in keys])
             raw = k8[b, j0:j1, hk, :] @ q8[b, i, h, :]
             t = raw * scale * log2e * qs * ks
-            m_new = max(m, t.max())
+            bmax = t.max()
+            m_new = bmax if bmax > m + P_FP8_LAZY_LOG2 else m
             alpha = 2.0 ** (m - m_new) if m != -np.inf else 0.0
             p = 2.0 ** (t - m_new)
             l = l * alpha + p.sum()

@@ -353,3 +353,51 @@ def test_fp8_emulation_uniform_scores():
     dv = O.e4m3_table()[pre["vt8"][0, 0]].T * pre["sv"][0, 0]
     assert np.abs(o - dv.mean(axis=0)).max() <= 1e-12
     assert np.abs(l - math.log(128)).max() <= 1e-12
+
+
+def _fp8_scores_log2(pre, scale):
+    """Per-row scores t = s * scale * log2(e) of dequantised per-tensor codes."""
+    tab = O.e4m3_table()
+    dq = tab[pre["q8"][0, :, 0]] * pre["sq"][0]
+    dk = tab[pre["k8"][0, :, 0]] * pre["sk"][0]
+    return (dq @ dk.T) * scale / math.log(2.0)
+
+
+def test_fp8_emulation_lazy_maximum_keeps_first_block_reference():
+    # every row's maximum lies in the first key block: the later blocks never
+    # raise the reference point, so the blocked result equals the single-block
+    # evaluation (same m, same e4m3 grid for P) up to summation order
+    q, k, v = gen.qkv_fixed(1, 256, 1, 1, 64, seed=8)
+    k[:, 64:] = (k[:, 64:].float() * 0.05).to(k.dtype)
+    pre = O.fp8_prepass(q, k, v, mode="tensor", rotate=False)
+    t = _fp8_scores_log2(pre, 1 / 8)
+    assert np.all(t[:, :64].max(axis=1) > t[:, 64:].max(axis=1))
+    o1, l1 = O.fp8_attention_emulated(pre, block_n=64)
+    o2, l2 = O.fp8_attention_emulated(pre, block_n=256)
+    assert np.abs(o1 - o2).max() <= 1e-12 and np.abs(l1 - l2).max() <= 1e-12
+
+
+def test_fp8_emulation_lazy_maximum_raise_rescales():
+    # the last key block exceeds the first block's maximum by more than the lazy
+    # margin for some rows, so the reference point is raised and the running
+    # sums are rescaled; without P quantisation the result is still the exact
+    # softmax of the dequantised inputs, and with it P never exceeds 2^tau
+    q, k, v = gen.qkv_fixed(1, 256, 1, 1, 64, seed=9)
+    k[:, 192:] = (k[:, 192:].float() * 6.0).to(k.dtype)
+    pre = O.fp8_prepass(q, k, v, mode="tensor", rotate=False)
+    t = _fp8_scores_log2(pre, 1 / 8)
+    assert np.any(t[:, 192:].max(axis=1) > t[:, :64].max(axis=1) + O.P_FP8_LAZY_LOG2 + 1)
+    tab = O.e4m3_table()
+    dq = (tab[pre["q8"]] * pre["sq"][0]).astype(np.float32)
+    dk = (tab[pre["k8"]] * pre["sk"][0]).astype(np.float32)
+    dv = (tab[pre["vt8"]].transpose(0, 3, 1, 2) * pre["sv"][0]).astype(np.float32)[:, :256]
+    ref_o, ref_l = O.attention_bruteforce(dq, dk, dv)
+    o, l = O.fp8_attention_emulated(pre, block_n=64, quantize_p=False)
+    assert np.abs(o - ref_o[0, :, 0]).max() <= 1e-5
+    assert np.abs(l - ref_l[0, 0]).max() <= 1e-5
+    assert O.P_FP8_MULT * 2.0 ** O.P_FP8_LAZY_LOG2 <= 256.0
+    # with P quantised (no code saturates) the result stays within e4m3
+    # rounding of P (3 mantissa bits) of the exact one
+    oq, lq = O.fp8_attention_emulated(pre, block_n=64)
+    assert np.abs(oq - ref_o[0, :, 0]).max() <= 0.05 * np.abs(dv).max()
+    assert np.abs(lq - ref_l[0, 0]).max() <= 1e-5
