@@ -34,7 +34,6 @@ struct FwdParams {
   int vt_ld;               // FP8 only: row stride (keys) of transposed V
   int fp8_block;           // FP8 only: 1 = per-block/per-channel scales, 0 = per-tensor
   float scale_log2;        // softmax scale * log2(e)
-  float out_mult;          // FP8 only: 1 / (P multiplier)
   unsigned long long timeout_ns;
   unsigned int* err;       // device error word
 };

@@ -187,7 +187,6 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* s
   p.vt_ld = ldv;
   p.fp8_block = mode == ATTN_FP8_PER_BLOCK;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.out_mult = 1.0f / 256.0f;
   p.timeout_ns = api_timeout_ns();
   p.err = err;
   cudaError_t e = launch_fwd_fp8_d128(mq, mk, mv, p, causal != 0, sm, static_cast<cudaStream_t>(stream));

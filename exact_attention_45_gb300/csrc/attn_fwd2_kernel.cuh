@@ -21,9 +21,9 @@
 //
 // Warps 0-3: softmax/correction/epilogue of tile A; warps 4-7: tile B (thread
 // r of a warpgroup owns row r = TMEM lane r); warp 8: TMA; warp 9: MMA;
-// warps 10-11 idle. The block launches at 168 registers per thread; the
-// producer warpgroup (8-11) gives registers back (72 each) and the two
-// softmax warpgroups take 208 each: 2*128*208 + 128*72 = 62464 <= 384*168.
+// warp 10: slot watcher; warp 11 idle. Every thread keeps the launch's 168
+// registers: moving registers between warpgroups (setmaxnreg) was measured to
+// slow the MMA issue loop by more than the softmax gains.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -34,7 +34,11 @@
 namespace attn45 {
 
 constexpr int SUPER_M = 2 * BLOCK_M;          // query rows per CTA work unit
-constexpr float LAZY_RESCALE_LOG2 = 8.0f;     // raise m only past this margin
+constexpr float LAZY_RESCALE_LOG2 = 8.0f;     // raise m only past this margin (16-bit P)
+// FP8 P: raise m past 2^4 only and quantise 2^4 P, so codes stay <= 256 < 448
+// (the e4m3 maximum) while probabilities down to 2^-10 of the reference keep
+// normal e4m3 codes.
+constexpr float FP8_LAZY_LOG2 = 4.0f;
 
 // Element kinds of the two-tile kernel.
 enum : int { KIND_FP16 = 0, KIND_BF16 = 1, KIND_E4M3 = 2 };
@@ -166,9 +170,10 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 // KIND_BF16 / KIND_FP16: Q, K, V in that type, V tiles MN-major (rows of
 // keys). KIND_E4M3: e4m3 codes with scales (FP8 path): S = Q8 K8^T is
 // dequantised by the per-block scalar sq * sk folded into the softmax scale,
-// P is multiplied by 256 and rounded to e4m3 for O += P V^T with V given
-// transposed (rows of channels, K-major), and the epilogue applies the V
-// channel scale and 1/256.
+// P is computed as 2^(t - m + 4) = 16 P (the multiplier folded into the
+// exponent) and rounded to e4m3 for O += P V^T with V given transposed (rows of
+// channels, K-major); l sums the same 16 P, so O / l needs no correction and
+// the epilogue applies the V channel scale; lse subtracts log2(16).
 template <int D, int BN, int STAGES, bool CAUSAL, bool VARLEN, int KIND>
 __global__ void __launch_bounds__(384, 1)
 attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -233,9 +238,6 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     else return tile2_fixed<CAUSAL>(p, t);
   };
 
-  if (warp >= 8) {
-    regs_dec<72>();
-  }
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -399,15 +401,15 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------- softmax / correction / epilogue
-    regs_inc<208>();
     const int x = warp >> 2;                           // 0 = tile A, 1 = tile B
     const int r = threadIdx.x & 127;                   // row within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t ts = tmem + lane_off + T::TMEM_S + x * BN;
     const uint32_t to = tmem + lane_off + T::TMEM_O + x * D;
-    // raise m only past this margin (FP8: P * 256 must stay <= 448, so m
-    // follows the block maxima exactly)
-    constexpr float lazy = FP8 ? 0.f : LAZY_RESCALE_LOG2;
+    // raise m only past this margin; FP8 P carries the factor 2^4 in its
+    // exponent (p_log2 below)
+    constexpr float lazy = FP8 ? FP8_LAZY_LOG2 : LAZY_RESCALE_LOG2;
+    constexpr float p_log2 = FP8 ? FP8_LAZY_LOG2 : 0.f;
     int s_cnt = 0, o_tiles = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
@@ -456,7 +458,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           mxd = fmaxf(mxd, fmaxf(s[c + 6], s[c + 7]));
         }
         const float mx = fmaxf(fmaxf(mxa, mxb), fmaxf(mxc, mxd)) * sl2;
-        // raise the running max only when it moved by more than 2^8
+        // raise the running max only when it moved by more than the margin
         const bool raise = mx > m + lazy;
         const float m_new = raise ? mx : m;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
@@ -464,7 +466,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         // p = 2^(s * scale * log2(e) - m): the affine step and the row sum run
         // as packed f32x2 operations, the exponentials on the MUFU unit
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
-        const uint64_t negm2 = f2_pack(-m_use, -m_use);
+        const uint64_t negm2 = f2_pack(p_log2 - m_use, p_log2 - m_use);
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
         for (int c = 0; c < BN; c += 4) {
@@ -486,12 +488,11 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         l = l * alpha + (sum0 + sum1);
         m = m_new;
         if constexpr (FP8) {
-          // P * 256 as e4m3, four per TMEM column
+          // 16 P as e4m3, four per TMEM column
           static_assert(BN == 128, "P tile is one 32-column store");
           uint32_t u[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            u[i] = pack_e4m3x4(s[4 * i] * 256.f, s[4 * i + 1] * 256.f, s[4 * i + 2] * 256.f, s[4 * i + 3] * 256.f);
+          for (int i = 0; i < 32; ++i) u[i] = pack_e4m3x4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
           tmem_st32(ts, u);
         } else {
 #pragma unroll
@@ -525,7 +526,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (!ok) break;
       tc_fence_after();
       const bool valid = i_row < tl.n;
-      const float inv_l = FP8 ? p.out_mult / l : 1.f / l;
+      const float inv_l = 1.f / l;
       const size_t tok = (size_t)tl.tok0 + (size_t)(valid ? i_row : 0);
       uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.o) + (tok * p.H + tl.h) * D);
       const float* svp = FP8 ? (p.fp8_block ? p.sv + ((size_t)tl.seq * p.Hkv + hk) * D : p.sv) : nullptr;
@@ -555,7 +556,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
       if (valid) {
-        const float lse = (m + lg2_approx(l)) * 0.69314718055994530942f;
+        const float lse = (m + (lg2_approx(l) - p_log2)) * 0.69314718055994530942f;
         if constexpr (VARLEN) p.lse[(size_t)tl.h * p.total + tok] = lse;
         else p.lse[((size_t)tl.seq * p.H + tl.h) * p.N + i_row] = lse;
       }
