@@ -258,7 +258,7 @@ def run_ours(args):
                    "l2": "flushed between timed iterations (512 MiB write)"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": None,
-                     "peak_source": f"{pk['source']} bf16 burst (cuBLAS)", "kernel": "attn_fwd_f16_kernel"},
+                     "peak_source": f"{pk['source']} bf16 burst (cuBLAS)", "kernel": "attn_fwd2_kernel<128,128,2,false,false,BF16>"},
         "e2e": {"value": round(e2e_flops / e2e_max / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2,
                 "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4},

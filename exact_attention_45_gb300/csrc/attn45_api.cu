@@ -120,11 +120,12 @@ int check_common(int H, int Hkv, int d, int causal, float scale, int dtype) {
 }
 
 cudaError_t launch_f16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                       const FwdParams& p, bool causal, bool varlen, bool bf16, int sm_count, cudaStream_t s) {
+                       const CUtensorMap& o, const FwdParams& p, bool causal, bool varlen, bool bf16,
+                       int sm_count, cudaStream_t s) {
   switch (d) {
-    case 64: return launch_fwd_f16_d64(q, k, v, p, causal, varlen, bf16, sm_count, s);
-    case 128: return launch_fwd_f16_d128(q, k, v, p, causal, varlen, bf16, sm_count, s);
-    default: return launch_fwd_f16_d256(q, k, v, p, causal, varlen, bf16, sm_count, s);
+    case 64: return launch_fwd_f16_d64(q, k, v, o, p, causal, varlen, bf16, sm_count, s);
+    case 128: return launch_fwd_f16_d128(q, k, v, o, p, causal, varlen, bf16, sm_count, s);
+    default: return launch_fwd_f16_d256(q, k, v, o, p, causal, varlen, bf16, sm_count, s);
   }
 }
 
@@ -215,10 +216,12 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if ((rc = device_info(&dev))) return rc;
   const int bn = f16_block_n(d);
   const CUtensorMapDataType dt = dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if ((rc = make_map(&mq, dt, 2, q, d, H, N, B, 64, BLOCK_M))) return rc;
   if ((rc = make_map(&mk, dt, 2, k, d, Hkv, N, B, 64, bn))) return rc;
   if ((rc = make_map(&mv, dt, 2, v, d, Hkv, N, B, 64, bn))) return rc;
+  // output: 64 columns x 32 rows per bulk store (one warp's rows)
+  if ((rc = make_map(&mo, dt, 2, o, d, H, N, B, 64, 32))) return rc;
   FwdParams p;
   memset(&p, 0, sizeof(p));
   p.o = o;
@@ -232,7 +235,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
   p.err = dev->err;
-  cudaError_t e = launch_f16(d, mq, mk, mv, p, causal != 0, false, dtype == ATTN_BF16, dev->sm_count,
+  cudaError_t e = launch_f16(d, mq, mk, mv, mo, p, causal != 0, false, dtype == ATTN_BF16, dev->sm_count,
                              static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
   return ATTN_OK;
@@ -275,7 +278,9 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
   p.err = dev->err;
-  cudaError_t e = launch_f16(d, mq, mk, mv, p, causal != 0, true, dtype == ATTN_BF16, dev->sm_count,
+  // varlen stores O row by row (a tile's last rows may belong to the next
+  // sequence), so the output-map argument is not read
+  cudaError_t e = launch_f16(d, mq, mk, mv, mq, p, causal != 0, true, dtype == ATTN_BF16, dev->sm_count,
                              static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_varlen launch");
   return ATTN_OK;

@@ -166,11 +166,13 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* s
   unsigned int* err = nullptr;
   if ((rc = api_device(&sm, &err))) return rc;
   const int ldv = attn_fp8_vt_ld(N);
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if ((rc = api_make_map(&mq, true, q8, d, H, N, B, 128, 128))) return rc;
   if ((rc = api_make_map(&mk, true, k8, d, Hkv, N, B, 128, 128))) return rc;
   // V^T codes: [B*Hkv][d][ldv] read as boxes of (128 keys) x (d channel rows)
   if ((rc = api_make_map_rows(&mv, vt8, ldv, d, (uint64_t)B * Hkv, 128, d))) return rc;
+  // bf16 output: 64 columns x 32 rows per bulk store (one warp's rows)
+  if ((rc = api_make_map(&mo, false, o, d, H, N, B, 64, 32))) return rc;
   FwdParams p;
   memset(&p, 0, sizeof(p));
   p.o = o;
@@ -189,7 +191,7 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* s
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = api_timeout_ns();
   p.err = err;
-  cudaError_t e = launch_fwd_fp8_d128(mq, mk, mv, p, causal != 0, sm, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_fwd_fp8_d128(mq, mk, mv, mo, p, causal != 0, sm, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return api_cuda_fail(e, "attn_fwd_fp8 launch");
   return ATTN_OK;
 }

@@ -43,7 +43,11 @@ constexpr float FP8_LAZY_LOG2 = 4.0f;
 // Element kinds of the two-tile kernel.
 enum : int { KIND_FP16 = 0, KIND_BF16 = 1, KIND_E4M3 = 2 };
 
-template <int D, int BN, int STAGES, int ELEM = 2>
+// STAGE_OUT: the epilogue stages each warp's 32 output rows (64 columns at a
+// time, 128-byte swizzle) in shared memory and writes them with bulk tensor
+// stores; without it (varlen, where a tile's last rows may belong to the next
+// sequence) every thread stores its own row.
+template <int D, int BN, int STAGES, int ELEM = 2, bool STAGE_OUT = false>
 struct Pair2Traits {
   static constexpr int NC = D * ELEM / 128;              // 128-byte chunks per Q/K row
   static constexpr int Q_CHUNK = BLOCK_M * 128;
@@ -53,7 +57,9 @@ struct Pair2Traits {
   static constexpr int OFF_Q = 0;                        // Q_A then Q_B
   static constexpr int OFF_K = 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr int OFF_BARS = OFF_V + STAGES * KV_BYTES;
+  static constexpr int OFF_STAGE = OFF_V + STAGES * KV_BYTES;  // 8 softmax warps x 4 KB
+  static constexpr int STAGE_BYTES = STAGE_OUT ? 8 * 4096 : 0;
+  static constexpr int OFF_BARS = OFF_STAGE + STAGE_BYTES;
   static constexpr int BARS_BYTES = 512;
   static constexpr int OFF_PREFIX = OFF_BARS + BARS_BYTES;
   static constexpr int SMEM_FIXED = OFF_PREFIX + 1024;
@@ -177,11 +183,13 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 template <int D, int BN, int STAGES, bool CAUSAL, bool VARLEN, int KIND>
 __global__ void __launch_bounds__(384, 1)
 attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                 const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                 const FwdParams p) {
   constexpr bool FP8 = KIND == KIND_E4M3;
   constexpr bool BF16 = KIND == KIND_BF16;
   constexpr int ELEM = FP8 ? 1 : 2;
-  using T = Pair2Traits<D, BN, STAGES, ELEM>;
+  constexpr bool STAGE_OUT = !VARLEN;
+  using T = Pair2Traits<D, BN, STAGES, ELEM, STAGE_OUT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sQ = smem + T::OFF_Q;
@@ -221,6 +229,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    if (STAGE_OUT) tma_prefetch_desc(&tmO);
   }
   int ntiles = p.ntiles;
   if constexpr (VARLEN) {
@@ -468,41 +477,36 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         const uint64_t negm2 = f2_pack(p_log2 - m_use, p_log2 - m_use);
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+        // P packed as it is produced (e4m3 quads, or 16-bit pairs), so the
+        // fp32 scores die early and the softmax fits its registers
+        static_assert(BN == 128, "P tile is one (FP8) or two (16-bit) 32-column stores");
+        constexpr int PW = FP8 ? BN / 4 : BN / 2;
+        uint32_t pk[PW];
 #pragma unroll
         for (int c = 0; c < BN; c += 4) {
           float a0, a1, b0, b1;
           f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, negm2), a0, a1);
           f2_unpack(f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, negm2), b0, b1);
-          s[c] = ex2_approx(a0);
-          s[c + 1] = ex2_approx(a1);
-          s[c + 2] = ex2_approx(b0);
-          s[c + 3] = ex2_approx(b1);
-          acc0 = f2_add(acc0, f2_pack(s[c], s[c + 1]));
-          acc1 = f2_add(acc1, f2_pack(s[c + 2], s[c + 3]));
+          a0 = ex2_approx(a0);
+          a1 = ex2_approx(a1);
+          b0 = ex2_approx(b0);
+          b1 = ex2_approx(b1);
+          acc0 = f2_add(acc0, f2_pack(a0, a1));
+          acc1 = f2_add(acc1, f2_pack(b0, b1));
+          if constexpr (FP8) {
+            pk[c / 4] = pack_e4m3x4(a0, a1, b0, b1);     // 16 P as e4m3, four per TMEM column
+          } else {
+            pk[c / 2] = pack2(a0, a1, BF16);
+            pk[c / 2 + 1] = pack2(b0, b1, BF16);
+          }
         }
         float sum0, sum1, sum2, sum3;
         f2_unpack(acc0, sum0, sum1);
         f2_unpack(acc1, sum2, sum3);
-        sum0 = (sum0 + sum1) + (sum2 + sum3);
-        sum1 = 0.f;
-        l = l * alpha + (sum0 + sum1);
+        l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
         m = m_new;
-        if constexpr (FP8) {
-          // 16 P as e4m3, four per TMEM column
-          static_assert(BN == 128, "P tile is one 32-column store");
-          uint32_t u[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = pack_e4m3x4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
-          tmem_st32(ts, u);
-        } else {
-#pragma unroll
-          for (int c = 0; c < BN / 64; ++c) {
-            uint32_t u[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = pack2(s[c * 64 + 2 * i], s[c * 64 + 2 * i + 1], BF16);
-            tmem_st32(ts + c * 32, u);
-          }
-        }
+        tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        if constexpr (!FP8) tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         // correction: O_x += P(j-1) V has completed (it was issued before
         // S_x(j), whose completion we just observed), so O_x is stable.
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
@@ -549,7 +553,24 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           for (int i = 0; i < 32; ++i)
             w[i] = pack2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l, BF16);
         }
-        if (valid) {
+        if constexpr (STAGE_OUT) {
+          // this warp's 32 rows x 64 columns: 128-byte rows, 16-byte chunk i of
+          // row `lane` at chunk position i ^ (lane % 8) (the bulk tensor
+          // store's 128-byte swizzle; conflict-free shared stores), then one
+          // bulk store; rows past the sequence end are clipped by the copy
+          const uint32_t stg = smem_u32(smem + T::OFF_STAGE + warp * 4096);
+          if (lane == 0) tma_store_wait_read();     // previous use of the buffer
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            st_shared_v4(stg + lane * 128 + ((i ^ (lane & 7)) << 4), w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(&tmO, smem + T::OFF_STAGE + warp * 4096, c * 64, tl.h, row0 + (warp & 3) * 32, tl.tma_b);
+            tma_store_commit();
+          }
+        } else if (valid) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             orow[c * 8 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
@@ -561,6 +582,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         else p.lse[((size_t)tl.seq * p.H + tl.h) * p.N + i_row] = lse;
       }
     }
+    if (STAGE_OUT && lane == 0) tma_store_wait_all();   // no bulk store outlives the CTA
   }
 
   tc_fence_before();

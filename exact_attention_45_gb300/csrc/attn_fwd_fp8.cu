@@ -4,8 +4,8 @@
 
 namespace attn45 {
 cudaError_t launch_fwd_fp8_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                const FwdParams& p, bool causal, int sm_count, cudaStream_t s) {
-  if (causal) return launch_pair<128, 128, 4, true, false, KIND_E4M3>(q, k, v, p, sm_count, s);
-  return launch_pair<128, 128, 4, false, false, KIND_E4M3>(q, k, v, p, sm_count, s);
+                                const CUtensorMap& o, const FwdParams& p, bool causal, int sm_count, cudaStream_t s) {
+  if (causal) return launch_pair<128, 128, 4, true, false, KIND_E4M3>(q, k, v, o, p, sm_count, s);
+  return launch_pair<128, 128, 4, false, false, KIND_E4M3>(q, k, v, o, p, sm_count, s);
 }
 }  // namespace attn45

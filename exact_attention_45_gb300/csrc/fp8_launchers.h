@@ -6,7 +6,8 @@
 
 namespace attn45 {
 // q, k: e4m3 maps {d, heads, N, B} with 128 x 128-byte boxes; v: V^T map
-// {ldv, d, B*Hkv, 1} with 128-key x d-row boxes.
+// {ldv, d, B*Hkv, 1} with 128-key x d-row boxes; o: bf16 output map {d, H, N,
+// B} with 64-element x 32-row boxes.
 cudaError_t launch_fwd_fp8_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                const FwdParams& p, bool causal, int sm_count, cudaStream_t s);
+                                const CUtensorMap& o, const FwdParams& p, bool causal, int sm_count, cudaStream_t s);
 }  // namespace attn45

@@ -19,7 +19,8 @@ inline int persistent_grid(const FwdParams& p, bool varlen, int rows_per_unit, i
   return (int)(units < sm_count ? units : sm_count);
 }
 
-// One 128-row query tile per CTA (used for head dim 256).
+// One 128-row query tile per CTA (used for head dim 256; O leaves through plain
+// stores, so it takes no output map).
 template <int D, int BN, int ST, bool CAUSAL, bool VARLEN, bool BF16>
 cudaError_t launch_f16_single(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, FwdParams p,
                               int sm_count, cudaStream_t stream) {
@@ -36,31 +37,31 @@ cudaError_t launch_f16_single(const CUtensorMap& q, const CUtensorMap& k, const 
 
 // Two 128-row query tiles per CTA (head dims 64 and 128).
 template <int D, int BN, int ST, bool CAUSAL, bool VARLEN, int KIND>
-cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, FwdParams p,
-                        int sm_count, cudaStream_t stream) {
+cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
+                        FwdParams p, int sm_count, cudaStream_t stream) {
   static_assert(BN == f16_block_n(D), "tensor-map box height and kernel BN must agree");
-  using T = Pair2Traits<D, BN, ST, KIND == KIND_E4M3 ? 1 : 2>;
+  using T = Pair2Traits<D, BN, ST, KIND == KIND_E4M3 ? 1 : 2, !VARLEN>;
   auto kern = attn_fwd2_kernel<D, BN, ST, CAUSAL, VARLEN, KIND>;
   const int grid = persistent_grid(p, VARLEN, SUPER_M, sm_count, &p.ntiles);
   const int smem = T::SMEM_FIXED + (VARLEN ? 4 * (p.nseq + 1) : 0);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 384, smem, stream>>>(q, k, v, p);
+  kern<<<grid, 384, smem, stream>>>(q, k, v, o, p);
   return cudaGetLastError();
 }
 
 template <int D, int BN, int ST, bool PAIR, bool CA, bool VL, bool BF>
-cudaError_t launch_f16_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p,
-                           int sm_count, cudaStream_t s) {
-  if constexpr (PAIR) return launch_pair<D, BN, ST, CA, VL, BF ? KIND_BF16 : KIND_FP16>(q, k, v, p, sm_count, s);
+cudaError_t launch_f16_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
+                           const FwdParams& p, int sm_count, cudaStream_t s) {
+  if constexpr (PAIR) return launch_pair<D, BN, ST, CA, VL, BF ? KIND_BF16 : KIND_FP16>(q, k, v, o, p, sm_count, s);
   else return launch_f16_single<D, BN, ST, CA, VL, BF>(q, k, v, p, sm_count, s);
 }
 
 template <int D, int BN, int ST, bool PAIR>
 cudaError_t launch_f16_dispatch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                const FwdParams& p, bool causal, bool varlen, bool bf16, int sm_count,
+                                const CUtensorMap& o, const FwdParams& p, bool causal, bool varlen, bool bf16, int sm_count,
                                 cudaStream_t s) {
-#define ATTN45_L(CA, VL, BF) return launch_f16_one<D, BN, ST, PAIR, CA, VL, BF>(q, k, v, p, sm_count, s)
+#define ATTN45_L(CA, VL, BF) return launch_f16_one<D, BN, ST, PAIR, CA, VL, BF>(q, k, v, o, p, sm_count, s)
   if (causal) {
     if (varlen) { if (bf16) ATTN45_L(true, true, true); else ATTN45_L(true, true, false); }
     else        { if (bf16) ATTN45_L(true, false, true); else ATTN45_L(true, false, false); }
