@@ -202,9 +202,9 @@ def attention_flops(B: int, H: int, N: int, d: int, causal: bool) -> float:
 _M64 = (1 << 64) - 1
 Q_BLOCK = 128      # rows of Q per quantisation block (one scale per block)
 K_BLOCK = 128      # rows of K per quantisation block
-P_FP8_LAZY_LOG2 = 4.0  # FP8 P: the running maximum is raised only when a block
+P_FP8_LAZY_LOG2 = 8.0  # FP8 P: the running maximum is raised only when a block
                        # maximum exceeds it by more than this (log2 units)
-P_FP8_MULT = 16.0      # = 2^(8 - P_FP8_LAZY_LOG2): P <= 2^4 maps to codes <= 256
+P_FP8_MULT = 1.0       # = 2^(8 - P_FP8_LAZY_LOG2): P <= 2^8 maps to codes <= 256
 
 
 def splitmix64(x: int) -> int:
@@ -392,8 +392,8 @@ def fp8_attention_emulated(pre: dict, causal: bool = False, scale: float | None 
       O     = acc * sv / (M l),  lse = (m + log2 l) * ln 2
     The lazy maximum is the same online softmax with a stale reference point:
     O and lse do not depend on m in exact arithmetic, only the e4m3 grid P
-    lands on does. The P quantisation (lazy margin 2^4, multiplier 2^4, l from
-    unquantised p) is our reading; parity unpinned beyond the special cases
+    lands on does. The P quantisation (lazy margin 2^8, the same as the 16-bit
+    path's, multiplier 1, l from unquantised p) is our reading; parity unpinned beyond the special cases
     tested (a single key block equals a direct evaluation; blocks after one
     that holds the row maximum reproduce the single-block result; uniform
     scores give the mean of dequantised V).
