@@ -34,11 +34,9 @@
 namespace attn45 {
 
 constexpr int SUPER_M = 2 * BLOCK_M;          // query rows per CTA work unit
-constexpr float LAZY_RESCALE_LOG2 = 8.0f;     // raise m only past this margin (16-bit P)
-// FP8 P: raise m past 2^4 only and quantise 2^4 P, so codes stay <= 256 < 448
-// (the e4m3 maximum) while probabilities down to 2^-10 of the reference keep
-// normal e4m3 codes.
-constexpr float FP8_LAZY_LOG2 = 4.0f;
+// Raise m only past this margin (log2 units). P <= 2^8 then fits 16-bit P and
+// encodes to e4m3 without saturation (codes <= 256 < 448) for the FP8 path.
+constexpr float LAZY_RESCALE_LOG2 = 8.0f;
 
 // Element kinds of the two-tile kernel.
 enum : int { KIND_FP16 = 0, KIND_BF16 = 1, KIND_E4M3 = 2 };
@@ -176,10 +174,9 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 // KIND_BF16 / KIND_FP16: Q, K, V in that type, V tiles MN-major (rows of
 // keys). KIND_E4M3: e4m3 codes with scales (FP8 path): S = Q8 K8^T is
 // dequantised by the per-block scalar sq * sk folded into the softmax scale,
-// P is computed as 2^(t - m + 4) = 16 P (the multiplier folded into the
-// exponent) and rounded to e4m3 for O += P V^T with V given transposed (rows of
-// channels, K-major); l sums the same 16 P, so O / l needs no correction and
-// the epilogue applies the V channel scale; lse subtracts log2(16).
+// P (<= 2^8 under the lazy maximum) is rounded to e4m3 for O += P V^T with V
+// given transposed (rows of channels, K-major), and the epilogue applies the
+// V channel scale.
 template <int D, int BN, int STAGES, bool CAUSAL, bool VARLEN, int KIND>
 __global__ void __launch_bounds__(384, 1)
 attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -189,6 +186,10 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   constexpr bool BF16 = KIND == KIND_BF16;
   constexpr int ELEM = FP8 ? 1 : 2;
   constexpr bool STAGE_OUT = !VARLEN;
+  // Slot watcher (16-bit kinds): measured to help when the GEMMs are long
+  // (BF16/FP16) and to cost a little with the shorter FP8 GEMMs, where the MMA
+  // thread waits for the slot itself.
+  constexpr bool WATCH = !FP8;
   using T = Pair2Traits<D, BN, STAGES, ELEM, STAGE_OUT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -215,7 +216,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
     // tile A's P-ready barrier also carries "slot j has landed" from the
     // watcher warp, so the MMA thread waits once for both
-    mbar_init(&bars->p_full[0], 129);
+    mbar_init(&bars->p_full[0], WATCH ? 129 : 128);
     mbar_init(&bars->p_full[1], 128);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -330,11 +331,11 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             if (!ok) continue;
             const bool pv = j >= 1 && j - 1 < nb[x];
             int& pc = x == 0 ? p_cnt0 : p_cnt1;
-            if (pv) {
+            if (x == 0 && (!WATCH || !pv))
+              ok = mbar_wait(&bars->slot_full[st], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);
+            if (ok && pv) {
               ok = mbar_wait(&bars->p_full[x], pc & 1, tmo, abort_flag, p.err);
               ++pc;
-            } else if (x == 0) {
-              ok = mbar_wait(&bars->slot_full[st], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);
             }
             if (!ok) continue;
             tc_fence_after();
@@ -378,7 +379,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       mbar_wait_drain(&bars->mma_done, 0, tmo, p.err);
     }
     __syncwarp();
-  } else if (warp == 10) {
+  } else if (warp == 10 && WATCH) {
     // ------------------------------------------------------------ slot watcher
     // For every slot j >= 1 that tile A consumes together with P_A(j-1), wait
     // until its K/V data has landed and add one arrival to tile A's P-ready
@@ -415,10 +416,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t ts = tmem + lane_off + T::TMEM_S + x * BN;
     const uint32_t to = tmem + lane_off + T::TMEM_O + x * D;
-    // raise m only past this margin; FP8 P carries the factor 2^4 in its
-    // exponent (p_log2 below)
-    constexpr float lazy = FP8 ? FP8_LAZY_LOG2 : LAZY_RESCALE_LOG2;
-    constexpr float p_log2 = FP8 ? FP8_LAZY_LOG2 : 0.f;
+    constexpr float lazy = LAZY_RESCALE_LOG2;
     int s_cnt = 0, o_tiles = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
@@ -475,7 +473,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         // p = 2^(s * scale * log2(e) - m): the affine step and the row sum run
         // as packed f32x2 operations, the exponentials on the MUFU unit
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
-        const uint64_t negm2 = f2_pack(p_log2 - m_use, p_log2 - m_use);
+        const uint64_t negm2 = f2_pack(-m_use, -m_use);
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
         // P packed as it is produced (e4m3 quads, or 16-bit pairs), so the
         // fp32 scores die early and the softmax fits its registers
@@ -494,10 +492,12 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           acc0 = f2_add(acc0, f2_pack(a0, a1));
           acc1 = f2_add(acc1, f2_pack(b0, b1));
           if constexpr (FP8) {
-            pk[c / 4] = pack_e4m3x4(a0, a1, b0, b1);     // 16 P as e4m3, four per TMEM column
+            pk[c / 4] = pack_e4m3x4(a0, a1, b0, b1);     // P as e4m3, four per TMEM column
           } else {
             pk[c / 2] = pack2(a0, a1, BF16);
             pk[c / 2 + 1] = pack2(b0, b1, BF16);
+            // first 64 keys' P leave for TMEM halfway (keeps register use down)
+            if (c == 60) tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
           }
         }
         float sum0, sum1, sum2, sum3;
@@ -505,8 +505,11 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         f2_unpack(acc1, sum2, sum3);
         l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
         m = m_new;
-        tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        if constexpr (!FP8) tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        if constexpr (FP8) tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        else tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        // the stores read their source registers asynchronously: completing
+        // them here frees those registers for the (rare) correction below
+        tmem_st_wait();
         // correction: O_x += P(j-1) V has completed (it was issued before
         // S_x(j), whose completion we just observed), so O_x is stable.
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
@@ -519,8 +522,8 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             tmem_st32(to + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
             tmem_st32(to + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
           }
+          tmem_st_wait();
         }
-        tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->p_full[x]);
       }
@@ -577,7 +580,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
       if (valid) {
-        const float lse = (m + (lg2_approx(l) - p_log2)) * 0.69314718055994530942f;
+        const float lse = (m + lg2_approx(l)) * 0.69314718055994530942f;
         if constexpr (VARLEN) p.lse[(size_t)tl.h * p.total + tok] = lse;
         else p.lse[((size_t)tl.seq * p.H + tl.h) * p.N + i_row] = lse;
       }
