@@ -12,6 +12,9 @@ Contents
   in ``attn_oracle.c``; any subset of rows, fixed-length or packed varlen.
 * ``attention_bruteforce`` -- an independent numpy float64 statement that
   materialises the whole score matrix; for tiny shapes only.
+* ``attention_decode`` / ``combine_partials`` / ``decode_split_ranges`` --
+  one query token per (sequence, head) over a key/value cache, and the merge
+  of results computed over disjoint key ranges (split-KV decode).
 * FP8 pieces, each following the FP8 technique of "FlashAttention-3: Fast and
   Accurate Attention with Asynchrony and Low-precision" (abstract, technique
   (3): block quantization and incoherent processing):
@@ -37,6 +40,7 @@ import numpy as np
 
 __all__ = [
     "build", "attention", "attention_bruteforce", "attention_flops",
+    "attention_decode", "combine_partials", "decode_split_ranges",
     "splitmix64", "hadamard_signs", "sylvester", "fwht_f32", "rotate_f32",
     "E4M3_MAX", "e4m3_decode", "e4m3_encode", "e4m3_table",
     "fp8_quant_block_rows", "fp8_prepass", "fp8_attention_emulated",
@@ -183,6 +187,76 @@ def attention_bruteforce(q, k, v, causal: bool = False, scale: float | None = No
             o[b, :, h, :] = (W / Z) @ vf[b, :, h // g, :]
             lse[b, h, :] = (mx + np.log(Z))[:, 0]
     return o, lse
+
+
+def attention_decode(q, k_cache, v_cache, seqlens, scale: float | None = None):
+    """fp64 attention of one query token per (sequence b, query head h) over
+    the first ``seqlens[b]`` keys of its KV head's cache (decode phase: the
+    FlashAttention-3 page's references [49] "Lean attention ... decode-phase
+    of transformers" and [51] "Fast Transformer Decoding: One Write-Head is
+    All You Need"). The plain definition, one row at a time:
+        s_j = scale * q[b,h] . k[b,j,hk];  m = max_j s_j;  w_j = exp(s_j - m)
+        o[b,h] = sum_j w_j v[b,j,hk] / sum_j w_j;  lse[b,h] = m + ln sum_j w_j
+    with hk = h // (H / Hkv). q [B,H,d]; caches [B,Nmax,Hkv,d]; an empty
+    cache (seqlens[b] == 0) gives o = 0 and lse = -inf (an empty sum).
+    Returns o [B,H,d] and lse [B,H] (natural log, scale included), fp64.
+    """
+    qf = _f32(q).astype(np.float64)
+    kf = _f32(k_cache).astype(np.float64)
+    vf = _f32(v_cache).astype(np.float64)
+    B, H, d = qf.shape
+    Hkv = kf.shape[2]
+    g = H // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = np.zeros((B, H, d))
+    lse = np.full((B, H), -np.inf)
+    for b in range(B):
+        n = int(seqlens[b])
+        if n == 0:
+            continue
+        for h in range(H):
+            hk = h // g
+            s = scale * (kf[b, :n, hk, :] @ qf[b, h])
+            m = s.max()
+            w = np.exp(s - m)
+            o[b, h] = (w @ vf[b, :n, hk, :]) / w.sum()
+            lse[b, h] = m + math.log(w.sum())
+    return o, lse
+
+
+def combine_partials(o_parts, lse_parts):
+    """Merge attention results over disjoint key subsets into the result over
+    their union. The online softmax's rescaling step ("Related papers:
+    FlashAttention-4" page, online-softmax teaser: a running maximum and
+    normaliser let partial results be rescaled and summed), applied once
+    across subsets: with L = ln sum_s exp(lse_s),
+        lse = L,   o = sum_s exp(lse_s - L) o_s.
+    Computed as L = m + ln sum_s exp(lse_s - m), m = max_s lse_s. Subsets with
+    lse_s = -inf (no keys) weigh 0; if every subset is empty, o = 0 and
+    lse = -inf. o_parts [S, ..., d], lse_parts [S, ...]; fp64 results.
+    """
+    op = np.asarray(o_parts, np.float64)
+    lp = np.asarray(lse_parts, np.float64)
+    m = lp.max(axis=0)
+    mm = np.where(np.isfinite(m), m, 0.0)
+    w = np.exp(lp - mm)                       # exp(-inf) = 0 for empty subsets
+    tot = w.sum(axis=0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lse = np.where(tot > 0, mm + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)
+        o = np.where(tot[..., None] > 0, (w[..., None] * op).sum(axis=0) / np.where(tot > 0, tot, 1.0)[..., None], 0.0)
+    return o, lse
+
+
+def decode_split_ranges(seqlen: int, nmax: int, num_splits: int, block: int = 128):
+    """Key ranges [s0, s1) of the ``num_splits`` splits of one sequence: the
+    cache length ``nmax`` is cut into equal chunks of ceil(nmax / num_splits)
+    keys rounded up to ``block``; split s covers [s*chunk, (s+1)*chunk)
+    clipped to [0, seqlen) and is empty past the sequence end (our reading:
+    the pages fix no split rule)."""
+    chunk = -(-nmax // num_splits)
+    chunk = -(-chunk // block) * block
+    return [(min(s * chunk, seqlen), min((s + 1) * chunk, seqlen)) for s in range(num_splits)]
 
 
 def attention_flops(B: int, H: int, N: int, d: int, causal: bool) -> float:

@@ -401,3 +401,84 @@ def test_fp8_emulation_lazy_maximum_raise_rescales():
     oq, lq = O.fp8_attention_emulated(pre, block_n=64)
     assert np.abs(oq - ref_o[0, :, 0]).max() <= 0.05 * np.abs(dv).max()
     assert np.abs(lq - ref_l[0, 0]).max() <= 1e-5
+
+
+# ---------------------------------------------------------------- decode and split-KV combine
+
+def _decode_case(B=3, H=8, Hkv=2, nmax=700, d=64, seed=0):
+    q, _, _ = gen.qkv_fixed(B, 1, H, Hkv, d, seed=seed)
+    _, k, v = gen.qkv_fixed(B, nmax, Hkv, Hkv, d, seed=seed + 1)
+    return q[:, 0], k, v
+
+
+def test_decode_equals_last_causal_row_of_the_c_oracle():
+    # the last query row of a causal square problem attends to every key:
+    # the numpy decode statement must agree with the C core on it
+    B, N, H, Hkv, d = 2, 333, 6, 3, 64
+    q, k, v = gen.qkv_fixed(B, N, H, Hkv, d, seed=5)
+    rows = (np.repeat(np.arange(B), H), np.tile(np.arange(H), B), np.full(B * H, N - 1))
+    o_ref, l_ref = O.attention(q, k, v, causal=True, rows=rows)
+    o, l = O.attention_decode(q[:, N - 1], k, v, np.full(B, N))
+    assert np.abs(o.reshape(-1, d) - o_ref).max() <= 1e-12
+    assert np.abs(l.reshape(-1) - l_ref).max() <= 1e-12
+
+
+def test_decode_uniform_scores_and_empty_cache():
+    q, k, v = _decode_case()
+    q = torch.zeros_like(q)
+    n = np.array([1, 250, 0])
+    o, l = O.attention_decode(q, k, v, n)
+    vf = v.double().numpy()
+    for b in range(2):
+        for h in range(8):
+            assert np.abs(o[b, h] - vf[b, :n[b], h // 4].mean(axis=0)).max() <= 1e-12
+            assert abs(l[b, h] - math.log(n[b])) <= 1e-12
+    assert np.all(o[2] == 0) and np.all(l[2] == -np.inf)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+def test_split_then_combine_equals_unsplit(splits):
+    q, k, v = _decode_case(nmax=700)
+    n = np.array([700, 129, 1])
+    o_full, l_full = O.attention_decode(q, k, v, n)
+    parts_o, parts_l = [], []
+    for s in range(splits):
+        op = np.zeros_like(o_full)
+        lp = np.full_like(l_full, -np.inf)
+        for b in range(3):
+            s0, s1 = O.decode_split_ranges(int(n[b]), 700, splits)[s]
+            o_b, l_b = O.attention_decode(q[b:b + 1], k[b:b + 1, s0:], v[b:b + 1, s0:], [s1 - s0])
+            op[b], lp[b] = o_b[0], l_b[0]
+        parts_o.append(op)
+        parts_l.append(lp)
+    o, l = O.combine_partials(np.stack(parts_o), np.stack(parts_l))
+    assert np.abs(o - o_full).max() <= 1e-12
+    assert np.abs(l - l_full).max() <= 1e-12
+
+
+def test_combine_shift_invariance_and_empty_parts():
+    rng = np.random.default_rng(3)
+    o_parts = rng.standard_normal((4, 5, 16))
+    lse_parts = rng.standard_normal((4, 5)) * 3
+    o, l = O.combine_partials(o_parts, lse_parts)
+    # adding a constant to every lse shifts the result's lse and leaves o (no overflow at 1e3)
+    o2, l2 = O.combine_partials(o_parts, lse_parts + 1000.0)
+    assert np.abs(o2 - o).max() <= 1e-12 and np.abs(l2 - (l + 1000.0)).max() <= 1e-9
+    # an empty part weighs nothing; a single part is returned unchanged; all empty gives o = 0, lse = -inf
+    lp = lse_parts.copy()
+    lp[2] = -np.inf
+    o3, l3 = O.combine_partials(o_parts, lp)
+    o4, l4 = O.combine_partials(np.delete(o_parts, 2, 0), np.delete(lse_parts, 2, 0))
+    assert np.abs(o3 - o4).max() <= 1e-12 and np.abs(l3 - l4).max() <= 1e-12
+    o5, l5 = O.combine_partials(o_parts[:1], lse_parts[:1])
+    assert np.abs(o5 - o_parts[0]).max() <= 1e-15 and np.abs(l5 - lse_parts[0]).max() <= 1e-15
+    o6, l6 = O.combine_partials(o_parts, np.full_like(lse_parts, -np.inf))
+    assert np.all(o6 == 0) and np.all(l6 == -np.inf)
+
+
+def test_decode_split_ranges_cover_the_sequence():
+    for n, nmax, s in [(1, 1, 1), (700, 700, 3), (129, 700, 7), (32768, 32768, 13), (5, 4096, 40)]:
+        r = O.decode_split_ranges(n, nmax, s)
+        assert len(r) == s and r[0][0] == 0 and r[-1][1] == n
+        assert all(a[1] == b[0] for a, b in zip(r, r[1:]))
+        assert all(s0 % 128 == 0 or s0 == n for s0, _ in r)
