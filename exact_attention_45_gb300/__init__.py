@@ -12,6 +12,8 @@ Functions carry the C names:
 * ``attn_fp8_prepass(q, k, v, mode="block", rotate=True, hadamard_seed=0)``
 * ``attn_fwd_fp8(pre, causal=False, scale=None, ...)``
 * ``attn_fwd_fp8_auto(q, k, v, workspace=None, ...)``
+* ``attn_decode(q, k_cache, v_cache, seqlens, num_splits=0, ...)``
+* ``attn_combine(o_parts, lse_parts, dtype=torch.bfloat16)``
 * ``attn_get_device_error()``, ``attn_set_wait_timeout_ns(ns)``
 
 ``capi()`` returns the raw ctypes handle (pointer-and-size arguments).
@@ -31,7 +33,8 @@ __all__ = [
     "AttnError", "capi", "library_path",
     "attn_fwd", "attn_fwd_varlen", "attn_fp8_prepass", "attn_fwd_fp8", "attn_fwd_fp8_auto",
     "attn_fp8_workspace_size", "attn_fp8_vt_ld", "attn_get_device_error", "attn_set_wait_timeout_ns",
-    "attn_debug_timeout_probe", "EXPORTED_SYMBOLS",
+    "attn_debug_timeout_probe", "attn_decode", "attn_decode_num_splits", "attn_decode_workspace_size",
+    "attn_combine", "EXPORTED_SYMBOLS",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
@@ -43,7 +46,7 @@ EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_fwd_varlen", "attn_fp8_vt_ld", "attn_fp8_prepass", "attn_fwd_fp8",
     "attn_fp8_workspace_size", "attn_fwd_fp8_auto", "attn_fwd_fp8_auto_noalloc", "attn_get_device_error",
     "attn_set_wait_timeout_ns", "attn_debug_timeout_probe", "attn_status_string", "attn_last_error_message",
-    "attn_version",
+    "attn_version", "attn_decode", "attn_decode_num_splits", "attn_decode_workspace_size", "attn_combine",
 )
 
 
@@ -89,6 +92,10 @@ def capi(build_if_missing: bool = True):
             "attn_status_string": ([I], ctypes.c_char_p),
             "attn_last_error_message": ([], ctypes.c_char_p),
             "attn_version": ([], I),
+            "attn_decode": ([P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, I, P], I),
+            "attn_decode_num_splits": ([I, I, I], I),
+            "attn_decode_workspace_size": ([I, I, I, I], SZ),
+            "attn_combine": ([P, P, P, P, I, I, I, I, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -233,6 +240,56 @@ def attn_fwd_fp8_auto(q, k, v, causal: bool = False, scale: float | None = None,
                                     workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
                                     int(bool(causal)), scale, _FP8_MODE[mode], int(bool(rotate)),
                                     int(hadamard_seed), _stream(stream)))
+    return out, lse
+
+
+def attn_decode_num_splits(B: int, Hkv: int, Nmax: int) -> int:
+    return int(capi().attn_decode_num_splits(B, Hkv, Nmax))
+
+
+def attn_decode_workspace_size(B: int, H: int, d: int, num_splits: int) -> int:
+    return int(capi().attn_decode_workspace_size(B, H, d, num_splits))
+
+
+def attn_decode(q, k_cache, v_cache, seqlens, num_splits: int = 0, scale: float | None = None, workspace=None,
+                out=None, lse=None, stream=None):
+    """Split-KV decode: q [B,H,d], caches [B,Nmax,Hkv,d], int32 seqlens [B] on the device -> O [B,H,d], lse [B,H]."""
+    _need(q, "q", ndim=3)
+    _need(k_cache, "k_cache", q.dtype, 4)
+    _need(v_cache, "v_cache", q.dtype, 4)
+    _need(seqlens, "seqlens", torch.int32, 1)
+    if q.dtype not in _DTYPE:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "q must be bf16 or fp16")
+    B, H, d = q.shape
+    Nmax, Hkv = k_cache.shape[1], k_cache.shape[2]
+    if k_cache.shape != (B, Nmax, Hkv, d) or v_cache.shape != k_cache.shape or seqlens.numel() != B:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "caches must be [B,Nmax,Hkv,d] and seqlens [B]")
+    if num_splits <= 0:
+        num_splits = attn_decode_num_splits(B, Hkv, Nmax)
+    need = attn_decode_workspace_size(B, H, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check(capi().attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(out), _ptr(lse),
+                              _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, Hkv, Nmax, d,
+                              num_splits, scale, _DTYPE[q.dtype], _stream(stream)))
+    return out, lse
+
+
+def attn_combine(o_parts, lse_parts, dtype=torch.bfloat16, out=None, lse=None, stream=None):
+    """Merge fp32 partials o_parts [S, rows..., d], lse_parts [S, rows...] -> O (dtype), lse."""
+    _need(o_parts, "o_parts", torch.float32)
+    _need(lse_parts, "lse_parts", torch.float32)
+    S, d = o_parts.shape[0], o_parts.shape[-1]
+    rows = lse_parts[0].numel()
+    if lse_parts.shape[0] != S or o_parts.numel() != S * rows * d:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "o_parts must be [S, rows..., d] matching lse_parts [S, rows...]")
+    out = torch.empty(o_parts.shape[1:], dtype=dtype, device=o_parts.device) if out is None else out
+    lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=o_parts.device) if lse is None else lse
+    _check(capi().attn_combine(_ptr(o_parts), _ptr(lse_parts), _ptr(out), _ptr(lse), S, rows, d, _DTYPE[dtype],
+                               _stream(stream)))
     return out, lse
 
 

@@ -286,6 +286,97 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   return ATTN_OK;
 }
 
+int attn_decode_num_splits(int B, int Hkv, int Nmax) {
+  if (B < 1 || Hkv < 1 || Nmax < 1) return 1;
+  DeviceInfo* dev = nullptr;
+  const int sm = device_info(&dev) == ATTN_OK ? dev->sm_count : 148;
+  // about two units per SM (one CTA per SM walks them), at most one split
+  // per 128 cached keys
+  const long long units = (long long)B * Hkv;
+  long long s = (2LL * sm + units - 1) / units;
+  const long long smax = (Nmax + 127) / 128;
+  if (s > smax) s = smax;
+  return (int)(s < 1 ? 1 : s);
+}
+
+size_t attn_decode_workspace_size(int B, int H, int d, int num_splits) {
+  if (B < 1 || H < 1 || d < 1 || num_splits < 1) return 0;
+  const size_t rows = (size_t)num_splits * B * H;
+  return ((rows * d * 4 + 255) & ~size_t(255)) + ((rows * 4 + 255) & ~size_t(255));
+}
+
+int attn_combine(const float* o_parts, const float* lse_parts, void* o, float* lse, int num_splits, int rows, int d,
+                 int dtype, void* stream) {
+  if (num_splits < 1 || rows < 0 || d < 1 || d > 1024) return fail(ATTN_ERR_INVALID_ARG, "need num_splits >= 1, rows >= 0, 1 <= d <= 1024");
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return fail(ATTN_ERR_INVALID_ARG, "dtype %d unknown", dtype);
+  if (rows == 0) return ATTN_OK;
+  if (!o_parts || !lse_parts || !o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(o_parts, 4) || !aligned(lse_parts, 4) || !aligned(o, 2) || !aligned(lse, 4))
+    return fail(ATTN_ERR_INVALID_ARG, "misaligned pointer");
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  cudaError_t e = launch_combine(o_parts, lse_parts, o, lse, num_splits, rows, d, dtype == ATTN_BF16,
+                                 static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attn_combine launch");
+  return ATTN_OK;
+}
+
+int attn_decode(const void* q, const void* k_cache, const void* v_cache, const int* seqlens, void* o, float* lse,
+                void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int Nmax, int d, int num_splits,
+                float scale, int dtype, void* stream) {
+  int rc = check_common(H, Hkv, d, 0, scale, dtype);
+  if (rc) return rc;
+  if (d == 256) return fail(ATTN_ERR_UNSUPPORTED, "decode is built for head dims 64 and 128");
+  if (H / Hkv > BLOCK_M) return fail(ATTN_ERR_UNSUPPORTED, "at most %d query heads per KV head", BLOCK_M);
+  if (B < 1 || Nmax < 1) return fail(ATTN_ERR_INVALID_ARG, "need B >= 1 and Nmax >= 1 (B=%d Nmax=%d)", B, Nmax);
+  if (num_splits <= 0) num_splits = attn_decode_num_splits(B, Hkv, Nmax);
+  if ((long long)B * Hkv * num_splits > 0x7fffffffLL || (long long)B * Nmax > 0x7fffffffLL)
+    return fail(ATTN_ERR_INVALID_ARG, "problem too large for int32 indexing");
+  if (!q || !k_cache || !v_cache || !seqlens || !o || !lse || !workspace) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(seqlens, 4) || !aligned(workspace, 256))
+    return fail(ATTN_ERR_INVALID_ARG, "q, caches, o 16-byte, lse and seqlens 4-byte, workspace 256-byte aligned");
+  const size_t need = attn_decode_workspace_size(B, H, d, num_splits);
+  if (workspace_bytes < need) return fail(ATTN_ERR_INVALID_ARG, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  const CUtensorMapDataType dt = dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap mq, mk, mv;
+  // q [B][H][d] as rows of one "head": the query heads of a KV head are rows
+  if ((rc = make_map(&mq, dt, 2, q, d, 1, H, B, 64, BLOCK_M))) return rc;
+  if ((rc = make_map(&mk, dt, 2, k_cache, d, Hkv, Nmax, B, 64, 128))) return rc;
+  if ((rc = make_map(&mv, dt, 2, v_cache, d, Hkv, Nmax, B, 64, 128))) return rc;
+  const size_t rows = (size_t)num_splits * B * H;
+  float* o_parts = static_cast<float*>(workspace);
+  float* lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * d * 4 + 255) & ~size_t(255)));
+  int chunk = (Nmax + num_splits - 1) / num_splits;
+  chunk = (chunk + 127) / 128 * 128;
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.o = o_parts;
+  p.lse = lse_parts;
+  p.nseq = B;
+  p.N = Nmax;
+  p.total = B * Nmax;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.group = H / Hkv;
+  p.ntiles = B * Hkv * num_splits;
+  p.seqlens = seqlens;
+  p.num_splits = num_splits;
+  p.split_chunk = chunk;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = g_timeout_ns;
+  p.err = dev->err;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode_f16(d, mq, mk, mv, p, dtype == ATTN_BF16, dev->sm_count, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_decode launch");
+  e = launch_combine(o_parts, lse_parts, o, lse, num_splits, B * H, d, dtype == ATTN_BF16, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_decode combine launch");
+  return ATTN_OK;
+}
+
 int attn_get_device_error(void* stream) {
   DeviceInfo* dev = nullptr;
   int rc = device_info(&dev);

@@ -34,6 +34,9 @@ struct FwdParams {
   int vt_ld;               // FP8 only: row stride (keys) of transposed V
   int fp8_block;           // FP8 only: 1 = per-block/per-channel scales, 0 = per-tensor
   float scale_log2;        // softmax scale * log2(e)
+  const int* seqlens;      // decode only: cached keys per sequence (device, nseq)
+  int num_splits;          // decode only: key-range splits per (sequence, KV head)
+  int split_chunk;         // decode only: keys per split (a multiple of 128)
   unsigned long long timeout_ns;
   unsigned int* err;       // device error word
 };

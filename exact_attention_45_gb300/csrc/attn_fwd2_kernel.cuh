@@ -79,8 +79,11 @@ struct Bars2 {
 };
 static_assert(sizeof(Bars2) <= 512, "barrier block");
 
+// n: keys (= query rows for the square problems); nq: query rows.
+// Decode units: h is the KV head, the rows are its H/Hkv query heads
+// (qrow0 = first of them), n the keys of split `split`.
 struct Tile2 {
-  int seq, h, sblk, n, tok0, tma_row0, tma_b;
+  int seq, h, sblk, n, nq, qrow0, split, tok0, tma_row0, tma_b;
 };
 
 // Fixed length. Non-causal: head-major (all super tiles of one (b,h) are
@@ -102,6 +105,9 @@ __device__ __forceinline__ Tile2 tile2_fixed(const FwdParams& p, int t) {
   T.seq = bh / p.H;
   T.h = bh % p.H;
   T.n = p.N;
+  T.nq = p.N;
+  T.qrow0 = 0;
+  T.split = 0;
   T.tok0 = T.seq * p.N;
   T.tma_row0 = 0;
   T.tma_b = T.seq;
@@ -121,11 +127,37 @@ __device__ __forceinline__ Tile2 tile2_varlen(const FwdParams& p, const int* pre
   const int r = t - prefix[lo];
   const int a = __ldg(p.cu_seqlens + lo), b = __ldg(p.cu_seqlens + lo + 1);
   T.n = b - a;
+  T.nq = T.n;
+  T.qrow0 = 0;
+  T.split = 0;
   T.sblk = ceil_div(T.n, SUPER_M) - 1 - r / p.H;
   T.h = r % p.H;
   T.tok0 = a;
   T.tma_row0 = a;
   T.tma_b = 0;
+  return T;
+}
+
+// Split-KV decode: unit t -> (sequence b, KV head, split s), splits fastest.
+// The unit's rows are the H/Hkv query heads of that KV head (one token each),
+// its keys the cache range [s * chunk, (s + 1) * chunk) clipped to the
+// sequence's cached length (clamped to the cache size); a split past the end
+// has no keys.
+__device__ __forceinline__ Tile2 tile2_decode(const FwdParams& p, int t) {
+  Tile2 T;
+  T.split = t % p.num_splits;
+  const int bk = t / p.num_splits;
+  T.seq = bk / p.Hkv;
+  T.h = bk % p.Hkv;
+  const int n = min(max(__ldg(p.seqlens + T.seq), 0), p.N);
+  const int s0 = min(T.split * p.split_chunk, n);
+  T.n = min(s0 + p.split_chunk, n) - s0;
+  T.nq = p.group;
+  T.qrow0 = T.h * p.group;
+  T.sblk = 0;
+  T.tok0 = 0;
+  T.tma_row0 = s0;
+  T.tma_b = T.seq;
   return T;
 }
 
@@ -158,7 +190,7 @@ __device__ __forceinline__ void build_varlen_prefix2(const FwdParams& p, int* pr
 template <bool CAUSAL, int BN>
 __device__ __forceinline__ int tile2_blocks(const Tile2& tl, int x) {
   const int r0 = tl.sblk * SUPER_M + x * BLOCK_M;
-  if (r0 >= tl.n) return 0;
+  if (r0 >= tl.nq) return 0;
   int kend = tl.n;
   if (CAUSAL) kend = min(kend, r0 + BLOCK_M);
   return ceil_div(kend, BN);
@@ -177,7 +209,7 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 // P (<= 2^8 under the lazy maximum) is rounded to e4m3 for O += P V^T with V
 // given transposed (rows of channels, K-major), and the epilogue applies the
 // V channel scale.
-template <int D, int BN, int STAGES, bool CAUSAL, bool VARLEN, int KIND>
+template <int D, int BN, int STAGES, bool CAUSAL, bool VARLEN, int KIND, bool DECODE = false>
 __global__ void __launch_bounds__(384, 1)
 attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -185,7 +217,8 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   constexpr bool FP8 = KIND == KIND_E4M3;
   constexpr bool BF16 = KIND == KIND_BF16;
   constexpr int ELEM = FP8 ? 1 : 2;
-  constexpr bool STAGE_OUT = !VARLEN;
+  constexpr bool STAGE_OUT = !VARLEN && !DECODE;
+  static_assert(!DECODE || (!CAUSAL && !VARLEN && !FP8), "decode units are non-causal 16-bit fixed-cache");
   // Slot watcher (16-bit kinds): measured to help when the GEMMs are long
   // (BF16/FP16) and to cost a little with the shorter FP8 GEMMs, where the MMA
   // thread waits for the slot itself.
@@ -245,27 +278,39 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
   auto get_tile = [&](int t) -> Tile2 {
     if constexpr (VARLEN) return tile2_varlen(p, prefix, t);
+    else if constexpr (DECODE) return tile2_decode(p, t);
     else return tile2_fixed<CAUSAL>(p, t);
   };
+  // KV head of a unit (decode units carry it directly)
+  auto kv_head = [&](const Tile2& tl) -> int { return DECODE ? tl.h : tl.h / p.group; };
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int slot_it = 0, tile_i = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tile_i) {
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         const Tile2 tl = get_tile(t);
-        const int hk = tl.h / p.group;
+        const int hk = kv_head(tl);
         const int nkv = max(tile2_blocks<CAUSAL, BN>(tl, 0), tile2_blocks<CAUSAL, BN>(tl, 1));
+        if (nkv == 0) continue;                       // a decode split past the sequence end
         ok = mbar_wait(&bars->q_empty, (tile_i & 1) ^ 1, tmo, abort_flag, p.err);
         if (!ok) break;
         mbar_expect_tx(&bars->q_full, 2 * T::Q_BYTES);
 #pragma unroll
         for (int x = 0; x < 2; ++x)
 #pragma unroll
-          for (int c = 0; c < T::NC; ++c)
-            tma_load_4d(&tmQ, &bars->q_full, sQ + x * T::Q_BYTES + c * T::Q_CHUNK, c * (128 / ELEM), tl.h,
-                        tl.tma_row0 + tl.sblk * SUPER_M + x * BLOCK_M, tl.tma_b);
+          for (int c = 0; c < T::NC; ++c) {
+            // Q map: {d, H, N, B} rows of one head; decode: {d, 1, H, B}, the
+            // rows being the query heads of the unit's KV head
+            if constexpr (DECODE)
+              tma_load_4d(&tmQ, &bars->q_full, sQ + x * T::Q_BYTES + c * T::Q_CHUNK, c * (128 / ELEM), 0,
+                          tl.qrow0 + x * BLOCK_M, tl.tma_b);
+            else
+              tma_load_4d(&tmQ, &bars->q_full, sQ + x * T::Q_BYTES + c * T::Q_CHUNK, c * (128 / ELEM), tl.h,
+                          tl.tma_row0 + tl.sblk * SUPER_M + x * BLOCK_M, tl.tma_b);
+          }
+        ++tile_i;
         // slot j: K_j (j < nkv) and V_{j-1} (j >= 1)
         for (int j = 0; j <= nkv; ++j, ++slot_it) {
           const int st = slot_it % STAGES;
@@ -316,11 +361,13 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       int slot_it = 0, tile_i = 0;
       int p_cnt0 = 0, p_cnt1 = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tile_i) {
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         const Tile2 tl = get_tile(t);
         const int nb[2] = {tile2_blocks<CAUSAL, BN>(tl, 0), tile2_blocks<CAUSAL, BN>(tl, 1)};
         const int nkv = max(nb[0], nb[1]);
+        if (nkv == 0) continue;
         ok = mbar_wait(&bars->q_full, tile_i & 1, tmo, abort_flag, p.err);
+        ++tile_i;
         if (!ok) break;
         for (int j = 0; j <= nkv && ok; ++j, ++slot_it) {
           const int st = slot_it % STAGES;
@@ -392,6 +439,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const Tile2 tl = get_tile(t);
         const int na = tile2_blocks<CAUSAL, BN>(tl, 0);
         const int nkv = max(na, tile2_blocks<CAUSAL, BN>(tl, 1));
+        if (nkv == 0) continue;                       // no slots for an empty unit
         for (int j = 0; j <= nkv; ++j, ++slot_it) {
           // Every slot is waited for, in order, even those this warp does not
           // report: a parity wait is only unambiguous while the waiter is at
@@ -422,10 +470,15 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       const Tile2 tl = get_tile(t);
       const int nblk = tile2_blocks<CAUSAL, BN>(tl, x);
-      if (nblk == 0) continue;                        // tile B past the sequence end
       const int row0 = tl.sblk * SUPER_M + x * BLOCK_M;  // first row of this tile
       const int i_row = row0 + r;
-      const int hk = tl.h / p.group;
+      if (nblk == 0) {                                // tile B past the sequence end
+        // a decode split with no keys: its partial has lse = -inf (weight 0)
+        if (DECODE && x == 0 && i_row < tl.nq)
+          p.lse[((size_t)tl.split * p.nseq + tl.seq) * p.H + tl.qrow0 + i_row] = -INFINITY;
+        continue;
+      }
+      const int hk = kv_head(tl);
       const int nb128 = ceil_div(tl.n, BLOCK_M);      // 128-row scale blocks (FP8)
       float sq_x = 1.f;
       if constexpr (FP8)
@@ -532,7 +585,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       ++o_tiles;
       if (!ok) break;
       tc_fence_after();
-      const bool valid = i_row < tl.n;
+      const bool valid = i_row < tl.nq;
       const float inv_l = 1.f / l;
       const size_t tok = (size_t)tl.tok0 + (size_t)(valid ? i_row : 0);
       uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.o) + (tok * p.H + tl.h) * D);
@@ -541,6 +594,18 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       for (int c = 0; c < D / 64; ++c) {
         uint32_t u[64];
         tmem_ld64(to + c * 64, u);
+        if constexpr (DECODE) {
+          // fp32 partial O of this split: [split][b][H][d]
+          if (valid) {
+            float4* prow = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) +
+                                                     (((size_t)tl.split * p.nseq + tl.seq) * p.H + tl.qrow0 + i_row) * D);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              prow[c * 16 + i] = make_float4(__uint_as_float(u[4 * i]) * inv_l, __uint_as_float(u[4 * i + 1]) * inv_l,
+                                             __uint_as_float(u[4 * i + 2]) * inv_l, __uint_as_float(u[4 * i + 3]) * inv_l);
+          }
+          continue;
+        }
         uint32_t w[32];
         if constexpr (FP8) {
 #pragma unroll
@@ -582,6 +647,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (valid) {
         const float lse = (m + lg2_approx(l)) * 0.69314718055994530942f;
         if constexpr (VARLEN) p.lse[(size_t)tl.h * p.total + tok] = lse;
+        else if constexpr (DECODE) p.lse[((size_t)tl.split * p.nseq + tl.seq) * p.H + tl.qrow0 + i_row] = lse;
         else p.lse[((size_t)tl.seq * p.H + tl.h) * p.N + i_row] = lse;
       }
     }

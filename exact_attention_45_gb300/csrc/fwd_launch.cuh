@@ -36,13 +36,15 @@ cudaError_t launch_f16_single(const CUtensorMap& q, const CUtensorMap& k, const 
 }
 
 // Two 128-row query tiles per CTA (head dims 64 and 128).
-template <int D, int BN, int ST, bool CAUSAL, bool VARLEN, int KIND>
+// DECODE: p.ntiles holds the number of (sequence, KV head, split) units.
+template <int D, int BN, int ST, bool CAUSAL, bool VARLEN, int KIND, bool DECODE = false>
 cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
                         FwdParams p, int sm_count, cudaStream_t stream) {
   static_assert(BN == f16_block_n(D), "tensor-map box height and kernel BN must agree");
-  using T = Pair2Traits<D, BN, ST, KIND == KIND_E4M3 ? 1 : 2, !VARLEN>;
-  auto kern = attn_fwd2_kernel<D, BN, ST, CAUSAL, VARLEN, KIND>;
-  const int grid = persistent_grid(p, VARLEN, SUPER_M, sm_count, &p.ntiles);
+  using T = Pair2Traits<D, BN, ST, KIND == KIND_E4M3 ? 1 : 2, !VARLEN && !DECODE>;
+  auto kern = attn_fwd2_kernel<D, BN, ST, CAUSAL, VARLEN, KIND, DECODE>;
+  const int grid = DECODE ? (p.ntiles < sm_count ? p.ntiles : sm_count)
+                          : persistent_grid(p, VARLEN, SUPER_M, sm_count, &p.ntiles);
   const int smem = T::SMEM_FIXED + (VARLEN ? 4 * (p.nseq + 1) : 0);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

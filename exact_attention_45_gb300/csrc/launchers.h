@@ -19,6 +19,15 @@ cudaError_t launch_fwd_f16_d64(const CUtensorMap& q, const CUtensorMap& k, const
 cudaError_t launch_fwd_f16_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                 const CUtensorMap& o, const FwdParams& p, bool causal, bool varlen, bool bf16, int sm_count,
                                 cudaStream_t s);
+// Split-KV decode units of the two-tile kernel (head dim 64 or 128): fp32
+// partial O [splits][B][H][d] to p.o and partial lse [splits][B][H] to p.lse.
+cudaError_t launch_decode_f16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                              const FwdParams& p, bool bf16, int sm_count, cudaStream_t s);
+// Merge of per-split partials into O (bf16/fp16) and lse; splits with lse =
+// -inf are skipped without reading their O.
+cudaError_t launch_combine(const float* o_parts, const float* lse_parts, void* o, float* lse, int splits, int rows,
+                           int d, bool bf16, cudaStream_t s);
+
 cudaError_t launch_fwd_f16_d256(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                 const CUtensorMap& o, const FwdParams& p, bool causal, bool varlen, bool bf16, int sm_count,
                                 cudaStream_t s);

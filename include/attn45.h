@@ -157,6 +157,47 @@ ATTN45_API int attn_fwd_fp8_auto_noalloc(const void* q, const void* k, const voi
                                          int H, int Hkv, int N, int d, int causal, float scale, int mode, int rotate,
                                          uint64_t hadamard_seed, void* stream);
 
+/*
+ * Split-KV decode: one query token per sequence and query head attends to
+ * the first seqlens[b] keys of its KV head's cache (the decode phase of
+ * "FlashAttention-3 ..." references [49] and [51]; the merge of partial
+ * results is the online-softmax rescaling of the "Related papers:
+ * FlashAttention-4" page's online-softmax teaser, applied across splits).
+ *
+ * attn_decode -- BF16/FP16, head dim 64 or 128, H % Hkv == 0, H/Hkv <= 128.
+ *   q [B, H, d]; k_cache, v_cache [B, Nmax, Hkv, d] (BSHD, contiguous);
+ *   seqlens: DEVICE int32[B], keys cached per sequence (values are clamped to
+ *   [0, Nmax]; 0 gives o = 0 and lse = -inf); o [B, H, d] in q's dtype;
+ *   lse [B, H] fp32 (natural log, scale included).
+ *   The cache of every sequence is cut into num_splits ranges of
+ *   ceil(Nmax / num_splits) keys rounded up to 128; each (sequence, KV head,
+ *   range) is one unit of the forward kernel, which writes a partial O (fp32,
+ *   normalised by its own sum) and its lse into `workspace`; a second kernel
+ *   merges the partials. num_splits <= 0 picks attn_decode_num_splits().
+ *   workspace: DEVICE, 256-byte aligned, >= attn_decode_workspace_size(B, H,
+ *   d, num_splits) bytes, owned by the caller; its contents are scratch.
+ */
+ATTN45_API int attn_decode(const void* q, const void* k_cache, const void* v_cache, const int* seqlens, void* o,
+                           float* lse, void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int Nmax,
+                           int d, int num_splits, float scale, int dtype, void* stream);
+/* Splits attn_decode picks for num_splits <= 0: about two units per SM, at
+ * most one split per 128 cached keys. */
+ATTN45_API int attn_decode_num_splits(int B, int Hkv, int Nmax);
+/* Bytes of attn_decode's workspace: fp32 partial O [splits][B][H][d] then
+ * partial lse [splits][B][H], each padded to 256 bytes; 0 for bad sizes. */
+ATTN45_API size_t attn_decode_workspace_size(int B, int H, int d, int num_splits);
+/*
+ * attn_combine -- merge results computed over disjoint key subsets:
+ *   o_parts [num_splits][rows][d] fp32, lse_parts [num_splits][rows] fp32
+ *   (DEVICE) -> o [rows][d] (dtype: ATTN_BF16 / ATTN_FP16), lse [rows] fp32:
+ *   lse = m + ln sum_s exp(lse_s - m) (m = max_s lse_s),
+ *   o = sum_s exp(lse_s - lse) o_s. A part with lse_s = -inf is skipped
+ *   without reading its o_s; if every part is empty, o = 0 and lse = -inf.
+ *   1 <= d <= 1024; o 2-byte, other pointers 4-byte aligned.
+ */
+ATTN45_API int attn_combine(const float* o_parts, const float* lse_parts, void* o, float* lse, int num_splits,
+                            int rows, int d, int dtype, void* stream);
+
 /* Synchronises `stream`, reads and clears the current device's error word.
  * ATTN_OK, ATTN_ERR_TIMEOUT (a bounded device wait gave up) or ATTN_ERR_CUDA. */
 ATTN45_API int attn_get_device_error(void* stream);

@@ -1,0 +1,97 @@
+"""GPU parity of split-KV decode and the partial-result combine (through the
+C ABI) against the fp64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs as gen
+import oracle as O
+from _attn_util import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(B, H, Hkv, nmax, d, seed, dtype="bf16"):
+    q, _, _ = gen.qkv_fixed(B, 1, H, Hkv, d, seed=seed, dtype=dtype)
+    _, k, v = gen.qkv_fixed(B, nmax, Hkv, Hkv, d, seed=seed + 1, dtype=dtype)
+    return q[:, 0].contiguous(), k, v
+
+
+def _run(q, k, v, seqlens, splits):
+    import exact_attention_45_gb300 as A
+    sl = torch.as_tensor(np.asarray(seqlens), dtype=torch.int32).cuda()
+    o, lse = A.attn_decode(q.cuda(), k.cuda(), v.cuda(), sl, num_splits=splits)
+    torch.cuda.synchronize()
+    assert A.attn_get_device_error() == 0
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("splits", [1, 3, 0, 40])
+def test_decode_matches_oracle(d, splits):
+    B, H, Hkv, nmax = 5, 8, 2, 1000
+    seqlens = [1, 127, 128, 129, 1000]
+    q, k, v = _inputs(B, H, Hkv, nmax, d, seed=d + splits)
+    o, lse = _run(q, k, v, seqlens, splits)
+    o_ref, l_ref = O.attention_decode(q, k, v, seqlens)
+    assert_close(o, o_ref, lse, l_ref, what=f"decode d{d} splits={splits}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_fp16_and_mha(d):
+    q, k, v = _inputs(3, 4, 4, 300, d, seed=7, dtype="fp16")
+    seqlens = [300, 2, 257]
+    o, lse = _run(q, k, v, seqlens, 2)
+    o_ref, l_ref = O.attention_decode(q, k, v, seqlens)
+    assert_close(o, o_ref, lse, l_ref, what="decode fp16 MHA")
+
+
+def test_decode_single_key_and_empty_cache():
+    q, k, v = _inputs(2, 4, 1, 256, 128, seed=3)
+    o, lse = _run(q, k, v, [1, 0], 3)
+    assert np.array_equal(o[0], np.repeat(v[0, 0].float().numpy(), 4, axis=0))
+    assert np.all(o[1] == 0) and np.all(lse[1] == -np.inf)
+    o_ref, l_ref = O.attention_decode(q, k, v, [1, 0])
+    assert np.abs(lse[0] - l_ref[0]).max() <= 1e-3
+
+
+def test_decode_gqa_long_cache_full_size():
+    # 8 sequences with cached lengths uniform in [1k, 32k], H=32, Hkv=8, d=128
+    seqlens = gen.varlen_lengths(8, 1024, 32768, seed=0)
+    nmax = 32768
+    q, k, v = _inputs(8, 32, 8, nmax, 128, seed=11)
+    o, lse = _run(q, k, v, seqlens, 0)
+    o_ref, l_ref = O.attention_decode(q, k, v, seqlens)
+    assert_close(o, o_ref, lse, l_ref, what="decode GQA 32k")
+
+
+def test_combine_matches_oracle():
+    import exact_attention_45_gb300 as A
+    rng = np.random.default_rng(5)
+    S, rows, d = 6, 37, 128
+    o_parts = rng.standard_normal((S, rows, d)).astype(np.float32)
+    lse_parts = (rng.standard_normal((S, rows)) * 4).astype(np.float32)
+    lse_parts[2, :] = -np.inf
+    lse_parts[:, 5] = -np.inf              # a row with no keys at all
+    o_parts[2, :] = np.nan                 # never read: its lse is -inf
+    o, lse = A.attn_combine(torch.from_numpy(o_parts).cuda(), torch.from_numpy(lse_parts).cuda())
+    torch.cuda.synchronize()
+    op = o_parts.astype(np.float64)
+    op[2] = 0.0
+    o_ref, l_ref = O.combine_partials(op, lse_parts)
+    o_h, l_h = o.float().cpu().numpy(), lse.cpu().numpy()
+    assert np.all(o_h[5] == 0) and l_h[5] == -np.inf
+    ok = np.isfinite(l_ref)
+    assert np.abs(o_h - o_ref).max() <= 1e-2
+    assert np.abs(l_h[ok] - l_ref[ok]).max() <= 1e-4
+
+
+def test_decode_invalid_arguments():
+    import exact_attention_45_gb300 as A
+    q, k, v = _inputs(1, 2, 1, 128, 256, seed=0)
+    sl = torch.tensor([128], dtype=torch.int32).cuda()
+    with pytest.raises(A.AttnError) as e:
+        A.attn_decode(q.cuda(), k.cuda(), v.cuda(), sl)
+    assert e.value.status == A.ATTN_ERR_UNSUPPORTED
