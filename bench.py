@@ -267,6 +267,8 @@ def run_ours(args):
     }
     if rank == 0 and not args.no_fp8:
         line["fp8"] = fp8_measure(min(args.steps, 50), args.warmup)
+    if rank == 0 and not args.no_decode:
+        line["decode"] = decode_measure(min(args.steps, 50), args.warmup)
     if rank == 0 and not args.no_cpu_baseline:
         rate, threads, sample = cpu_oracle_rate(w, budget_s=args.cpu_budget)
         line["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -275,6 +277,62 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1 and dist.is_initialized():
         dist.destroy_process_group()
+
+
+DECODE = {"workload": "split-KV decode bf16 d128", "B": 8, "H": 32, "Hkv": 8, "d": 128, "Nmax": 32768,
+          "seqlens": "uniform integers in [1024, 32768], seed 0"}
+
+
+def decode_measure(steps: int, warmup: int, seed: int = 0, splits: int = 0):
+    """Split-KV decode (one query token per sequence and head over a KV cache)
+    on the GQA shape of the varlen configuration: 8 sequences with cached
+    lengths uniform in [1k, 32k], H=32, Hkv=8, d=128, bf16. HBM-bound: the
+    algorithmic bytes are the cached K and V rows each sequence attends to,
+    plus q, o and lse. Timed with CUDA events, L2 flushed before each call."""
+    import torch
+
+    import attn_inputs as gen
+    import exact_attention_45_gb300 as A
+    w = DECODE
+    B, H, Hkv, d, nmax = w["B"], w["H"], w["Hkv"], w["d"], w["Nmax"]
+    seqlens = gen.varlen_lengths(B, 1024, nmax, seed=seed)
+    q, _, _ = gen.qkv_fixed(B, 1, H, Hkv, d, seed=seed)
+    _, k, v = gen.qkv_fixed(B, nmax, Hkv, Hkv, d, seed=seed + 1)
+    q, k, v = q[:, 0].contiguous().cuda(), k.cuda(), v.cuda()
+    sl = torch.as_tensor(seqlens, dtype=torch.int32).cuda()
+    splits = splits if splits > 0 else A.attn_decode_num_splits(B, Hkv, nmax)
+    ws = torch.empty(A.attn_decode_workspace_size(B, H, d, splits), dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    call = lambda: A.attn_decode(q, k, v, sl, num_splits=splits, workspace=ws, out=o, lse=lse)
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    ev = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    if A.attn_get_device_error() != 0:
+        raise RuntimeError("device error in the decode path")
+    t = sum(a.elapsed_time(b) for a, b in ev) / steps / 1e3
+    kv_bytes = int(sum(seqlens)) * Hkv * d * 2 * 2
+    io_bytes = q.numel() * 2 * 2 + lse.numel() * 4
+    pk = peaks()
+    gbs = (kv_bytes + io_bytes) / t / 1e9
+    return {
+        "config": {k2: v2 for k2, v2 in w.items()}, "num_splits": splits, "ms": round(t * 1e3, 4),
+        "tokens_per_s": round(B * H / t, 1),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs / pk["hbm_gbs"], 4), "algorithmic_bytes": kv_bytes + io_bytes,
+                     "peak_source": f"{pk['source']} copy"},
+        "gpu_launches_per_step": 2,
+    }
 
 
 def fp8_measure(steps: int, warmup: int, seed: int = 0):
@@ -424,8 +482,10 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 sub-measurement")
-    ap.add_argument("--workload", choices=("bf16", "fp8"), default="bf16",
-                    help="fp8: run only the FP8 path (pre-pass + forward), e.g. for profiling")
+    ap.add_argument("--no-decode", action="store_true", help="skip the split-KV decode sub-measurement")
+    ap.add_argument("--decode-splits", type=int, default=0, help="decode key-range splits (0 = automatic)")
+    ap.add_argument("--workload", choices=("bf16", "fp8", "decode"), default="bf16",
+                    help="fp8 / decode: run only that path (e.g. for profiling)")
     ap.add_argument("--sweep", action="store_true", help="time every BF16 configuration instead")
     ap.add_argument("--sweep-reps", type=int, default=20)
     args = ap.parse_args(argv)
@@ -434,6 +494,10 @@ def main(argv=None):
         import torch
         torch.cuda.set_device(0)
         print(json.dumps({"fp8": fp8_measure(args.steps, args.warmup)}), flush=True)
+    elif args.workload == "decode":
+        import torch
+        torch.cuda.set_device(0)
+        print(json.dumps({"decode": decode_measure(args.steps, args.warmup, splits=args.decode_splits)}), flush=True)
     elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":

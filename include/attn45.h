@@ -180,7 +180,7 @@ ATTN45_API int attn_fwd_fp8_auto_noalloc(const void* q, const void* k, const voi
 ATTN45_API int attn_decode(const void* q, const void* k_cache, const void* v_cache, const int* seqlens, void* o,
                            float* lse, void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int Nmax,
                            int d, int num_splits, float scale, int dtype, void* stream);
-/* Splits attn_decode picks for num_splits <= 0: about two units per SM, at
+/* Splits attn_decode picks for num_splits <= 0: about four units per SM, at
  * most one split per 128 cached keys. */
 ATTN45_API int attn_decode_num_splits(int B, int Hkv, int Nmax);
 /* Bytes of attn_decode's workspace: fp32 partial O [splits][B][H][d] then
