@@ -12,6 +12,7 @@ Contents
   in ``attn_oracle.c``; any subset of rows, fixed-length or packed varlen.
 * ``attention_bruteforce`` -- an independent numpy float64 statement that
   materialises the whole score matrix; for tiny shapes only.
+* ``attention_backward`` -- fp64 gradients dQ, dK, dV of sum(dO * O).
 * ``attention_decode`` / ``combine_partials`` / ``decode_split_ranges`` --
   one query token per (sequence, head) over a key/value cache, and the merge
   of results computed over disjoint key ranges (split-KV decode).
@@ -40,7 +41,7 @@ import numpy as np
 
 __all__ = [
     "build", "attention", "attention_bruteforce", "attention_flops",
-    "attention_decode", "combine_partials", "decode_split_ranges",
+    "attention_decode", "combine_partials", "decode_split_ranges", "attention_backward",
     "splitmix64", "hadamard_signs", "sylvester", "fwht_f32", "rotate_f32",
     "E4M3_MAX", "e4m3_decode", "e4m3_encode", "e4m3_table",
     "fp8_quant_block_rows", "fp8_prepass", "fp8_attention_emulated",
@@ -187,6 +188,50 @@ def attention_bruteforce(q, k, v, causal: bool = False, scale: float | None = No
             o[b, :, h, :] = (W / Z) @ vf[b, :, h // g, :]
             lse[b, h, :] = (mx + np.log(Z))[:, 0]
     return o, lse
+
+
+def attention_backward(q, k, v, do, causal: bool = False, scale: float | None = None):
+    """fp64 gradients of the loss sum(dO * O) with O = softmax(scale Q K^T [+ causal mask]) V.
+
+    The backward pass of the FlashAttention papers (FA1, "trains Transformers
+    faster", consumes the forward's logsumexp); written here as the plain
+    chain rule, one (b, h) at a time:
+        P  = softmax(S),  S = scale Q K^T (masked keys: P = 0)
+        dV = P^T dO                     dP = dO V^T
+        D_i = sum_c dO_ic O_ic          dS = P * (dP - D)   (row-wise D)
+        dQ = scale dS K                 dK = scale dS^T Q
+    With grouped-query attention, dK and dV of a KV head sum over the query
+    heads that share it. Inputs BSHD (q, do [B,N,H,d]; k, v [B,N,Hkv,d]);
+    returns dq, dk, dv in fp64 with the same shapes.
+    """
+    qf = _f32(q).astype(np.float64)
+    kf = _f32(k).astype(np.float64)
+    vf = _f32(v).astype(np.float64)
+    gf = _f32(do).astype(np.float64)
+    B, N, H, d = qf.shape
+    Hkv = kf.shape[2]
+    g = H // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = np.zeros_like(qf)
+    dk = np.zeros_like(kf)
+    dv = np.zeros_like(vf)
+    mask = np.tril(np.ones((N, N), dtype=bool)) if causal else np.ones((N, N), dtype=bool)
+    for b in range(B):
+        for h in range(H):
+            hk = h // g
+            Q, K, V, G = qf[b, :, h], kf[b, :, hk], vf[b, :, hk], gf[b, :, h]
+            S = np.where(mask, scale * (Q @ K.T), -np.inf)
+            P = np.exp(S - S.max(axis=1, keepdims=True))
+            P /= P.sum(axis=1, keepdims=True)
+            O = P @ V
+            dv[b, :, hk] += P.T @ G
+            dP = G @ V.T
+            D = (G * O).sum(axis=1, keepdims=True)
+            dS = P * (dP - D)
+            dq[b, :, h] = scale * (dS @ K)
+            dk[b, :, hk] += scale * (dS.T @ Q)
+    return dq, dk, dv
 
 
 def attention_decode(q, k_cache, v_cache, seqlens, scale: float | None = None):

@@ -482,3 +482,59 @@ def test_decode_split_ranges_cover_the_sequence():
         assert len(r) == s and r[0][0] == 0 and r[-1][1] == n
         assert all(a[1] == b[0] for a, b in zip(r, r[1:]))
         assert all(s0 % 128 == 0 or s0 == n for s0, _ in r)
+
+
+# ---------------------------------------------------------------- backward
+
+def _loss(q, k, v, do, causal):
+    """sum(dO * O) through the C core (an implementation independent of the backward)."""
+    B, N, H, d = q.shape
+    o, _ = O.attention(q, k, v, causal=causal)
+    return float((o * do.double().numpy()).sum())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_finite_differences_of_the_forward(causal):
+    # central differences of the C core's fp64 forward; inputs are fp32 so a
+    # perturbation is representable exactly in the widened values
+    B, N, H, Hkv, d = 1, 37, 4, 2, 16
+    q, k, v = (t.float() for t in gen.qkv_fixed(B, N, H, Hkv, d, seed=21))
+    do = gen.qkv_fixed(B, N, H, H, d, seed=22)[0].float()
+    dq, dk, dv = O.attention_backward(q, k, v, do, causal=causal)
+    rng = np.random.default_rng(0)
+    eps = 1e-3
+    for name, t, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for _ in range(6):
+            idx = tuple(int(rng.integers(0, s)) for s in t.shape)
+            tp, tm = t.clone(), t.clone()
+            tp[idx] += eps
+            tm[idx] -= eps
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = tp, tm
+            fd = (_loss(args_p["q"], args_p["k"], args_p["v"], do, causal) -
+                  _loss(args_m["q"], args_m["k"], args_m["v"], do, causal)) / (float(tp[idx]) - float(tm[idx]))
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(grad[idx])), (name, idx, fd, grad[idx])
+
+
+def test_backward_invariants():
+    # dS rows sum to zero, so dQ is unchanged when every key row is shifted by a
+    # constant vector; dV = P^T dO sums dO over queries (column sums of P^T are 1)
+    B, N, H, d = 1, 50, 2, 32
+    q, k, v = gen.qkv_fixed(B, N, H, H, d, seed=23)
+    do = gen.qkv_fixed(B, N, H, H, d, seed=24)[0]
+    dq, dk, dv = O.attention_backward(q, k, v, do)
+    u = torch.randn(d).to(k.dtype)
+    dq2, _, _ = O.attention_backward(q, (k.float() + u.float()).to(torch.float32), v, do)
+    dq_f, _, _ = O.attention_backward(q, k.float(), v, do)
+    assert np.abs(dq2 - dq_f).max() <= 1e-9
+    assert np.abs(dv.sum(axis=1) - do.double().numpy().sum(axis=1)).max() <= 1e-9
+    # GQA: dK, dV of a shared KV head are the sums over its query heads
+    qg, kg, vg = gen.qkv_fixed(1, 40, 4, 1, 16, seed=25)
+    dog = gen.qkv_fixed(1, 40, 4, 4, 16, seed=26)[0]
+    _, dkg, dvg = O.attention_backward(qg, kg, vg, dog)
+    acc_k, acc_v = 0, 0
+    for h in range(4):
+        _, dkh, dvh = O.attention_backward(qg[:, :, h:h + 1], kg, vg, dog[:, :, h:h + 1])
+        acc_k, acc_v = acc_k + dkh, acc_v + dvh
+    assert np.abs(dkg - acc_k).max() <= 1e-12 and np.abs(dvg - acc_v).max() <= 1e-12
