@@ -14,6 +14,7 @@ Functions carry the C names:
 * ``attn_fwd_fp8_auto(q, k, v, workspace=None, ...)``
 * ``attn_decode(q, k_cache, v_cache, seqlens, num_splits=0, ...)``
 * ``attn_combine(o_parts, lse_parts, dtype=torch.bfloat16)``
+* ``attn_bwd(q, k, v, o, lse, dout, causal=False, ...)``
 * ``attn_get_device_error()``, ``attn_set_wait_timeout_ns(ns)``
 
 ``capi()`` returns the raw ctypes handle (pointer-and-size arguments).
@@ -34,7 +35,7 @@ __all__ = [
     "attn_fwd", "attn_fwd_varlen", "attn_fp8_prepass", "attn_fwd_fp8", "attn_fwd_fp8_auto",
     "attn_fp8_workspace_size", "attn_fp8_vt_ld", "attn_get_device_error", "attn_set_wait_timeout_ns",
     "attn_debug_timeout_probe", "attn_decode", "attn_decode_num_splits", "attn_decode_workspace_size",
-    "attn_combine", "EXPORTED_SYMBOLS",
+    "attn_combine", "attn_bwd", "attn_bwd_workspace_size", "EXPORTED_SYMBOLS",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
@@ -47,6 +48,7 @@ EXPORTED_SYMBOLS = (
     "attn_fp8_workspace_size", "attn_fwd_fp8_auto", "attn_fwd_fp8_auto_noalloc", "attn_get_device_error",
     "attn_set_wait_timeout_ns", "attn_debug_timeout_probe", "attn_status_string", "attn_last_error_message",
     "attn_version", "attn_decode", "attn_decode_num_splits", "attn_decode_workspace_size", "attn_combine",
+    "attn_bwd", "attn_bwd_workspace_size",
 )
 
 
@@ -96,6 +98,8 @@ def capi(build_if_missing: bool = True):
             "attn_decode_num_splits": ([I, I, I], I),
             "attn_decode_workspace_size": ([I, I, I, I], SZ),
             "attn_combine": ([P, P, P, P, I, I, I, I, P], I),
+            "attn_bwd": ([P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, I, P], I),
+            "attn_bwd_workspace_size": ([I, I, I, I], SZ),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -291,6 +295,36 @@ def attn_combine(o_parts, lse_parts, dtype=torch.bfloat16, out=None, lse=None, s
     _check(capi().attn_combine(_ptr(o_parts), _ptr(lse_parts), _ptr(out), _ptr(lse), S, rows, d, _DTYPE[dtype],
                                _stream(stream)))
     return out, lse
+
+
+def attn_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(capi().attn_bwd_workspace_size(B, H, N, d))
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, workspace=None, dq=None,
+             dk=None, dv=None, stream=None):
+    """dQ, dK, dV of sum(dout * o) for the forward attn_fwd(q, k, v) that returned (o, lse)."""
+    _need(q, "q", ndim=4)
+    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _need(t, name, q.dtype, 4)
+    _need(lse, "lse", torch.float32, 3)
+    if q.dtype not in _DTYPE:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "q must be bf16 or fp16")
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape or o.shape != q.shape or dout.shape != q.shape:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "shapes must match the forward's (BSHD)")
+    need = attn_bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check(capi().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                           _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
+                           int(bool(causal)), scale, _DTYPE[q.dtype], _stream(stream)))
+    return dq, dk, dv
 
 
 def attn_get_device_error(stream=None) -> int:

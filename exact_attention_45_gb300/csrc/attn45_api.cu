@@ -14,6 +14,7 @@
 #include "attn45.h"
 #include "attn_common.cuh"
 #include "api_internal.h"
+#include "bwd_launchers.h"
 #include "launchers.h"
 #include "ptx.cuh"
 
@@ -374,6 +375,67 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
   if (e != cudaSuccess) return cuda_fail(e, "attn_decode launch");
   e = launch_combine(o_parts, lse_parts, o, lse, num_splits, B * H, d, dtype == ATTN_BF16, st);
   if (e != cudaSuccess) return cuda_fail(e, "attn_decode combine launch");
+  return ATTN_OK;
+}
+
+size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  const size_t rows = (size_t)B * N * H;
+  return ((rows * d * 4 + 255) & ~size_t(255)) + ((rows * 4 + 255) & ~size_t(255));
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+             void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+             int causal, float scale, int dtype, void* stream) {
+  int rc = check_common(H, Hkv, d, causal, scale, dtype);
+  if (rc) return rc;
+  if (d == 256) return fail(ATTN_ERR_UNSUPPORTED, "the backward is built for head dims 64 and 128");
+  if (B < 1 || N < 1) return fail(ATTN_ERR_INVALID_ARG, "need B >= 1 and N >= 1 (B=%d N=%d)", B, N);
+  if ((long long)B * N * H > 0x7fffffffLL) return fail(ATTN_ERR_INVALID_ARG, "problem too large for int32 indexing");
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(workspace, 256))
+    return fail(ATTN_ERR_INVALID_ARG, "tensors 16-byte, lse 4-byte, workspace 256-byte aligned");
+  const size_t need = attn_bwd_workspace_size(B, H, N, d);
+  if (workspace_bytes < need) return fail(ATTN_ERR_INVALID_ARG, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  const CUtensorMapDataType dt = dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap mq, mk, mv, mdo;
+  if ((rc = make_map(&mq, dt, 2, q, d, H, N, B, 64, 128))) return rc;
+  if ((rc = make_map(&mk, dt, 2, k, d, Hkv, N, B, 64, 128))) return rc;
+  if ((rc = make_map(&mv, dt, 2, v, d, Hkv, N, B, 64, 128))) return rc;
+  if ((rc = make_map(&mdo, dt, 2, dout, d, H, N, B, 64, 128))) return rc;
+  const size_t rows = (size_t)B * N * H;
+  float* dq_acc = static_cast<float*>(workspace);
+  float* dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * d * 4 + 255) & ~size_t(255)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool bf16 = dtype == ATTN_BF16;
+  cudaError_t e = cudaMemsetAsync(dq_acc, 0, rows * d * 4, st);
+  if (e != cudaSuccess) return cuda_fail(e, "zeroing the dQ accumulator");
+  e = launch_bwd_dvec(d, o, dout, dvec, B, N, H, bf16, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd row-sum launch");
+  BwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.lse = lse;
+  p.dvec = dvec;
+  p.dq_acc = dq_acc;
+  p.dk = dk;
+  p.dv = dv;
+  p.B = B;
+  p.N = N;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.group = H / Hkv;
+  p.nunits = B * Hkv * ((N + 127) / 128);
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = g_timeout_ns;
+  p.err = dev->err;
+  e = launch_bwd(d, mq, mk, mv, mdo, p, causal != 0, bf16, dev->sm_count, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
+  e = launch_bwd_dq_convert(dq_acc, dq, (long long)rows * d, bf16, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dQ conversion launch");
   return ATTN_OK;
 }
 

@@ -1,0 +1,443 @@
+// attn_bwd.cu -- BF16/FP16 attention backward (dQ, dK, dV), head dim 64/128.
+//
+// The backward pass of the FlashAttention papers (FA1: exact attention that
+// "trains Transformers faster"; it consumes the forward's logsumexp, so P is
+// recomputed from S and lse instead of stored). For a key block j of 128 keys
+// and every query block i of 128 rows that sees it (every head of the group
+// for grouped-query attention):
+//     S  = Q_i K_j^T                 P  = exp(scale S - lse_i)      (recomputed)
+//     dP = dO_i V_j^T                dS = scale P * (dP - D_i),  D_i = rowsum(dO_i * O_i)
+//     dV_j += P^T dO_i               dK_j += dS^T Q_i               dQ_i += dS K_j
+// One CTA owns a (batch, KV head, key block) unit: dV_j and dK_j stay in TMEM
+// across all its query blocks and are written once; dQ_i is produced per
+// block in TMEM and added into an fp32 accumulator in HBM with vector
+// reductions (other key blocks add to the same rows), converted at the end.
+//
+// Roles (192 threads): warps 0-3 compute (thread r owns TMEM lane r: query
+// row r for S/dP/dQ, key r for dV/dK), warp 4 lane 0 loads by TMA, warp 5
+// lane 0 issues the MMAs. TMEM: S (128 cols, reused for dQ), dP (128), dV (d),
+// dK (d). Shared memory: K_j, V_j, Q_i, dO_i tiles and the bf16 P and dS tiles
+// that feed the last three products (MN-major for P^T / dS^T, K-major for dS).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include "api_internal.h"
+#include "attn_common.cuh"
+#include "bwd_launchers.h"
+#include "ptx.cuh"
+
+namespace attn45 {
+namespace {
+
+template <int D>
+struct BwdTraits {
+  static constexpr int CHUNK = 128 * 128;            // 128 rows x 128 bytes
+  static constexpr int TILE = 128 * D * 2;           // one 128-row bf16 tile of width d
+  static constexpr int PTILE = 128 * 128 * 2;        // P or dS: 128 queries x 128 keys
+  static constexpr int OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE, OFF_DO = 3 * TILE;
+  static constexpr int OFF_P = 4 * TILE, OFF_DS = OFF_P + PTILE;
+  static constexpr int OFF_BARS = OFF_DS + PTILE;
+  static constexpr int SMEM = OFF_BARS + 256 + 1024;  // + alignment slack
+  static constexpr int T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
+};
+
+struct BwdBars {
+  uint64_t kv_full, kv_empty, qdo_full, qdo_empty, s_full, p_full, dq_full, dq_empty, dkv_full, dkv_empty, done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// kind::f16 instruction descriptor with either operand MN-major.
+__host__ __device__ constexpr uint32_t idesc_f16_ab(int M, int N, bool bf16, bool a_mn, bool b_mn) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+struct BwdUnit {
+  int b, hkv, j, i0, nI, nblk;
+};
+
+__device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int t, bool causal) {
+  BwdUnit u;
+  const int bk = p.B * p.Hkv;
+  u.j = t / bk;                       // key block; the longest (causal: j = 0) first
+  const int r = t % bk;
+  u.b = r / p.Hkv;
+  u.hkv = r % p.Hkv;
+  const int nqb = ceil_div(p.N, 128);
+  u.i0 = causal ? u.j : 0;
+  u.nI = nqb - u.i0;
+  u.nblk = u.nI * p.group;
+  return u;
+}
+
+__device__ __forceinline__ float to_f(uint32_t u) { return __uint_as_float(u); }
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+  uint32_t r;
+  if (BF16) asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(192, 1)
+attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                const BwdParams p) {
+  using T = BwdTraits<D>;
+  constexpr int NC = D / 64;                         // 128-byte chunks per row of a d-wide tile
+  constexpr int KS = D / 16;                         // K steps over d
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + T::OFF_BARS);
+  volatile int* abort_flag = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);
+    mbar_init(&bars->qdo_full, 1);
+    mbar_init(&bars->qdo_empty, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_empty, 128);
+    mbar_init(&bars->dkv_full, 1);
+    mbar_init(&bars->dkv_empty, 128);
+    mbar_init(&bars->done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmDO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const uint64_t tmo = p.timeout_ns;
+  const int nunits = p.nunits;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int unit_i = 0, blk_it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < nunits && ok; t += gridDim.x, ++unit_i) {
+        const BwdUnit u = bwd_unit(p, t, CAUSAL);
+        ok = mbar_wait(&bars->kv_empty, (unit_i & 1) ^ 1, tmo, abort_flag, p.err);
+        if (!ok) break;
+        mbar_expect_tx(&bars->kv_full, 2 * T::TILE);
+        for (int c = 0; c < NC; ++c) {
+          tma_load_4d(&tmK, &bars->kv_full, smem + T::OFF_K + c * T::CHUNK, c * 64, u.hkv, u.j * 128, u.b);
+          tma_load_4d(&tmV, &bars->kv_full, smem + T::OFF_V + c * T::CHUNK, c * 64, u.hkv, u.j * 128, u.b);
+        }
+        for (int it = 0; it < u.nblk; ++it, ++blk_it) {
+          const int h = u.hkv * p.group + it / u.nI;
+          const int i = u.i0 + it % u.nI;
+          ok = mbar_wait(&bars->qdo_empty, (blk_it & 1) ^ 1, tmo, abort_flag, p.err);
+          if (!ok) break;
+          mbar_expect_tx(&bars->qdo_full, 2 * T::TILE);
+          for (int c = 0; c < NC; ++c) {
+            tma_load_4d(&tmQ, &bars->qdo_full, smem + T::OFF_Q + c * T::CHUNK, c * 64, h, i * 128, u.b);
+            tma_load_4d(&tmDO, &bars->qdo_full, smem + T::OFF_DO + c * T::CHUNK, c * 64, h, i * 128, u.b);
+          }
+        }
+      }
+      // never leave with copies in flight
+      if (blk_it > 0) mbar_wait_drain(&bars->qdo_full, (blk_it - 1) & 1, tmo, p.err);
+      if (unit_i > 0) mbar_wait_drain(&bars->kv_full, (unit_i - 1) & 1, tmo, p.err);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_kk = idesc_f16_ab(128, 128, BF16, false, false);   // S, dP
+      constexpr uint32_t id_mm = idesc_f16_ab(128, D, BF16, true, true);       // dV, dK
+      constexpr uint32_t id_km = idesc_f16_ab(128, D, BF16, false, true);      // dQ
+      const uint32_t sk = smem_u32(smem + T::OFF_K), sv = smem_u32(smem + T::OFF_V);
+      const uint32_t sq = smem_u32(smem + T::OFF_Q), sdo = smem_u32(smem + T::OFF_DO);
+      const uint32_t sp = smem_u32(smem + T::OFF_P), sds = smem_u32(smem + T::OFF_DS);
+      int unit_i = 0, blk_it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < nunits && ok; t += gridDim.x, ++unit_i) {
+        const BwdUnit u = bwd_unit(p, t, CAUSAL);
+        ok = mbar_wait(&bars->kv_full, unit_i & 1, tmo, abort_flag, p.err);
+        for (int it = 0; it < u.nblk && ok; ++it, ++blk_it) {
+          ok = mbar_wait(&bars->qdo_full, blk_it & 1, tmo, abort_flag, p.err);
+          // S / dQ columns free once the previous block's dQ has been read
+          if (ok && blk_it > 0) ok = mbar_wait(&bars->dq_empty, (blk_it - 1) & 1, tmo, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          // S = Q_i K_j^T and dP = dO_i V_j^T (K-major operands, K = d)
+#pragma unroll
+          for (int k = 0; k < KS; ++k) {
+            const uint32_t off = (k >> 2) * T::CHUNK + (k & 3) * 32;
+            umma_f16_ss(tmem + T::T_S, sdesc_kmajor_sw128(sq + off), sdesc_kmajor_sw128(sk + off), id_kk, k > 0);
+          }
+#pragma unroll
+          for (int k = 0; k < KS; ++k) {
+            const uint32_t off = (k >> 2) * T::CHUNK + (k & 3) * 32;
+            umma_f16_ss(tmem + T::T_DP, sdesc_kmajor_sw128(sdo + off), sdesc_kmajor_sw128(sv + off), id_kk, k > 0);
+          }
+          umma_commit(&bars->s_full);
+          ok = mbar_wait(&bars->p_full, blk_it & 1, tmo, abort_flag, p.err);
+          // the previous unit's dK/dV must have been read before they restart at zero
+          if (ok && it == 0 && unit_i > 0) ok = mbar_wait(&bars->dkv_empty, (unit_i - 1) & 1, tmo, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          // dV += P^T dO_i, dK += dS^T Q_i: K = 128 query rows; A (P^T, dS^T) and
+          // B (dO_i, Q_i) MN-major: 16 query rows per step = 2048 bytes
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            umma_f16_ss(tmem + T::T_DV, sdesc_mnmajor_sw128(sp + k * 2048, T::CHUNK),
+                        sdesc_mnmajor_sw128(sdo + k * 2048, T::CHUNK), id_mm, (it > 0 || k > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            umma_f16_ss(tmem + T::T_DK, sdesc_mnmajor_sw128(sds + k * 2048, T::CHUNK),
+                        sdesc_mnmajor_sw128(sq + k * 2048, T::CHUNK), id_mm, (it > 0 || k > 0) ? 1u : 0u);
+          }
+          // dQ_i = dS K_j: A = dS K-major (K = 128 keys), B = K_j MN-major (N = d)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t aoff = (k >> 2) * T::CHUNK + (k & 3) * 32;
+            umma_f16_ss(tmem + T::T_S, sdesc_kmajor_sw128(sds + aoff), sdesc_mnmajor_sw128(sk + k * 2048, T::CHUNK),
+                        id_km, k > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars->dq_full);
+          umma_commit(&bars->qdo_empty);
+        }
+        if (!ok) break;
+        umma_commit(&bars->dkv_full);
+        umma_commit(&bars->kv_empty);
+      }
+      umma_commit(&bars->done);
+      mbar_wait_drain(&bars->done, 0, tmo, p.err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ compute warps
+    const int r = threadIdx.x;                               // TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const float scale = p.scale;
+    uint8_t* tp = smem + T::OFF_P;
+    uint8_t* tds = smem + T::OFF_DS;
+    // row r of a P/dS tile: chunk (64 keys) at +16 KB, 16-byte unit u at u ^ (r % 8)
+    const uint32_t prow = smem_u32(tp) + r * 128;
+    const uint32_t dsrow = smem_u32(tds) + r * 128;
+    int unit_i = 0, blk_it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < nunits && ok; t += gridDim.x, ++unit_i) {
+      const BwdUnit u = bwd_unit(p, t, CAUSAL);
+      for (int it = 0; it < u.nblk && ok; ++it, ++blk_it) {
+        const int h = u.hkv * p.group + it / u.nI;
+        const int i = u.i0 + it % u.nI;
+        const int qrow = i * 128 + r;
+        const bool row_ok = qrow < p.N;
+        const size_t lrow = ((size_t)u.b * p.H + h) * p.N + (row_ok ? qrow : 0);
+        const float lse2 = row_ok ? __ldg(p.lse + lrow) * 1.4426950408889634f : 0.f;
+        const float Drow = row_ok ? __ldg(p.dvec + lrow) : 0.f;
+        ok = mbar_wait(&bars->s_full, blk_it & 1, tmo, abort_flag, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        // keys of this block visible to row qrow
+        int kmax = p.N - u.j * 128;                            // keys past the end are masked
+        if (CAUSAL) kmax = min(kmax, qrow - u.j * 128 + 1);
+        if (!row_ok) kmax = 0;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {                          // 32 keys at a time
+          uint32_t su[32], du[32];
+          tmem_ld32(tmem + lane_off + T::T_S + c * 32, su);
+          tmem_ld32(tmem + lane_off + T::T_DP + c * 32, du);
+          uint32_t pw[16], dw[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int key = c * 32 + e;
+            const float p0 = key < kmax ? ex2_approx(to_f(su[e]) * sl2 - lse2) : 0.f;
+            const float p1 = key + 1 < kmax ? ex2_approx(to_f(su[e + 1]) * sl2 - lse2) : 0.f;
+            const float d0 = scale * p0 * (to_f(du[e]) - Drow);
+            const float d1 = scale * p1 * (to_f(du[e + 1]) - Drow);
+            pw[e / 2] = pack16<BF16>(p0, p1);
+            dw[e / 2] = pack16<BF16>(d0, d1);
+          }
+          // keys c*32 .. c*32+31 are 16-byte units 4c .. 4c+3 of the row (chunk c / 2)
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int unit = (c & 1) * 4 + q4;
+            const uint32_t off = (c >> 1) * T::CHUNK + ((unit ^ (r & 7)) << 4);
+            st_shared_v4(prow + off, pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
+            st_shared_v4(dsrow + off, dw[4 * q4], dw[4 * q4 + 1], dw[4 * q4 + 2], dw[4 * q4 + 3]);
+          }
+        }
+        fence_proxy_async_smem();                             // P, dS visible to the MMAs
+        tc_fence_before();
+        mbar_arrive(&bars->p_full);
+        // dQ_i rows: add into the fp32 accumulator
+        ok = mbar_wait(&bars->dq_full, blk_it & 1, tmo, abort_flag, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        float* dqrow = p.dq_acc + (((size_t)u.b * p.N + (row_ok ? qrow : 0)) * p.H + h) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t qu[32];
+          tmem_ld32(tmem + lane_off + T::T_S + c * 32, qu);
+          if (row_ok) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              red_add_v4(dqrow + c * 32 + e, to_f(qu[e]), to_f(qu[e + 1]), to_f(qu[e + 2]), to_f(qu[e + 3]));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->dq_empty);
+      }
+      if (!ok) break;
+      // unit epilogue: dK_j, dV_j rows (thread r = key j*128 + r)
+      ok = mbar_wait(&bars->dkv_full, unit_i & 1, tmo, abort_flag, p.err);
+      if (!ok) break;
+      tc_fence_after();
+      const int key = u.j * 128 + r;
+      const bool key_ok = key < p.N;
+      const size_t krow = (((size_t)u.b * p.N + (key_ok ? key : 0)) * p.Hkv + u.hkv) * D;
+      uint4* dkp = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.dk) + krow);
+      uint4* dvp = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.dv) + krow);
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ku[32], vu[32];
+        tmem_ld32(tmem + lane_off + T::T_DK + c * 32, ku);
+        tmem_ld32(tmem + lane_off + T::T_DV + c * 32, vu);
+        if (key_ok) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            dkp[c * 4 + e] = make_uint4(pack16<BF16>(to_f(ku[8 * e]), to_f(ku[8 * e + 1])),
+                                        pack16<BF16>(to_f(ku[8 * e + 2]), to_f(ku[8 * e + 3])),
+                                        pack16<BF16>(to_f(ku[8 * e + 4]), to_f(ku[8 * e + 5])),
+                                        pack16<BF16>(to_f(ku[8 * e + 6]), to_f(ku[8 * e + 7])));
+            dvp[c * 4 + e] = make_uint4(pack16<BF16>(to_f(vu[8 * e]), to_f(vu[8 * e + 1])),
+                                        pack16<BF16>(to_f(vu[8 * e + 2]), to_f(vu[8 * e + 3])),
+                                        pack16<BF16>(to_f(vu[8 * e + 4]), to_f(vu[8 * e + 5])),
+                                        pack16<BF16>(to_f(vu[8 * e + 6]), to_f(vu[8 * e + 7])));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->dkv_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+// D_i = sum_c dO_ic O_ic, one warp per (b, row, head); written [B][H][N].
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dvec_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                                                       float* __restrict__ dvec, int B, int N, int H, int bf16) {
+  const long long wid = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= (long long)B * N * H) return;
+  const int h = (int)(wid % H);
+  const int n = (int)((wid / H) % N);
+  const int b = (int)(wid / ((long long)H * N));
+  const size_t base = (size_t)wid * D;     // BSHD row (b, n, h)
+  float acc = 0.f;
+  for (int c = lane * 2; c < D; c += 64) {
+    const uint32_t ov = *reinterpret_cast<const uint32_t*>(o + base + c);
+    const uint32_t gv = *reinterpret_cast<const uint32_t*>(dout + base + c);
+    float o0, o1, g0, g1;
+    if (bf16) {
+      o0 = __uint_as_float(ov << 16); o1 = __uint_as_float(ov & 0xffff0000u);
+      g0 = __uint_as_float(gv << 16); g1 = __uint_as_float(gv & 0xffff0000u);
+    } else {
+      o0 = __half2float(__ushort_as_half((unsigned short)(ov & 0xffff)));
+      o1 = __half2float(__ushort_as_half((unsigned short)(ov >> 16)));
+      g0 = __half2float(__ushort_as_half((unsigned short)(gv & 0xffff)));
+      g1 = __half2float(__ushort_as_half((unsigned short)(gv >> 16)));
+    }
+    acc = fmaf(o0, g0, fmaf(o1, g1, acc));
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) dvec[((size_t)b * H + h) * N + n] = acc;
+}
+
+// dQ = fp32 accumulator rounded to bf16/fp16.
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq,
+                                                             long long n, int bf16) {
+  const long long i = ((long long)blockIdx.x * 256 + threadIdx.x) * 4;
+  if (i >= n) return;
+  const float4 a = *reinterpret_cast<const float4*>(acc + i);
+  uint32_t lo, hi;
+  if (bf16) {
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(a.y), "f"(a.x));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(a.w), "f"(a.z));
+  } else {
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(a.y), "f"(a.x));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(a.w), "f"(a.z));
+  }
+  *reinterpret_cast<uint2*>(dq + i) = make_uint2(lo, hi);
+}
+
+template <int D, bool CAUSAL, bool BF16>
+cudaError_t launch_bwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
+                         const BwdParams& p, int sm_count, cudaStream_t s) {
+  auto kern = attn_bwd_kernel<D, CAUSAL, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdTraits<D>::SMEM);
+  if (e != cudaSuccess) return e;
+  const int grid = p.nunits < sm_count ? p.nunits : sm_count;
+  kern<<<grid, 192, BwdTraits<D>::SMEM, s>>>(q, k, v, dout, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const CUtensorMap& dout, const BwdParams& p, bool causal, bool bf16, int sm_count,
+                       cudaStream_t s) {
+#define ATTN45_B(D, C, F) return launch_bwd_t<D, C, F>(q, k, v, dout, p, sm_count, s)
+  if (d == 64) {
+    if (causal) { if (bf16) ATTN45_B(64, true, true); else ATTN45_B(64, true, false); }
+    else        { if (bf16) ATTN45_B(64, false, true); else ATTN45_B(64, false, false); }
+  }
+  if (causal) { if (bf16) ATTN45_B(128, true, true); else ATTN45_B(128, true, false); }
+  if (bf16) ATTN45_B(128, false, true);
+  ATTN45_B(128, false, false);
+#undef ATTN45_B
+}
+
+cudaError_t launch_bwd_dvec(int d, const void* o, const void* dout, float* dvec, int B, int N, int H, bool bf16,
+                            cudaStream_t s) {
+  const long long rows = (long long)B * N * H;
+  const unsigned grid = (unsigned)((rows + 7) / 8);
+  if (d == 64)
+    bwd_dvec_kernel<64><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), dvec,
+                                             B, N, H, bf16);
+  else
+    bwd_dvec_kernel<128><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
+                                              dvec, B, N, H, bf16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_convert(const float* acc, void* dq, long long n, bool bf16, cudaStream_t s) {
+  const unsigned grid = (unsigned)((n / 4 + 255) / 256);
+  bwd_dq_convert_kernel<<<grid, 256, 0, s>>>(acc, static_cast<uint16_t*>(dq), n, bf16);
+  return cudaGetLastError();
+}
+
+}  // namespace attn45

@@ -198,6 +198,28 @@ ATTN45_API size_t attn_decode_workspace_size(int B, int H, int d, int num_splits
 ATTN45_API int attn_combine(const float* o_parts, const float* lse_parts, void* o, float* lse, int num_splits,
                             int rows, int d, int dtype, void* stream);
 
+/*
+ * attn_bwd -- gradients of sum(dO * O) for the BF16/FP16 forward (head dim 64
+ * or 128, fixed length, causal or not, H % Hkv == 0). The backward pass of the
+ * FlashAttention papers: P is recomputed from S and the forward's lse;
+ * dV = P^T dO, dS = scale P (dO V^T - rowsum(dO * O)), dK = dS^T Q, dQ = dS K;
+ * dK, dV of a KV head sum over its query heads.
+ *   q, o, dout [B, N, H, d]; k, v [B, N, Hkv, d] (BSHD, the forward's inputs
+ *   and output); lse [B, H, N] fp32 as the forward wrote it; dq [B, N, H, d],
+ *   dk, dv [B, N, Hkv, d] outputs in the input dtype.
+ *   workspace: DEVICE, 256-byte aligned, >= attn_bwd_workspace_size(B, H, N,
+ *   d) bytes (an fp32 dQ accumulator and the row sums), owned by the caller.
+ *   Launches: a row-sum kernel, the main kernel (one CTA per (batch, KV head,
+ *   128-key block) unit: five tcgen05 GEMMs per query block, dK/dV kept in
+ *   TMEM, dQ added into the fp32 accumulator), a dQ conversion kernel.
+ */
+ATTN45_API int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                        int B, int H, int Hkv, int N, int d, int causal, float scale, int dtype, void* stream);
+/* Bytes of attn_bwd's workspace: fp32 [B,N,H,d] then fp32 [B,H,N], each
+ * padded to 256 bytes; 0 for bad sizes. */
+ATTN45_API size_t attn_bwd_workspace_size(int B, int H, int N, int d);
+
 /* Synchronises `stream`, reads and clears the current device's error word.
  * ATTN_OK, ATTN_ERR_TIMEOUT (a bounded device wait gave up) or ATTN_ERR_CUDA. */
 ATTN45_API int attn_get_device_error(void* stream);
