@@ -289,6 +289,8 @@ def run_ours(args):
         line["fp8"] = fp8_measure(min(args.steps, 50), args.warmup)
     if rank == 0 and not args.no_decode:
         line["decode"] = decode_measure(min(args.steps, 50), args.warmup)
+    if rank == 0 and not args.no_bwd:
+        line["bwd"] = bwd_measure(min(args.steps, 50), args.warmup)
     if rank == 0 and not args.no_cpu_baseline:
         rate, threads, sample = cpu_oracle_rate(w, budget_s=args.cpu_budget)
         line["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -297,6 +299,51 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1 and dist.is_initialized():
         dist.destroy_process_group()
+
+
+def bwd_measure(steps: int, warmup: int, seed: int = 0):
+    """Backward (dQ, dK, dV) on the forward's shape (B=4, N=4096, H=16, d=128,
+    non-causal, bf16): row sums, the main kernel and the dQ conversion, timed
+    with CUDA events, L2 flushed before each call. Work = 2.5 x the forward's
+    (five N x N x d GEMMs instead of two): 10 B H N^2 d flops."""
+    import torch
+
+    import attn_inputs as gen
+    import exact_attention_45_gb300 as A
+    w = dict(WORKLOAD)
+    B, N, H, d = w["B"], w["N"], w["H"], w["d"]
+    q, k, v = (t.cuda() for t in gen.qkv_fixed(B, N, H, H, d, seed=seed))
+    do = gen.qkv_fixed(B, N, H, H, d, seed=seed + 100)[0].cuda()
+    o, lse = A.attn_fwd(q, k, v)
+    ws = torch.empty(A.attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    call = lambda: A.attn_bwd(q, k, v, o, lse, do, workspace=ws, dq=dq, dk=dk, dv=dv)
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    ev = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    if A.attn_get_device_error() != 0:
+        raise RuntimeError("device error in the backward")
+    t = sum(a.elapsed_time(b) for a, b in ev) / steps / 1e3
+    fl = 2.5 * flops_of(w)
+    pk = peaks()
+    return {
+        "config": {"workload": "attn_bwd bf16 non-causal d128", "B": B, "N": N, "H": H, "d": d},
+        "ms": round(t * 1e3, 4), "tflops": round(fl / t / 1e12, 2),
+        "roofline": {"bound": "tensor", "achieved": round(fl / t / 1e12, 2), "peak": pk["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(fl / t / 1e12 / pk["bf16_tflops"], 4),
+                     "flops": fl, "peak_source": f"{pk['source']} bf16 burst (cuBLAS)"},
+        "gpu_launches_per_step": 4,
+    }
 
 
 DECODE = {"workload": "split-KV decode bf16 d128", "B": 8, "H": 32, "Hkv": 8, "d": 128, "Nmax": 32768,
@@ -503,8 +550,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 sub-measurement")
     ap.add_argument("--no-decode", action="store_true", help="skip the split-KV decode sub-measurement")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward sub-measurement")
     ap.add_argument("--decode-splits", type=int, default=0, help="decode key-range splits (0 = automatic)")
-    ap.add_argument("--workload", choices=("bf16", "fp8", "decode"), default="bf16",
+    ap.add_argument("--workload", choices=("bf16", "fp8", "decode", "bwd"), default="bf16",
                     help="fp8 / decode: run only that path (e.g. for profiling)")
     ap.add_argument("--sweep", action="store_true", help="time every BF16 configuration instead")
     ap.add_argument("--sweep-reps", type=int, default=20)
@@ -514,6 +562,10 @@ def main(argv=None):
         import torch
         torch.cuda.set_device(0)
         print(json.dumps({"fp8": fp8_measure(args.steps, args.warmup)}), flush=True)
+    elif args.workload == "bwd":
+        import torch
+        torch.cuda.set_device(0)
+        print(json.dumps({"bwd": bwd_measure(args.steps, args.warmup)}), flush=True)
     elif args.workload == "decode":
         import torch
         torch.cuda.set_device(0)

@@ -56,14 +56,16 @@ struct BwdUnit {
   int b, hkv, j, i0, nI, nblk;
 };
 
+// Units of one (batch, KV head) are adjacent, so the CTAs working on them at
+// the same time share that head's Q, dO and dQ rows in L2; inside a head the
+// key blocks run in order (causal: the longest, j = 0, first).
 __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int t, bool causal) {
   BwdUnit u;
-  const int bk = p.B * p.Hkv;
-  u.j = t / bk;                       // key block; the longest (causal: j = 0) first
-  const int r = t % bk;
+  const int nqb = ceil_div(p.N, 128);
+  u.j = t % nqb;
+  const int r = t / nqb;
   u.b = r / p.Hkv;
   u.hkv = r % p.Hkv;
-  const int nqb = ceil_div(p.N, 128);
   u.i0 = causal ? u.j : 0;
   u.nI = nqb - u.i0;
   u.nblk = u.nI * p.group;
