@@ -409,6 +409,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   const size_t rows = (size_t)B * N * H;
   float* dq_acc = static_cast<float*>(workspace);
   float* dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * d * 4 + 255) & ~size_t(255)));
+  CUtensorMap mdq;
+  if ((rc = make_map(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, d, H, N, B, 32, 128))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool bf16 = dtype == ATTN_BF16;
   cudaError_t e = cudaMemsetAsync(dq_acc, 0, rows * d * 4, st);
@@ -432,7 +434,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
   p.err = dev->err;
-  e = launch_bwd(d, mq, mk, mv, mdo, p, causal != 0, bf16, dev->sm_count, st);
+  e = launch_bwd(d, mq, mk, mv, mdo, mdq, p, causal != 0, bf16, dev->sm_count, st);
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
   e = launch_bwd_dq_convert(dq_acc, dq, (long long)rows * d, bf16, st);
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dQ conversion launch");

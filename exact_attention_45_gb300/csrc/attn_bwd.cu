@@ -10,8 +10,9 @@
 //     dV_j += P^T dO_i               dK_j += dS^T Q_i               dQ_i += dS K_j
 // One CTA owns a (batch, KV head, key block) unit: dV_j and dK_j stay in TMEM
 // across all its query blocks and are written once; dQ_i is produced per
-// block in TMEM and added into an fp32 accumulator in HBM with vector
-// reductions (other key blocks add to the same rows), converted at the end.
+// block in TMEM, staged in shared memory (over the P/dS tiles, which its
+// GEMM has finished reading) and added into an fp32 accumulator in HBM by bulk
+// tensor reductions (other key blocks add to the same rows); converted at the end.
 //
 // Roles (192 threads): warps 0-3 compute (thread r owns TMEM lane r: query
 // row r for S/dP/dQ, key r for dV/dK), warp 4 lane 0 loads by TMA, warp 5
@@ -53,7 +54,7 @@ __host__ __device__ constexpr uint32_t idesc_f16_ab(int M, int N, bool bf16, boo
 }
 
 struct BwdUnit {
-  int b, hkv, j, i0, nI, nblk;
+  int b, hkv, j, i0, nI, nblk, rot;
 };
 
 // Units of one (batch, KV head) are adjacent, so the CTAs working on them at
@@ -69,8 +70,14 @@ __device__ __forceinline__ BwdUnit bwd_unit(const BwdParams& p, int t, bool caus
   u.i0 = causal ? u.j : 0;
   u.nI = nqb - u.i0;
   u.nblk = u.nI * p.group;
+  // units of one head start at different query blocks, so CTAs running at
+  // the same time reduce into different dQ rows
+  u.rot = u.j % u.nI;
   return u;
 }
+
+// Query block of step `it` of a unit (heads of the group outermost).
+__device__ __forceinline__ int bwd_qblock(const BwdUnit& u, int it) { return u.i0 + (it % u.nI + u.rot) % u.nI; }
 
 __device__ __forceinline__ float to_f(uint32_t u) { return __uint_as_float(u); }
 
@@ -82,16 +89,11 @@ __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
   return r;
 }
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(192, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                const BwdParams p) {
+                const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using T = BwdTraits<D>;
   constexpr int NC = D / 64;                         // 128-byte chunks per row of a d-wide tile
   constexpr int KS = D / 16;                         // K steps over d
@@ -125,6 +127,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmDQ);
   }
   tc_fence_before();
   __syncthreads();
@@ -149,7 +152,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         for (int it = 0; it < u.nblk; ++it, ++blk_it) {
           const int h = u.hkv * p.group + it / u.nI;
-          const int i = u.i0 + it % u.nI;
+          const int i = bwd_qblock(u, it);
           ok = mbar_wait(&bars->qdo_empty, (blk_it & 1) ^ 1, tmo, abort_flag, p.err);
           if (!ok) break;
           mbar_expect_tx(&bars->qdo_full, 2 * T::TILE);
@@ -243,17 +246,31 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t prow = smem_u32(tp) + r * 128;
     const uint32_t dsrow = smem_u32(tds) + r * 128;
     int unit_i = 0, blk_it = 0;
+    float lse_next = 0.f, d_next = 0.f;
     bool ok = true;
     for (int t = blockIdx.x; t < nunits && ok; t += gridDim.x, ++unit_i) {
       const BwdUnit u = bwd_unit(p, t, CAUSAL);
       for (int it = 0; it < u.nblk && ok; ++it, ++blk_it) {
         const int h = u.hkv * p.group + it / u.nI;
-        const int i = u.i0 + it % u.nI;
+        const int i = bwd_qblock(u, it);
         const int qrow = i * 128 + r;
         const bool row_ok = qrow < p.N;
         const size_t lrow = ((size_t)u.b * p.H + h) * p.N + (row_ok ? qrow : 0);
-        const float lse2 = row_ok ? __ldg(p.lse + lrow) * 1.4426950408889634f : 0.f;
-        const float Drow = row_ok ? __ldg(p.dvec + lrow) : 0.f;
+        // this row's lse and D were fetched during the previous block (not for
+        // a unit's first block)
+        if (it == 0) {
+          lse_next = row_ok ? __ldg(p.lse + lrow) : 0.f;
+          d_next = row_ok ? __ldg(p.dvec + lrow) : 0.f;
+        }
+        const float lse2 = lse_next * 1.4426950408889634f;
+        const float Drow = d_next;
+        if (it + 1 < u.nblk) {
+          const int h1 = u.hkv * p.group + (it + 1) / u.nI;
+          const int q1 = bwd_qblock(u, it + 1) * 128 + r;
+          const size_t l1 = ((size_t)u.b * p.H + h1) * p.N + (q1 < p.N ? q1 : 0);
+          lse_next = __ldg(p.lse + l1);
+          d_next = __ldg(p.dvec + l1);
+        }
         ok = mbar_wait(&bars->s_full, blk_it & 1, tmo, abort_flag, p.err);
         if (!ok) break;
         tc_fence_after();
@@ -261,15 +278,19 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         int kmax = p.N - u.j * 128;                            // keys past the end are masked
         if (CAUSAL) kmax = min(kmax, qrow - u.j * 128 + 1);
         if (!row_ok) kmax = 0;
+        // the previous block's dQ reduction reads the P/dS tiles as its staging
+        if (blk_it > 0) {
+          if (r == 0) tma_store_wait_read();
+          named_bar_sync(1, 128);
+        }
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {                          // 32 keys at a time
-          uint32_t su[32], du[32];
-          tmem_ld32(tmem + lane_off + T::T_S + c * 32, su);
-          tmem_ld32(tmem + lane_off + T::T_DP + c * 32, du);
-          uint32_t pw[16], dw[16];
+        for (int c = 0; c < 2; ++c) {                          // 64 keys at a time
+          uint32_t su[64], du[64];
+          tmem_ld64_pair(tmem + lane_off + T::T_S + c * 64, su, tmem + lane_off + T::T_DP + c * 64, du);
+          uint32_t pw[32], dw[32];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int key = c * 32 + e;
+          for (int e = 0; e < 64; e += 2) {
+            const int key = c * 64 + e;
             const float p0 = key < kmax ? ex2_approx(to_f(su[e]) * sl2 - lse2) : 0.f;
             const float p1 = key + 1 < kmax ? ex2_approx(to_f(su[e + 1]) * sl2 - lse2) : 0.f;
             const float d0 = scale * p0 * (to_f(du[e]) - Drow);
@@ -277,13 +298,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             pw[e / 2] = pack16<BF16>(p0, p1);
             dw[e / 2] = pack16<BF16>(d0, d1);
           }
-          // keys c*32 .. c*32+31 are 16-byte units 4c .. 4c+3 of the row (chunk c / 2)
+          // keys c*64 .. c*64+63 fill chunk c of the row: 16-byte unit q at q ^ (r % 8)
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int unit = (c & 1) * 4 + q4;
-            const uint32_t off = (c >> 1) * T::CHUNK + ((unit ^ (r & 7)) << 4);
-            st_shared_v4(prow + off, pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
-            st_shared_v4(dsrow + off, dw[4 * q4], dw[4 * q4 + 1], dw[4 * q4 + 2], dw[4 * q4 + 3]);
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t off = c * T::CHUNK + ((q ^ (r & 7)) << 4);
+            st_shared_v4(prow + off, pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+            st_shared_v4(dsrow + off, dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
           }
         }
         fence_proxy_async_smem();                             // P, dS visible to the MMAs
@@ -293,16 +313,26 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         ok = mbar_wait(&bars->dq_full, blk_it & 1, tmo, abort_flag, p.err);
         if (!ok) break;
         tc_fence_after();
-        float* dqrow = p.dq_acc + (((size_t)u.b * p.N + (row_ok ? qrow : 0)) * p.H + h) * D;
+        // dQ rows -> staging: chunk cc (32 fp32 columns, 16 KB) row r, 16-byte
+        // unit v at v ^ (r % 8), the bulk reduction's 128-byte swizzle
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t qu[32];
-          tmem_ld32(tmem + lane_off + T::T_S + c * 32, qu);
-          if (row_ok) {
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t qu[64];
+          tmem_ld64(tmem + lane_off + T::T_S + c * 64, qu);
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              red_add_v4(dqrow + c * 32 + e, to_f(qu[e]), to_f(qu[e + 1]), to_f(qu[e + 2]), to_f(qu[e + 3]));
+          for (int v4 = 0; v4 < 16; ++v4) {
+            const int cc = c * 2 + (v4 >> 3);
+            const uint32_t off = cc * T::CHUNK + ((((v4 & 7) ^ (r & 7))) << 4);
+            st_shared_v4(prow + off, qu[4 * v4], qu[4 * v4 + 1], qu[4 * v4 + 2], qu[4 * v4 + 3]);
           }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (r == 0) {
+          // rows past the sequence end fall outside the map and are dropped
+          for (int cc = 0; cc < D / 32; ++cc)
+            tma_reduce_add_4d(&tmDQ, tp + cc * T::CHUNK, cc * 32, h, i * 128, u.b);
+          tma_store_commit();
         }
         tc_fence_before();
         mbar_arrive(&bars->dq_empty);
@@ -339,6 +369,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_before();
       mbar_arrive(&bars->dkv_empty);
     }
+    if (r == 0) tma_store_wait_all();                         // no reduction outlives the CTA
   }
 
   tc_fence_before();
@@ -398,21 +429,21 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
 
 template <int D, bool CAUSAL, bool BF16>
 cudaError_t launch_bwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
-                         const BwdParams& p, int sm_count, cudaStream_t s) {
+                         const CUtensorMap& dq, const BwdParams& p, int sm_count, cudaStream_t s) {
   auto kern = attn_bwd_kernel<D, CAUSAL, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdTraits<D>::SMEM);
   if (e != cudaSuccess) return e;
   const int grid = p.nunits < sm_count ? p.nunits : sm_count;
-  kern<<<grid, 192, BwdTraits<D>::SMEM, s>>>(q, k, v, dout, p);
+  kern<<<grid, 192, BwdTraits<D>::SMEM, s>>>(q, k, v, dout, dq, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                       const CUtensorMap& dout, const BwdParams& p, bool causal, bool bf16, int sm_count,
-                       cudaStream_t s) {
-#define ATTN45_B(D, C, F) return launch_bwd_t<D, C, F>(q, k, v, dout, p, sm_count, s)
+                       const CUtensorMap& dout, const CUtensorMap& dq, const BwdParams& p, bool causal, bool bf16,
+                       int sm_count, cudaStream_t s) {
+#define ATTN45_B(D, C, F) return launch_bwd_t<D, C, F>(q, k, v, dout, dq, p, sm_count, s)
   if (d == 64) {
     if (causal) { if (bf16) ATTN45_B(64, true, true); else ATTN45_B(64, true, false); }
     else        { if (bf16) ATTN45_B(64, false, true); else ATTN45_B(64, false, false); }

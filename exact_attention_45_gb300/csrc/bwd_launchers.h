@@ -19,10 +19,12 @@ struct BwdParams {
   unsigned int* err;       // device error word
 };
 
-// q, k, v, dout: maps {d, heads, N, B} with 64-element x 128-row boxes.
+// q, k, v, dout: maps {d, heads, N, B} with 64-element x 128-row boxes; dq:
+// fp32 accumulator map {d, H, N, B} with 32-element x 128-row boxes (bulk
+// reductions), all with 128-byte swizzle.
 cudaError_t launch_bwd(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                       const CUtensorMap& dout, const BwdParams& p, bool causal, bool bf16, int sm_count,
-                       cudaStream_t s);
+                       const CUtensorMap& dout, const CUtensorMap& dq, const BwdParams& p, bool causal, bool bf16,
+                       int sm_count, cudaStream_t s);
 cudaError_t launch_bwd_dvec(int d, const void* o, const void* dout, float* dvec, int B, int N, int H, bool bf16,
                             cudaStream_t s);
 cudaError_t launch_bwd_dq_convert(const float* acc, void* dq, long long n, bool bf16, cudaStream_t s);
