@@ -14,9 +14,10 @@
 // GEMM has finished reading) and added into an fp32 accumulator in HBM by bulk
 // tensor reductions (other key blocks add to the same rows); converted at the end.
 //
-// Roles (192 threads): warps 0-3 compute (thread r owns TMEM lane r: query
-// row r for S/dP/dQ, key r for dV/dK), warp 4 lane 0 loads by TMA, warp 5
-// lane 0 issues the MMAs. TMEM: S (128 cols, reused for dQ), dP (128), dV (d),
+// Roles (320 threads): warps 0-7 compute (thread r of a warpgroup owns TMEM
+// lane r: query row r for S/dP/dQ, key r for dV/dK; warpgroup 0 takes the
+// first half of the columns, warpgroup 1 the second), warp 8 lane 0 loads by
+// TMA, warp 9 lane 0 issues the MMAs. TMEM: S (128 cols, reused for dQ), dP (128), dV (d),
 // dK (d). Shared memory: K_j, V_j, Q_i, dO_i tiles and the bf16 P and dS tiles
 // that feed the last three products (MN-major for P^T / dS^T, K-major for dS).
 #include <cuda_bf16.h>
@@ -89,8 +90,11 @@ __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
   return r;
 }
 
+constexpr int BWD_THREADS = 320;
+constexpr int BWD_COMPUTE = 256;
+
 template <int D, bool CAUSAL, bool BF16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(BWD_THREADS, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                 const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
@@ -109,20 +113,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(&bars->qdo_full, 1);
     mbar_init(&bars->qdo_empty, 1);
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->p_full, BWD_COMPUTE);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_empty, 128);
+    mbar_init(&bars->dq_empty, BWD_COMPUTE);
     mbar_init(&bars->dkv_full, 1);
-    mbar_init(&bars->dkv_empty, 128);
+    mbar_init(&bars->dkv_empty, BWD_COMPUTE);
     mbar_init(&bars->done, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -136,7 +140,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint64_t tmo = p.timeout_ns;
   const int nunits = p.nunits;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int unit_i = 0, blk_it = 0;
@@ -167,7 +171,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       if (unit_i > 0) mbar_wait_drain(&bars->kv_full, (unit_i - 1) & 1, tmo, p.err);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_kk = idesc_f16_ab(128, 128, BF16, false, false);   // S, dP
@@ -236,7 +240,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncwarp();
   } else {
     // ------------------------------------------------------------ compute warps
-    const int r = threadIdx.x;                               // TMEM lane
+    const int r = threadIdx.x & 127;                         // TMEM lane
+    const int half = threadIdx.x >> 7;                       // column half this warpgroup owns
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
     const float scale = p.scale;
@@ -278,13 +283,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         int kmax = p.N - u.j * 128;                            // keys past the end are masked
         if (CAUSAL) kmax = min(kmax, qrow - u.j * 128 + 1);
         if (!row_ok) kmax = 0;
-        // the previous block's dQ reduction reads the P/dS tiles as its staging
-        if (blk_it > 0) {
-          if (r == 0) tma_store_wait_read();
-          named_bar_sync(1, 128);
-        }
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {                          // 64 keys at a time
+        {
+          const int c = half;                                  // keys c*64 .. c*64+63
           uint32_t su[64], du[64];
           tmem_ld64_pair(tmem + lane_off + T::T_S + c * 64, su, tmem + lane_off + T::T_DP + c * 64, du);
           uint32_t pw[32], dw[32];
@@ -297,6 +297,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const float d1 = scale * p1 * (to_f(du[e + 1]) - Drow);
             pw[e / 2] = pack16<BF16>(p0, p1);
             dw[e / 2] = pack16<BF16>(d0, d1);
+          }
+          // the previous block's dQ reduction reads the P/dS tiles as its
+          // staging: wait for it only now, after the loads and the arithmetic
+          if (blk_it > 0) {
+            if (threadIdx.x == 0) tma_store_wait_read();
+            named_bar_sync(1, BWD_COMPUTE);
           }
           // keys c*64 .. c*64+63 fill chunk c of the row: 16-byte unit q at q ^ (r % 8)
 #pragma unroll
@@ -313,22 +319,24 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         ok = mbar_wait(&bars->dq_full, blk_it & 1, tmo, abort_flag, p.err);
         if (!ok) break;
         tc_fence_after();
-        // dQ rows -> staging: chunk cc (32 fp32 columns, 16 KB) row r, 16-byte
-        // unit v at v ^ (r % 8), the bulk reduction's 128-byte swizzle
-#pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t qu[64];
-          tmem_ld64(tmem + lane_off + T::T_S + c * 64, qu);
+        // dQ rows (this warpgroup's D/2 columns) -> staging: chunk cc (32 fp32
+        // columns, 16 KB) row r, 16-byte unit v at v ^ (r % 8), the bulk
+        // reduction's 128-byte swizzle
+        {
+          constexpr int HC = D / 2;                            // columns per warpgroup
+          uint32_t qu[HC];
+          if constexpr (HC == 64) tmem_ld64(tmem + lane_off + T::T_S + half * HC, qu);
+          else tmem_ld32(tmem + lane_off + T::T_S + half * HC, qu);
 #pragma unroll
-          for (int v4 = 0; v4 < 16; ++v4) {
-            const int cc = c * 2 + (v4 >> 3);
+          for (int v4 = 0; v4 < HC / 4; ++v4) {
+            const int cc = half * (HC / 32) + (v4 >> 3);
             const uint32_t off = cc * T::CHUNK + ((((v4 & 7) ^ (r & 7))) << 4);
             st_shared_v4(prow + off, qu[4 * v4], qu[4 * v4 + 1], qu[4 * v4 + 2], qu[4 * v4 + 3]);
           }
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (r == 0) {
+        named_bar_sync(1, BWD_COMPUTE);
+        if (threadIdx.x == 0) {
           // rows past the sequence end fall outside the map and are dropped
           for (int cc = 0; cc < D / 32; ++cc)
             tma_reduce_add_4d(&tmDQ, tp + cc * T::CHUNK, cc * 32, h, i * 128, u.b);
@@ -348,7 +356,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       uint4* dkp = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.dk) + krow);
       uint4* dvp = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.dv) + krow);
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
         uint32_t ku[32], vu[32];
         tmem_ld32(tmem + lane_off + T::T_DK + c * 32, ku);
         tmem_ld32(tmem + lane_off + T::T_DV + c * 32, vu);
@@ -369,13 +377,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_before();
       mbar_arrive(&bars->dkv_empty);
     }
-    if (r == 0) tma_store_wait_all();                         // no reduction outlives the CTA
+    if (threadIdx.x == 0) tma_store_wait_all();               // no reduction outlives the CTA
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
 // D_i = sum_c dO_ic O_ic, one warp per (b, row, head); written [B][H][N].
@@ -434,7 +442,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUten
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdTraits<D>::SMEM);
   if (e != cudaSuccess) return e;
   const int grid = p.nunits < sm_count ? p.nunits : sm_count;
-  kern<<<grid, 192, BwdTraits<D>::SMEM, s>>>(q, k, v, dout, dq, p);
+  kern<<<grid, BWD_THREADS, BwdTraits<D>::SMEM, s>>>(q, k, v, dout, dq, p);
   return cudaGetLastError();
 }
 
