@@ -40,21 +40,37 @@ def flops_of(w) -> float:
     return f / 2 if w["causal"] else f
 
 
-def profiled_traffic(profile: str):
+FWD_BF16_KERNEL_SOURCES = ("attn_fwd2_kernel.cuh", "attn_common.cuh", "ptx.cuh", "fwd_launch.cuh", "attn_fwd_d128.cu",
+                           "launchers.h")
+
+
+def kernel_digest(files) -> str:
+    """sha256 over the named csrc files and the nvcc flags they are built with."""
+    import hashlib
+
+    from exact_attention_45_gb300 import build as _b
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(_b.CSRC, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    h.update(" ".join(_b.ARCH + _b.NVCC_FLAGS).encode())
+    return h.hexdigest()
+
+
+def profiled_traffic(profile: str, files):
     """DRAM bytes per launch recorded by an ncu capture summarised under
-    profiles/, if that capture ran the library sources built now (same
-    source digest); None once the kernel has changed since."""
+    profiles/, if that capture ran the kernel sources built now (same digest
+    of `files`); None once the kernel has changed since."""
     path = os.path.join(ROOT, "profiles", profile)
     if not os.path.exists(path):
         return None
     rec = {}
     with open(path) as fh:
         for line in fh:
-            if ":" in line and line.split(":")[0].strip() in ("library_source_digest", "traffic_bytes_per_launch"):
+            if ":" in line and line.split(":")[0].strip() in ("kernel_source_digest", "traffic_bytes_per_launch"):
                 key, val = line.split(":", 1)
                 rec[key.strip()] = val.strip()
-    from exact_attention_45_gb300 import build as _b
-    if rec.get("library_source_digest") != _b._digest() or "traffic_bytes_per_launch" not in rec:
+    if rec.get("kernel_source_digest") != kernel_digest(files) or "traffic_bytes_per_launch" not in rec:
         return None
     return int(rec["traffic_bytes_per_launch"])
 
@@ -115,7 +131,15 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            # nvidia-smi takes a while to start: wait for its first samples so
+            # that the timed region is covered
+            t0 = time.time()
+            while time.time() - t0 < 10.0:
+                self.fh.flush()
+                with open(self.out) as fh:
+                    if sum(1 for _ in fh) >= 2:
+                        break
+                time.sleep(0.05)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -256,13 +280,14 @@ def run_ours(args):
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    e2e_steps = min(args.steps, 200)          # each moves ~270 MB over PCIe/C2C
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(e2e_steps):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_s = e0.elapsed_time(e1) / 1e3
-    e2e_max, e2e_flops = aggregate(e2e_s, local_flops)
+    e2e_max, e2e_flops = aggregate(e2e_s, flops_of(w) * e2e_steps)
     if A.attn_get_device_error() != 0:
         raise RuntimeError("device error during timing")
 
@@ -277,7 +302,7 @@ def run_ours(args):
                    "l2": "flushed between timed iterations (512 MiB write)"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
-                     "traffic": profiled_traffic("attn_fwd2_bf16_d128_n4096_noncausal.md"),
+                     "traffic": profiled_traffic("attn_fwd2_bf16_d128_n4096_noncausal.md", FWD_BF16_KERNEL_SOURCES),
                      "peak_source": f"{pk['source']} bf16 burst (cuBLAS)", "kernel": "attn_fwd2_kernel<128,128,2,false,false,BF16>"},
         "e2e": {"value": round(e2e_flops / e2e_max / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2,
@@ -286,9 +311,9 @@ def run_ours(args):
         "clocks": clocks,
     }
     if rank == 0 and not args.no_fp8:
-        line["fp8"] = fp8_measure(min(args.steps, 50), args.warmup)
+        line["fp8"] = fp8_measure(min(args.steps, 100), args.warmup)
     if rank == 0 and not args.no_decode:
-        line["decode"] = decode_measure(min(args.steps, 50), args.warmup)
+        line["decode"] = decode_measure(min(args.steps, 100), args.warmup)
     if rank == 0 and not args.no_bwd:
         line["bwd"] = bwd_measure(min(args.steps, 50), args.warmup)
     if rank == 0 and not args.no_cpu_baseline:
@@ -543,7 +568,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
