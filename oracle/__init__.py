@@ -45,6 +45,7 @@ __all__ = [
     "splitmix64", "hadamard_signs", "sylvester", "fwht_f32", "rotate_f32",
     "E4M3_MAX", "e4m3_decode", "e4m3_encode", "e4m3_table",
     "fp8_quant_block_rows", "fp8_prepass", "fp8_attention_emulated",
+    "fp8_varlen_block_offsets", "fp8_prepass_varlen", "fp8_attention_emulated_varlen",
     "P_FP8_MULT", "P_FP8_LAZY_LOG2", "Q_BLOCK", "K_BLOCK",
 ]
 
@@ -565,4 +566,104 @@ def fp8_attention_emulated(pre: dict, causal: bool = False, scale: float | None 
             m = m_new
         o[r] = acc * svec / (P_FP8_MULT * l)
         lse[r] = (m + math.log2(l)) * math.log(2.0)
+    return o, lse
+
+
+# ------------------------------------------------------------------ FP8, packed variable-length sequences
+def fp8_varlen_block_offsets(cu_seqlens) -> np.ndarray:
+    """blk_off[s] = sum over earlier sequences of ceil(n/128): the first
+    128-row quantisation block (and 128-key V column block) of sequence s."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    n = cu[1:] - cu[:-1]
+    return np.concatenate([[0], np.cumsum((n + Q_BLOCK - 1) // Q_BLOCK)]).astype(np.int32)
+
+
+def fp8_prepass_varlen(q, k, v, cu_seqlens, mode: str = "block", rotate: bool = True, seed: int = 0):
+    """The FP8 pre-pass of packed sequences (THD: q [T,H,d], k, v [T,Hkv,d]).
+
+    Reading: every sequence is quantised as its own batch element of
+    ``fp8_prepass`` (blocks of 128 rows never cross a sequence boundary, V's
+    channel scales are per (sequence, KV head)); in "tensor" mode the three
+    scales cover the whole packed tensors. Layout (tmax = ceil(T/128) + nseq
+    bounds the number of blocks): q8 [T,H,d], k8 [T,Hkv,d]; vt8 [Hkv, d,
+    128*tmax] with sequence s's keys from column 128*blk_off[s] (pad keys of
+    its last block hold code 0); block mode sq [H, tmax], sk [Hkv, tmax] with
+    sequence s's block b at column blk_off[s] + b (other columns 0 here, not
+    written by the GPU), sv [nseq, Hkv, d]; tensor mode one value each.
+    """
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    nseq = cu.size - 1
+    qf, kf, vf = _f32(q), _f32(k), _f32(v)
+    T, H, d = qf.shape
+    Hkv = kf.shape[1]
+    boff = fp8_varlen_block_offsets(cu)
+    tmax = -(-T // Q_BLOCK) + nseq
+    q8 = np.zeros((T, H, d), np.uint8)
+    k8 = np.zeros((T, Hkv, d), np.uint8)
+    vt8 = np.zeros((Hkv, d, Q_BLOCK * tmax), np.uint8)
+    if mode == "tensor":
+        whole = fp8_prepass(qf[None], kf[None], vf[None], mode="tensor", rotate=rotate, seed=seed)
+        q8[:] = whole["q8"][0]
+        k8[:] = whole["k8"][0]
+        for s in range(nseq):
+            a, b = int(cu[s]), int(cu[s + 1])
+            vt8[:, :, Q_BLOCK * boff[s]:Q_BLOCK * boff[s] + (b - a)] = whole["vt8"][0, :, :, a:b]
+        sq, sk, sv = whole["sq"], whole["sk"], whole["sv"]
+    elif mode == "block":
+        sq = np.zeros((H, tmax), np.float32)
+        sk = np.zeros((Hkv, tmax), np.float32)
+        sv = np.zeros((nseq, Hkv, d), np.float32)
+        for s in range(nseq):
+            a, b = int(cu[s]), int(cu[s + 1])
+            if b == a:
+                continue
+            ps = fp8_prepass(qf[None, a:b], kf[None, a:b], vf[None, a:b], mode="block", rotate=rotate, seed=seed)
+            q8[a:b], k8[a:b] = ps["q8"][0], ps["k8"][0]
+            vt8[:, :, Q_BLOCK * boff[s]:Q_BLOCK * boff[s] + (b - a)] = ps["vt8"][0]
+            nb = ps["sq"].shape[2]
+            sq[:, boff[s]:boff[s] + nb] = ps["sq"][0]
+            sk[:, boff[s]:boff[s] + nb] = ps["sk"][0]
+            sv[s] = ps["sv"][0]
+    else:
+        raise ValueError(mode)
+    return {"q8": q8, "k8": k8, "vt8": vt8, "sq": sq, "sk": sk, "sv": sv, "blk_off": boff, "tmax": tmax,
+            "mode": mode, "rotate": rotate, "seed": seed}
+
+
+def fp8_attention_emulated_varlen(pre: dict, cu_seqlens, causal: bool = False, scale: float | None = None,
+                                  rows=None):
+    """``fp8_attention_emulated`` of every sequence of a packed pre-pass result
+    (each sequence is its own problem; causal masking is per sequence).
+    ``rows`` = (sequence, head, local row) arrays; default every row. Returns
+    o [R, d] and lse [R] in that row order."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    nseq = cu.size - 1
+    boff = pre["blk_off"]
+    H, d = pre["q8"].shape[1], pre["q8"].shape[2]
+    if rows is None:
+        rs, rh, ri = [], [], []
+        for s in range(nseq):
+            n = int(cu[s + 1] - cu[s])
+            for h in range(H):
+                rs += [s] * n
+                rh += [h] * n
+                ri += list(range(n))
+        rows = (np.array(rs, np.int64), np.array(rh, np.int64), np.array(ri, np.int64))
+    rs, rh, ri = (np.asarray(x, np.int64) for x in rows)
+    o = np.zeros((rs.size, d))
+    lse = np.zeros(rs.size)
+    for s in np.unique(rs):
+        a, b = int(cu[s]), int(cu[s + 1])
+        n = b - a
+        nb = -(-n // Q_BLOCK)
+        sel = np.nonzero(rs == s)[0]
+        blk = pre["mode"] == "block"
+        ps = {"q8": pre["q8"][None, a:b], "k8": pre["k8"][None, a:b],
+              "vt8": pre["vt8"][None, :, :, Q_BLOCK * boff[s]:Q_BLOCK * boff[s] + n],
+              "sq": pre["sq"][None, :, boff[s]:boff[s] + nb] if blk else pre["sq"],
+              "sk": pre["sk"][None, :, boff[s]:boff[s] + nb] if blk else pre["sk"],
+              "sv": pre["sv"][s:s + 1] if blk else pre["sv"], "mode": pre["mode"]}
+        os_, ls_ = fp8_attention_emulated(ps, causal=causal, scale=scale,
+                                          rows=(np.zeros(sel.size, np.int64), rh[sel], ri[sel]))
+        o[sel], lse[sel] = os_, ls_
     return o, lse

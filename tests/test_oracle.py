@@ -538,3 +538,59 @@ def test_backward_invariants():
         _, dkh, dvh = O.attention_backward(qg[:, :, h:h + 1], kg, vg, dog[:, :, h:h + 1])
         acc_k, acc_v = acc_k + dkh, acc_v + dvh
     assert np.abs(dkg - acc_k).max() <= 1e-12 and np.abs(dvg - acc_v).max() <= 1e-12
+
+
+# ---------------------------------------------------------------- FP8 packed sequences
+
+@pytest.mark.parametrize("mode", ["block", "tensor"])
+def test_fp8_varlen_equal_lengths_equals_fixed(mode):
+    # B sequences of the same length packed: the varlen layout holds exactly the
+    # fixed-length codes and scales, rearranged, and the attention agrees
+    B, N, H, Hkv, d = 3, 200, 4, 2, 64
+    q, k, v = gen.qkv_fixed(B, N, H, Hkv, d, seed=31, dist="outlier")
+    fx = O.fp8_prepass(q, k, v, mode=mode, rotate=True, seed=5)
+    cu = np.arange(B + 1) * N
+    vl = O.fp8_prepass_varlen(q.reshape(B * N, H, d), k.reshape(B * N, Hkv, d), v.reshape(B * N, Hkv, d), cu,
+                              mode=mode, rotate=True, seed=5)
+    nb = (N + 127) // 128
+    assert list(vl["blk_off"]) == [0, nb, 2 * nb, 3 * nb]
+    if mode == "block":
+        assert np.array_equal(vl["q8"], fx["q8"].reshape(B * N, H, d))
+        assert np.array_equal(vl["k8"], fx["k8"].reshape(B * N, Hkv, d))
+        for b in range(B):
+            assert np.array_equal(vl["sq"][:, b * nb:(b + 1) * nb], fx["sq"][b])
+            assert np.array_equal(vl["sk"][:, b * nb:(b + 1) * nb], fx["sk"][b])
+            assert np.array_equal(vl["vt8"][:, :, 128 * b * nb:128 * b * nb + N], fx["vt8"][b])
+            assert np.all(vl["vt8"][:, :, 128 * b * nb + N:128 * (b + 1) * nb] == 0)
+        assert np.array_equal(vl["sv"], fx["sv"])
+    else:
+        # one scale per packed tensor = one scale per fixed-length tensor
+        assert np.array_equal(vl["q8"], fx["q8"].reshape(B * N, H, d))
+        for name in ("sq", "sk", "sv"):
+            assert np.array_equal(vl[name], fx[name])
+    for causal in (False, True):
+        o_f, l_f = O.fp8_attention_emulated(fx, causal=causal)
+        o_v, l_v = O.fp8_attention_emulated_varlen(vl, cu, causal=causal)
+        # fixed rows are ordered (b, h, i); varlen rows (s, h, i) - the same order here
+        assert np.abs(o_f - o_v).max() <= 1e-12 and np.abs(l_f - l_v).max() <= 1e-12
+
+
+def test_fp8_varlen_sequences_are_independent():
+    # each sequence's result depends on that sequence only: quantising it alone
+    # as a fixed-length batch of one gives the same codes, scales and attention
+    lengths = [5, 300, 128, 0, 129]
+    q, k, v, cu = gen.qkv_varlen(lengths, 4, 2, 64, seed=33)
+    vl = O.fp8_prepass_varlen(q, k, v, cu, mode="block", rotate=True, seed=1)
+    boff = vl["blk_off"]
+    assert list(boff) == list(O.fp8_varlen_block_offsets(cu)) == [0, 1, 4, 5, 5, 7]
+    for s, n in enumerate(lengths):
+        if n == 0:
+            continue
+        a = int(cu[s])
+        one = O.fp8_prepass(q[None, a:a + n], k[None, a:a + n], v[None, a:a + n], mode="block", rotate=True, seed=1)
+        assert np.array_equal(vl["q8"][a:a + n], one["q8"][0])
+        assert np.array_equal(vl["vt8"][:, :, 128 * boff[s]:128 * boff[s] + n], one["vt8"][0])
+        o1, l1 = O.fp8_attention_emulated(one, causal=True)
+        rows = (np.full(4 * n, s), np.repeat(np.arange(4), n), np.tile(np.arange(n), 4))
+        ov, lv = O.fp8_attention_emulated_varlen(vl, cu, causal=True, rows=rows)
+        assert np.abs(ov - o1).max() <= 1e-12 and np.abs(lv - l1).max() <= 1e-12
