@@ -616,6 +616,8 @@ def fp8_prepass_varlen(q, k, v, cu_seqlens, mode: str = "block", rotate: bool = 
         for s in range(nseq):
             a, b = int(cu[s]), int(cu[s + 1])
             if b == a:
+                # no rows: the channel amax over an empty set is 0, whose scale is 1
+                sv[s] = _scale_from_amax(np.zeros((Hkv, d), np.float32))
                 continue
             ps = fp8_prepass(qf[None, a:b], kf[None, a:b], vf[None, a:b], mode="block", rotate=rotate, seed=seed)
             q8[a:b], k8[a:b] = ps["q8"][0], ps["k8"][0]
