@@ -316,6 +316,8 @@ def run_ours(args):
         line["decode"] = decode_measure(min(args.steps, 100), args.warmup)
     if rank == 0 and not args.no_bwd:
         line["bwd"] = bwd_measure(min(args.steps, 50), args.warmup)
+    if rank == 0 and not args.no_fp8:
+        line["fp8_varlen"] = fp8_varlen_measure(min(args.steps, 20), args.warmup)
     if rank == 0 and not args.no_cpu_baseline:
         rate, threads, sample = cpu_oracle_rate(w, budget_s=args.cpu_budget)
         line["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -368,6 +370,60 @@ def bwd_measure(steps: int, warmup: int, seed: int = 0):
                      "unit": "TFLOP/s", "frac": round(fl / t / 1e12 / pk["bf16_tflops"], 4),
                      "flops": fl, "peak_source": f"{pk['source']} bf16 burst (cuBLAS)"},
         "gpu_launches_per_step": 4,
+    }
+
+
+def fp8_varlen_measure(steps: int, warmup: int, seed: int = 0):
+    """FP8 over packed sequences on the GQA varlen shape: 8 sequences with
+    lengths uniform in [1k, 32k] (seed 0), H=32, Hkv=8, d=128, causal, outlier
+    inputs, per-block scales + rotation. Work = sum over sequences of
+    2 H n^2 d (causal half of 4 H n^2 d). Pre-pass and forward timed apart
+    with CUDA events, L2 flushed before each call."""
+    import numpy as np
+    import torch
+
+    import attn_inputs as gen
+    import exact_attention_45_gb300 as A
+    lengths = gen.varlen_lengths(8, 1024, 32768, seed=seed)
+    q, k, v, cu = gen.qkv_varlen(lengths, 32, 8, 128, seed=seed, dist="outlier")
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    dcu = torch.as_tensor(cu, dtype=torch.int32).cuda()
+    pre = A.attn_fp8_prepass_varlen(q, k, v, dcu)
+    o = torch.empty((q.shape[0], 32, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((32, q.shape[0]), dtype=torch.float32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def timed(fn):
+        for _ in range(warmup):
+            flush.zero_()
+            fn()
+        ev = []
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            ev.append((e0, e1))
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / steps / 1e3
+
+    t_fwd = timed(lambda: A.attn_fwd_fp8_varlen(pre, causal=True, out=o, lse=lse))
+    t_pre = timed(lambda: A.attn_fp8_prepass_varlen(q, k, v, dcu))
+    if A.attn_get_device_error() != 0:
+        raise RuntimeError("device error in the FP8 varlen path")
+    fl = float(sum(2.0 * 32 * float(n) ** 2 * 128 for n in lengths))
+    pk = peaks()
+    fp8_peak = 2.0 * pk["bf16_tflops"]
+    return {
+        "config": {"workload": "fp8 varlen GQA causal d128", "nseq": 8, "lengths": "uniform [1024, 32768], seed 0",
+                   "H": 32, "Hkv": 8, "d": 128, "tokens": int(np.sum(lengths))},
+        "fwd_tflops": round(fl / t_fwd / 1e12, 2), "fwd_ms": round(t_fwd * 1e3, 4),
+        "fwd_roofline": {"bound": "tensor", "achieved": round(fl / t_fwd / 1e12, 2), "peak": fp8_peak,
+                         "unit": "TFLOP/s", "frac": round(fl / t_fwd / 1e12 / fp8_peak, 4),
+                         "peak_source": f"2 x {pk['source']} bf16 burst"},
+        "prepass_ms": round(t_pre * 1e3, 4),
+        "gpu_launches_per_step": 5,
     }
 
 

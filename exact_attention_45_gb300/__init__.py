@@ -15,6 +15,7 @@ Functions carry the C names:
 * ``attn_decode(q, k_cache, v_cache, seqlens, num_splits=0, ...)``
 * ``attn_combine(o_parts, lse_parts, dtype=torch.bfloat16)``
 * ``attn_bwd(q, k, v, o, lse, dout, causal=False, ...)``
+* ``attn_fp8_prepass_varlen(q, k, v, cu_seqlens, ...)``, ``attn_fwd_fp8_varlen(pre, ...)``
 * ``attn_get_device_error()``, ``attn_set_wait_timeout_ns(ns)``
 
 ``capi()`` returns the raw ctypes handle (pointer-and-size arguments).
@@ -35,7 +36,8 @@ __all__ = [
     "attn_fwd", "attn_fwd_varlen", "attn_fp8_prepass", "attn_fwd_fp8", "attn_fwd_fp8_auto",
     "attn_fp8_workspace_size", "attn_fp8_vt_ld", "attn_get_device_error", "attn_set_wait_timeout_ns",
     "attn_debug_timeout_probe", "attn_decode", "attn_decode_num_splits", "attn_decode_workspace_size",
-    "attn_combine", "attn_bwd", "attn_bwd_workspace_size", "EXPORTED_SYMBOLS",
+    "attn_combine", "attn_bwd", "attn_bwd_workspace_size", "attn_fp8_varlen_tmax", "attn_fp8_prepass_varlen",
+    "attn_fwd_fp8_varlen", "EXPORTED_SYMBOLS",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
@@ -48,7 +50,7 @@ EXPORTED_SYMBOLS = (
     "attn_fp8_workspace_size", "attn_fwd_fp8_auto", "attn_fwd_fp8_auto_noalloc", "attn_get_device_error",
     "attn_set_wait_timeout_ns", "attn_debug_timeout_probe", "attn_status_string", "attn_last_error_message",
     "attn_version", "attn_decode", "attn_decode_num_splits", "attn_decode_workspace_size", "attn_combine",
-    "attn_bwd", "attn_bwd_workspace_size",
+    "attn_bwd", "attn_bwd_workspace_size", "attn_fp8_varlen_tmax", "attn_fp8_prepass_varlen", "attn_fwd_fp8_varlen",
 )
 
 
@@ -100,6 +102,9 @@ def capi(build_if_missing: bool = True):
             "attn_combine": ([P, P, P, P, I, I, I, I, P], I),
             "attn_bwd": ([P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, I, P], I),
             "attn_bwd_workspace_size": ([I, I, I, I], SZ),
+            "attn_fp8_varlen_tmax": ([I, I], I),
+            "attn_fp8_prepass_varlen": ([P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, U64, P], I),
+            "attn_fwd_fp8_varlen": ([P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -325,6 +330,58 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
                            _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
                            int(bool(causal)), scale, _DTYPE[q.dtype], _stream(stream)))
     return dq, dk, dv
+
+
+def attn_fp8_varlen_tmax(total: int, nseq: int) -> int:
+    return int(capi().attn_fp8_varlen_tmax(total, nseq))
+
+
+def attn_fp8_prepass_varlen(q, k, v, cu_seqlens, mode: str = "block", rotate: bool = True, hadamard_seed: int = 0,
+                            stream=None):
+    """e4m3 codes and scales of packed bf16 q [T,H,d], k/v [T,Hkv,d] (int32 cu_seqlens on the device); a dict."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, H, d = q.shape
+    Hkv = k.shape[1]
+    nseq = cu_seqlens.numel() - 1
+    tmax = attn_fp8_varlen_tmax(T, nseq)
+    dev = q.device
+    u8 = torch.uint8
+    blk = mode == "block"
+    pre = {
+        "q8": torch.empty((T, H, d), dtype=u8, device=dev),
+        "k8": torch.empty((T, Hkv, d), dtype=u8, device=dev),
+        "vt8": torch.zeros((Hkv, d, 128 * tmax), dtype=u8, device=dev),
+        "sq": torch.empty((H, tmax) if blk else (1,), dtype=torch.float32, device=dev),
+        "sk": torch.empty((Hkv, tmax) if blk else (1,), dtype=torch.float32, device=dev),
+        "sv": torch.empty((nseq, Hkv, d) if blk else (1,), dtype=torch.float32, device=dev),
+        "blk_off": torch.empty((nseq + 1,), dtype=torch.int32, device=dev),
+        "cu_seqlens": cu_seqlens, "tmax": tmax, "mode": mode, "rotate": rotate, "seed": hadamard_seed,
+    }
+    _check(capi().attn_fp8_prepass_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(pre["q8"]),
+                                          _ptr(pre["k8"]), _ptr(pre["vt8"]), _ptr(pre["sq"]), _ptr(pre["sk"]),
+                                          _ptr(pre["sv"]), _ptr(pre["blk_off"]), nseq, T, H, Hkv, d, _FP8_MODE[mode],
+                                          int(bool(rotate)), int(hadamard_seed), _stream(stream)))
+    return pre
+
+
+def attn_fwd_fp8_varlen(pre: dict, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                        stream=None):
+    """O [T,H,d] (bf16) and lse [H,T] from attn_fp8_prepass_varlen outputs."""
+    q8, k8 = pre["q8"], pre["k8"]
+    T, H, d = q8.shape
+    Hkv = k8.shape[1]
+    cu = pre["cu_seqlens"]
+    nseq = cu.numel() - 1
+    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    lse = torch.empty((H, T), dtype=torch.float32, device=q8.device) if lse is None else lse
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check(capi().attn_fwd_fp8_varlen(_ptr(q8), _ptr(k8), _ptr(pre["vt8"]), _ptr(pre["sq"]), _ptr(pre["sk"]),
+                                      _ptr(pre["sv"]), _ptr(pre["blk_off"]), _ptr(cu), _ptr(out), _ptr(lse), nseq, T,
+                                      H, Hkv, d, int(bool(causal)), scale, _FP8_MODE[pre["mode"]], _stream(stream)))
+    return out, lse
 
 
 def attn_get_device_error(stream=None) -> int:

@@ -36,6 +36,8 @@ struct FwdParams {
   float scale_log2;        // softmax scale * log2(e)
   const int* seqlens;      // decode only: cached keys per sequence (device, nseq)
   int num_splits;          // decode only: key-range splits per (sequence, KV head)
+  const int* blk_off;      // FP8 packed sequences: first 128-row block of each sequence
+  int tmax;                // FP8 packed sequences: columns of the block-scale rows
   int split_chunk;         // decode only: keys per split (a multiple of 128)
   unsigned long long timeout_ns;
   unsigned int* err;       // device error word

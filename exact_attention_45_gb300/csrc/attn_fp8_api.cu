@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "api_internal.h"
+#include "attn_common.cuh"
 #include "attn45.h"
 #include "fp8_launchers.h"
 #include "fp8_prepass.h"
@@ -191,7 +192,7 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* s
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = api_timeout_ns();
   p.err = err;
-  cudaError_t e = launch_fwd_fp8_d128(mq, mk, mv, mo, p, causal != 0, sm, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_fwd_fp8_d128(mq, mk, mv, mo, p, causal != 0, false, sm, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return api_cuda_fail(e, "attn_fwd_fp8 launch");
   return ATTN_OK;
 }
@@ -213,6 +214,119 @@ int attn_fwd_fp8_auto(const void* q, const void* k, const void* v, void* o, floa
   if (rc) return rc;
   return attn_fwd_fp8(w + L.q8, w + L.k8, w + L.vt8, sq, sk, sv, o, lse, B, H, Hkv, N, d, causal, scale, mode,
                       stream);
+}
+
+int attn_fp8_varlen_tmax(int total, int nseq) {
+  if (total < 0 || nseq < 1) return 0;
+  return (total + 127) / 128 + nseq;
+}
+
+int attn_fp8_prepass_varlen(const void* q, const void* k, const void* v, const int* cu_seqlens, void* q8, void* k8,
+                            void* vt8, float* sq, float* sk, float* sv, int* blk_off, int nseq, int total, int H,
+                            int Hkv, int d, int mode, int rotate, uint64_t hadamard_seed, void* stream) {
+  if (nseq < 1 || nseq > MAX_VARLEN_SEQS) return api_fail(ATTN_ERR_INVALID_ARG, "nseq must be in [1, 2048]");
+  if (total < 0) return api_fail(ATTN_ERR_INVALID_ARG, "total must be >= 0");
+  if (H < 1 || Hkv < 1 || H % Hkv != 0) return api_fail(ATTN_ERR_INVALID_ARG, "need H % Hkv == 0");
+  if (d != 64 && d != 128 && d != 256) return api_fail(ATTN_ERR_UNSUPPORTED, "head dim not in {64,128,256}");
+  if (mode != ATTN_FP8_PER_TENSOR && mode != ATTN_FP8_PER_BLOCK) return api_fail(ATTN_ERR_INVALID_ARG, "unknown FP8 mode");
+  if (rotate != 0 && rotate != 1) return api_fail(ATTN_ERR_INVALID_ARG, "rotate must be 0 or 1");
+  const int tmax = attn_fp8_varlen_tmax(total, nseq);
+  if ((long long)(H + 2 * Hkv) * tmax > 0x7fffffffLL || (long long)total * H * d > 0x7fffffffffLL)
+    return api_fail(ATTN_ERR_INVALID_ARG, "problem too large");
+  if (!q || !k || !v || !cu_seqlens || !q8 || !k8 || !vt8 || !sq || !sk || !sv || !blk_off)
+    return api_fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q8, 16) || !aligned(k8, 16) ||
+      !aligned(vt8, 16) || !aligned(sq, 4) || !aligned(sk, 4) || !aligned(sv, 4) || !aligned(blk_off, 4) ||
+      !aligned(cu_seqlens, 4))
+    return api_fail(ATTN_ERR_INVALID_ARG, "tensors must be 16-byte aligned, scales and indices 4-byte aligned");
+  int sm = 0;
+  unsigned int* err = nullptr;
+  int rc;
+  if ((rc = api_device(&sm, &err))) return rc;
+  PrepassArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.q8 = static_cast<uint8_t*>(q8);
+  a.k8 = static_cast<uint8_t*>(k8);
+  a.vt8 = static_cast<uint8_t*>(vt8);
+  a.sq = sq;
+  a.sk = sk;
+  a.sv = sv;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.ldv = 128 * tmax;
+  a.block_mode = mode == ATTN_FP8_PER_BLOCK;
+  a.rotate = rotate;
+  a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
+  for (int c = 0; c < d; ++c)
+    if (splitmix64(hadamard_seed + (uint64_t)c) & 1ull) a.sign_bits[c >> 5] |= 1u << (c & 31);
+  a.timeout_ns = api_timeout_ns();
+  a.err = err;
+  a.varlen = 1;
+  a.nseq = nseq;
+  a.tmax = tmax;
+  a.cu = cu_seqlens;
+  a.blk_off = blk_off;
+  cudaError_t e = launch_fp8_prepass_varlen(a, d, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return api_cuda_fail(e, "attn_fp8_prepass_varlen launch");
+  return ATTN_OK;
+}
+
+int attn_fwd_fp8_varlen(const void* q8, const void* k8, const void* vt8, const float* sq, const float* sk,
+                        const float* sv, const int* blk_off, const int* cu_seqlens, void* o, float* lse, int nseq,
+                        int total, int H, int Hkv, int d, int causal, float scale, int mode, void* stream) {
+  if (nseq < 1 || nseq > MAX_VARLEN_SEQS) return api_fail(ATTN_ERR_INVALID_ARG, "nseq must be in [1, 2048]");
+  if (total < 0) return api_fail(ATTN_ERR_INVALID_ARG, "total must be >= 0");
+  if (H < 1 || Hkv < 1 || H % Hkv != 0) return api_fail(ATTN_ERR_INVALID_ARG, "need H % Hkv == 0");
+  if (d != 128) return api_fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward is built for head dim 128");
+  if (mode != ATTN_FP8_PER_TENSOR && mode != ATTN_FP8_PER_BLOCK) return api_fail(ATTN_ERR_INVALID_ARG, "unknown FP8 mode");
+  if (causal != 0 && causal != 1) return api_fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return api_fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if ((long long)H * ((long long)total / 128 + nseq + 1) > 0x7fffffffLL)
+    return api_fail(ATTN_ERR_INVALID_ARG, "problem too large for int32 indexing");
+  if (total == 0) return ATTN_OK;
+  if (!q8 || !k8 || !vt8 || !sq || !sk || !sv || !blk_off || !cu_seqlens || !o || !lse)
+    return api_fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(vt8, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(sq, 4) || !aligned(sk, 4) || !aligned(sv, 4) || !aligned(blk_off, 4) || !aligned(cu_seqlens, 4))
+    return api_fail(ATTN_ERR_INVALID_ARG, "tensors must be 16-byte aligned, scales and indices 4-byte aligned");
+  int sm = 0;
+  unsigned int* err = nullptr;
+  int rc;
+  if ((rc = api_device(&sm, &err))) return rc;
+  const int tmax = attn_fp8_varlen_tmax(total, nseq);
+  CUtensorMap mq, mk, mv;
+  if ((rc = api_make_map(&mq, true, q8, d, H, total, 1, 128, 128))) return rc;
+  if ((rc = api_make_map(&mk, true, k8, d, Hkv, total, 1, 128, 128))) return rc;
+  // V^T codes: [Hkv][d][128 * tmax] read as boxes of (128 keys) x (d channel rows)
+  if ((rc = api_make_map_rows(&mv, vt8, 128 * (uint64_t)tmax, d, Hkv, 128, d))) return rc;
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.o = o;
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.sq = sq;
+  p.sk = sk;
+  p.sv = sv;
+  p.blk_off = blk_off;
+  p.tmax = tmax;
+  p.nseq = nseq;
+  p.total = total;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.group = H / Hkv;
+  p.ntiles = 0;          // counted on the device from cu_seqlens
+  p.vt_ld = 128 * tmax;
+  p.fp8_block = mode == ATTN_FP8_PER_BLOCK;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = api_timeout_ns();
+  p.err = err;
+  // packed sequences store O row by row: the output-map argument is not read
+  cudaError_t e = launch_fwd_fp8_d128(mq, mk, mv, mq, p, causal != 0, true, sm, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return api_cuda_fail(e, "attn_fwd_fp8_varlen launch");
+  return ATTN_OK;
 }
 
 // Same computation as attn_fwd_fp8_auto, for callers that are not allowed to

@@ -160,12 +160,14 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return m;
 }
 
-// Q or K row block: rows [blk*128, blk*128+128) of (b, head).
+// Q or K row block: rows [blk*128, blk*128+128) of a sequence whose row 0 is
+// token tok0 and which has nrows rows; the block's scale goes to sc[sc_idx].
 // phase 0, block mode : rotate, block amax -> scale, codes, scale written.
 // phase 0, tensor mode: rotate, block amax -> atomicMax into amax_out[0].
 // phase 1, tensor mode: rotate, codes with the tensor amax in amax_out[0].
 template <int E>
-__device__ void qk_block(const PrepassArgs& a, bool is_q, int b, int head, int blk, int phase) {
+__device__ void qk_block(const PrepassArgs& a, bool is_q, size_t tok0, int nrows, int head, int blk, size_t sc_idx,
+                         int phase) {
   __shared__ float red[THREADS / 32];
   const int Hx = is_q ? a.H : a.Hkv;
   const __nv_bfloat16* src = is_q ? a.q : a.k;
@@ -179,8 +181,8 @@ __device__ void qk_block(const PrepassArgs& a, bool is_q, int b, int head, int b
 #pragma unroll
   for (int rr = 0; rr < ROWS_PER_WARP; ++rr) {
     const int n = blk * ROWS + warp * ROWS_PER_WARP + rr;
-    if (n < a.N) {
-      const size_t row = ((size_t)b * a.N + n) * Hx + head;
+    if (n < nrows) {
+      const size_t row = (tok0 + n) * Hx + head;
       load_row<E>(src + row * d + E * lane, x[rr]);
       if (a.rotate) rotate_row<E>(x[rr], sign_lane, a.inv_sqrt_d, lane);
 #pragma unroll
@@ -191,7 +193,7 @@ __device__ void qk_block(const PrepassArgs& a, bool is_q, int b, int head, int b
   if (a.block_mode) {
     amax = block_max(amax, red);
     s = scale_from_amax(amax);
-    if (threadIdx.x == 0) sc[((size_t)b * Hx + head) * a.nblk + blk] = s;
+    if (threadIdx.x == 0) sc[sc_idx] = s;
   } else if (phase == 0) {
     amax = block_max(amax, red);
     if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(sc), __float_as_uint(amax));
@@ -203,18 +205,21 @@ __device__ void qk_block(const PrepassArgs& a, bool is_q, int b, int head, int b
 #pragma unroll
   for (int rr = 0; rr < ROWS_PER_WARP; ++rr) {
     const int n = blk * ROWS + warp * ROWS_PER_WARP + rr;
-    if (n < a.N) {
-      const size_t row = ((size_t)b * a.N + n) * Hx + head;
+    if (n < nrows) {
+      const size_t row = (tok0 + n) * Hx + head;
       store_codes<E>(dst + row * d + E * lane, x[rr], dv);
     }
   }
 }
 
-// V row block of (b, kv head). phase 0: per-channel (block mode) or whole
-// tensor amax -> atomicMax into sv. phase 1: codes with those amax values,
-// written transposed into vt8[b][head][c][n] through shared memory.
+// V row block of (sequence, kv head): rows as in qk_block; sv_row = first of
+// the D per-channel amax values of (sequence, kv head). phase 0: per-channel
+// (block mode) or whole tensor amax -> atomicMax into sv. phase 1: codes with
+// those amax values, written transposed through shared memory into rows
+// vt_row0 + c (row length a.ldv) from column vt_col.
 template <int E>
-__device__ void v_block(const PrepassArgs& a, int b, int head, int blk, int phase) {
+__device__ void v_block(const PrepassArgs& a, size_t tok0, int nrows, int head, int blk, size_t sv_row, size_t vt_row0,
+                        size_t vt_col, int phase) {
   constexpr int D = E * 32;
   constexpr int TP = ROWS + 4;                      // padded row of the transposed tile
   __shared__ __align__(16) uint8_t tile[D * TP];
@@ -227,8 +232,8 @@ __device__ void v_block(const PrepassArgs& a, int b, int head, int blk, int phas
 #pragma unroll
   for (int rr = 0; rr < ROWS_PER_WARP; ++rr) {
     const int n = blk * ROWS + warp * ROWS_PER_WARP + rr;
-    if (n < a.N) {
-      const size_t row = ((size_t)b * a.N + n) * a.Hkv + head;
+    if (n < nrows) {
+      const size_t row = (tok0 + n) * a.Hkv + head;
       load_row<E>(a.v + row * D + E * lane, x[rr]);
 #pragma unroll
       for (int e = 0; e < E; ++e) amax_c[e] = fmaxf(amax_c[e], fabsf(x[rr][e]));
@@ -249,8 +254,7 @@ __device__ void v_block(const PrepassArgs& a, int b, int head, int blk, int phas
         float m = part[0][threadIdx.x];
 #pragma unroll
         for (int w = 1; w < THREADS / 32; ++w) m = fmaxf(m, part[w][threadIdx.x]);
-        atomicMax(reinterpret_cast<unsigned int*>(sv + ((size_t)b * a.Hkv + head) * D + threadIdx.x),
-                  __float_as_uint(m));
+        atomicMax(reinterpret_cast<unsigned int*>(sv + sv_row + threadIdx.x), __float_as_uint(m));
       }
     } else {
       float m = 0.f;
@@ -265,7 +269,7 @@ __device__ void v_block(const PrepassArgs& a, int b, int head, int blk, int phas
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const unsigned int bits = a.block_mode
-        ? *reinterpret_cast<volatile unsigned int*>(sv + ((size_t)b * a.Hkv + head) * D + E * lane + e)
+        ? *reinterpret_cast<volatile unsigned int*>(sv + sv_row + E * lane + e)
         : *reinterpret_cast<volatile unsigned int*>(sv);
     s[e] = scale_from_amax(__uint_as_float(bits));
   }
@@ -287,35 +291,88 @@ __device__ void v_block(const PrepassArgs& a, int b, int head, int blk, int phas
     }
   }
   __syncthreads();
-  // rows of vt8: 128 keys = 32 lanes x 4 bytes; pad keys (n >= N) hold code 0
-  const size_t base = ((size_t)b * a.Hkv + head) * D;
+  // rows of vt8: 128 keys = 32 lanes x 4 bytes; pad keys (n >= nrows) hold code 0
   for (int c = warp; c < D; c += THREADS / 32) {
     const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[c * TP + 4 * lane]);
-    *reinterpret_cast<uint32_t*>(a.vt8 + (base + c) * a.ldv + (size_t)blk * ROWS + 4 * lane) = w;
+    *reinterpret_cast<uint32_t*>(a.vt8 + (vt_row0 + c) * a.ldv + vt_col + 4 * lane) = w;
   }
 }
 
 template <int E>
 __global__ void __launch_bounds__(THREADS) prepass_kernel(const PrepassArgs a, int phase, int block_offset) {
-  // blocks: [Q blocks][K blocks][V blocks], each B * heads * nblk
+  constexpr int D = E * 32;
   int id = blockIdx.x + block_offset;
+  if (a.varlen) {
+    // blocks: [Q: H x tmax][K: Hkv x tmax][V: Hkv x tmax] of global block
+    // indices gb; sequence s owns gb in [blk_off[s], blk_off[s+1])
+    int kind, head, gb;
+    if (id < a.H * a.tmax) { kind = 0; head = id / a.tmax; gb = id % a.tmax; }
+    else if ((id -= a.H * a.tmax) < a.Hkv * a.tmax) { kind = 1; head = id / a.tmax; gb = id % a.tmax; }
+    else { id -= a.Hkv * a.tmax; kind = 2; head = id / a.tmax; gb = id % a.tmax; }
+    if (gb >= __ldg(a.blk_off + a.nseq)) return;
+    if (kind < 2 && phase == 1 && a.block_mode) return;
+    int lo = 0, hi = a.nseq - 1;                        // last s with blk_off[s] <= gb
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(a.blk_off + mid) <= gb) lo = mid; else hi = mid - 1;
+    }
+    const int s = lo;
+    const int blk = gb - __ldg(a.blk_off + s);
+    const size_t tok0 = (size_t)__ldg(a.cu + s);
+    const int nrows = __ldg(a.cu + s + 1) - __ldg(a.cu + s);
+    if (kind < 2) {
+      qk_block<E>(a, kind == 0, tok0, nrows, head, blk, (size_t)head * a.tmax + gb, phase);
+    } else {
+      v_block<E>(a, tok0, nrows, head, blk, ((size_t)s * a.Hkv + head) * D, (size_t)head * D, (size_t)gb * ROWS,
+                 phase);
+    }
+    return;
+  }
+  // blocks: [Q blocks][K blocks][V blocks], each B * heads * nblk
   const int nq = a.B * a.H * a.nblk, nk = a.B * a.Hkv * a.nblk;
   if (id < nq) {
     if (phase == 1 && a.block_mode) return;   // Q done in phase 0
     const int blk = id % a.nblk, bh = id / a.nblk;
-    qk_block<E>(a, true, bh / a.H, bh % a.H, blk, phase);
+    const int b = bh / a.H, h = bh % a.H;
+    qk_block<E>(a, true, (size_t)b * a.N, a.N, h, blk, ((size_t)b * a.H + h) * a.nblk + blk, phase);
     return;
   }
   id -= nq;
   if (id < nk) {
     if (phase == 1 && a.block_mode) return;
     const int blk = id % a.nblk, bh = id / a.nblk;
-    qk_block<E>(a, false, bh / a.Hkv, bh % a.Hkv, blk, phase);
+    const int b = bh / a.Hkv, h = bh % a.Hkv;
+    qk_block<E>(a, false, (size_t)b * a.N, a.N, h, blk, ((size_t)b * a.Hkv + h) * a.nblk + blk, phase);
     return;
   }
   id -= nk;
   const int blk = id % a.nblk, bh = id / a.nblk;
-  v_block<E>(a, bh / a.Hkv, bh % a.Hkv, blk, phase);
+  const int b = bh / a.Hkv, h = bh % a.Hkv;
+  v_block<E>(a, (size_t)b * a.N, a.N, h, blk, ((size_t)b * a.Hkv + h) * D, ((size_t)b * a.Hkv + h) * D,
+             (size_t)blk * ROWS, phase);
+}
+
+// blk_off[s] = sum over s' < s of ceil(n_s' / 128), s = 0..nseq (one CTA).
+__global__ void __launch_bounds__(1024) varlen_block_offsets_kernel(const int* cu, int nseq, int* blk_off) {
+  __shared__ int part[1024];
+  const int per = (nseq + 1023) / 1024;
+  const int s0 = threadIdx.x * per;
+  int sum = 0;
+  for (int s = s0; s < s0 + per && s < nseq; ++s) sum += (__ldg(cu + s + 1) - __ldg(cu + s) + ROWS - 1) / ROWS;
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {          // inclusive scan of the per-thread sums
+    const int v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int run = threadIdx.x > 0 ? part[threadIdx.x - 1] : 0;
+  for (int s = s0; s < s0 + per && s < nseq; ++s) {
+    blk_off[s] = run;
+    run += (__ldg(cu + s + 1) - __ldg(cu + s) + ROWS - 1) / ROWS;
+  }
+  if (threadIdx.x == 1023) blk_off[nseq] = part[1023];
 }
 
 
@@ -566,6 +623,35 @@ __global__ void finalize_kernel(float* sq, float* sk, float* sv, int nsv, int te
 }
 
 }  // namespace
+
+// Packed sequences (a.varlen): block offsets, then the generic kernels over
+// H x tmax, Hkv x tmax and Hkv x tmax global blocks (those past the last
+// sequence exit at once).
+cudaError_t launch_fp8_prepass_varlen(const PrepassArgs& a, int d, cudaStream_t s) {
+  const size_t nsv = a.block_mode ? (size_t)a.nseq * a.Hkv * d : 1;
+  cudaError_t e = cudaMemsetAsync(a.sv, 0, nsv * sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  if (!a.block_mode) {
+    if ((e = cudaMemsetAsync(a.sq, 0, sizeof(float), s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(a.sk, 0, sizeof(float), s)) != cudaSuccess) return e;
+  }
+  // V^T pad keys of each sequence's last block are written as code 0 by the
+  // V kernel; columns past the last block are never read
+  varlen_block_offsets_kernel<<<1, 1024, 0, s>>>(a.cu, a.nseq, a.blk_off);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int blocks = (a.H + 2 * a.Hkv) * a.tmax;
+  for (int phase = 0; phase < 2; ++phase) {
+    switch (d) {
+      case 64: prepass_kernel<2><<<blocks, THREADS, 0, s>>>(a, phase, 0); break;
+      case 128: prepass_kernel<4><<<blocks, THREADS, 0, s>>>(a, phase, 0); break;
+      default: prepass_kernel<8><<<blocks, THREADS, 0, s>>>(a, phase, 0); break;
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  // amax values -> scales (phase 1 derived its divisors from the amax values)
+  finalize_kernel<<<(int)((nsv + 255) / 256), 256, 0, s>>>(a.sq, a.sk, a.sv, (int)nsv, a.block_mode ? 0 : 1);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps* maps, int sm_count,
                                cudaStream_t s) {

@@ -326,7 +326,13 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           if (j >= 1) {
             if constexpr (FP8) {
               // V^T block: 128 keys x D channel rows of (batch, kv head)
-              tma_load_4d(&tmV, &bars->slot_full[st], sV + st * T::KV_BYTES, (j - 1) * BN, 0, tl.seq * p.Hkv + hk, 0);
+              // V^T block: 128 keys x D channel rows; fixed: [B*Hkv][D][ldv];
+              // packed sequences: [Hkv][D][ldv] from column 128 * blk_off[seq]
+              if constexpr (VARLEN)
+                tma_load_4d(&tmV, &bars->slot_full[st], sV + st * T::KV_BYTES,
+                            (__ldg(p.blk_off + tl.seq) + j - 1) * BN, 0, hk, 0);
+              else
+                tma_load_4d(&tmV, &bars->slot_full[st], sV + st * T::KV_BYTES, (j - 1) * BN, 0, tl.seq * p.Hkv + hk, 0);
             } else {
 #pragma unroll
               for (int c = 0; c < T::NC; ++c)
@@ -479,15 +485,20 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         continue;
       }
       const int hk = kv_head(tl);
-      const int nb128 = ceil_div(tl.n, BLOCK_M);      // 128-row scale blocks (FP8)
+      // FP8 block scales: fixed [B][heads][ceil(N/128)]; packed sequences
+      // [heads][tmax] from column blk_off[seq]
+      const int nb128 = VARLEN ? p.tmax : ceil_div(tl.n, BLOCK_M);
+      const size_t sblk0 = VARLEN ? (size_t)(FP8 ? __ldg(p.blk_off + tl.seq) : 0) : 0;
+      const size_t sq_row = VARLEN ? (size_t)tl.h * nb128 + sblk0 : ((size_t)tl.seq * p.H + tl.h) * nb128;
+      const size_t sk_row = VARLEN ? (size_t)hk * nb128 + sblk0 : ((size_t)tl.seq * p.Hkv + hk) * nb128;
       float sq_x = 1.f;
       if constexpr (FP8)
-        sq_x = p.fp8_block ? __ldg(p.sq + ((size_t)tl.seq * p.H + tl.h) * nb128 + (row0 >> 7)) : __ldg(p.sq);
+        sq_x = p.fp8_block ? __ldg(p.sq + sq_row + (row0 >> 7)) : __ldg(p.sq);
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nblk; ++j) {
         float sl2 = p.scale_log2;
         if constexpr (FP8)
-          sl2 *= sq_x * (p.fp8_block ? __ldg(p.sk + ((size_t)tl.seq * p.Hkv + hk) * nb128 + j) : __ldg(p.sk));
+          sl2 *= sq_x * (p.fp8_block ? __ldg(p.sk + sk_row + j) : __ldg(p.sk));
         ok = mbar_wait(&bars->s_full[x], s_cnt & 1, tmo, abort_flag, p.err);
         ++s_cnt;
         if (!ok) break;

@@ -17,6 +17,13 @@ struct PrepassArgs {
   uint32_t sign_bits[8];           // bit c set <=> sigma_c = -1 (d <= 256)
   unsigned long long timeout_ns;   // bound for device waits
   unsigned int* err;               // device error word
+  // packed sequences (varlen != 0): inputs THD [total, heads, d], sequence s
+  // owns tokens [cu[s], cu[s+1]); blk_off [nseq+1] is written by the pre-pass;
+  // scales sq [H, tmax], sk [Hkv, tmax], sv [nseq, Hkv, d]; vt8 [Hkv, d, ldv]
+  // with ldv = 128 * tmax and sequence s's keys from column 128 * blk_off[s].
+  int varlen, nseq, tmax;
+  const int* cu;
+  int* blk_off;
 };
 
 // Tensor maps of the head-dim-128 path: bf16 inputs (Q, K, V) {128, heads, N, B}
@@ -30,5 +37,7 @@ struct Prepass128Maps {
 // maps: required for the fast head-dim-128 path (nullptr selects the generic one).
 cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps* maps, int sm_count,
                                cudaStream_t s);
+// Packed sequences: block offsets, two passes of the generic kernels, finalise.
+cudaError_t launch_fp8_prepass_varlen(const PrepassArgs& a, int d, cudaStream_t s);
 
 }  // namespace attn45

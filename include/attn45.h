@@ -158,6 +158,33 @@ ATTN45_API int attn_fwd_fp8_auto_noalloc(const void* q, const void* k, const voi
                                          uint64_t hadamard_seed, void* stream);
 
 /*
+ * FP8 over packed variable-length sequences (THD, as attn_fwd_varlen).
+ * Every sequence is quantised on its own (128-row blocks never cross a
+ * sequence boundary; V's channel scales are per (sequence, KV head)).
+ *   tmax = attn_fp8_varlen_tmax(total, nseq) = ceil(total/128) + nseq bounds
+ *   the number of 128-row blocks over all sequences.
+ * attn_fp8_prepass_varlen -- bf16 q [total,H,d], k, v [total,Hkv,d] ->
+ *   q8 [total,H,d], k8 [total,Hkv,d] (e4m3 codes); vt8 [Hkv, d, 128*tmax]
+ *   (V codes transposed, sequence s's keys from column 128*blk_off[s], the
+ *   pad keys of its last block code 0); block mode: sq [H, tmax],
+ *   sk [Hkv, tmax] (sequence s's block b in column blk_off[s] + b),
+ *   sv [nseq, Hkv, d]; tensor mode: sq, sk, sv one float each; blk_off:
+ *   DEVICE int32 [nseq+1] written here, blk_off[s] = sum over s' < s of
+ *   ceil(n_s'/128). d in {64, 128, 256}; cu_seqlens as in attn_fwd_varlen.
+ * attn_fwd_fp8_varlen -- the FP8 forward over those outputs (d = 128):
+ *   o [total, H, d] bf16, lse [H, total] fp32; causal masking per sequence.
+ */
+ATTN45_API int attn_fp8_varlen_tmax(int total, int nseq);
+ATTN45_API int attn_fp8_prepass_varlen(const void* q, const void* k, const void* v, const int* cu_seqlens, void* q8,
+                                       void* k8, void* vt8, float* sq, float* sk, float* sv, int* blk_off, int nseq,
+                                       int total, int H, int Hkv, int d, int mode, int rotate, uint64_t hadamard_seed,
+                                       void* stream);
+ATTN45_API int attn_fwd_fp8_varlen(const void* q8, const void* k8, const void* vt8, const float* sq, const float* sk,
+                                   const float* sv, const int* blk_off, const int* cu_seqlens, void* o, float* lse,
+                                   int nseq, int total, int H, int Hkv, int d, int causal, float scale, int mode,
+                                   void* stream);
+
+/*
  * Split-KV decode: one query token per sequence and query head attends to
  * the first seqlens[b] keys of its KV head's cache (the decode phase of
  * "FlashAttention-3 ..." references [49] and [51]; the merge of partial

@@ -1,0 +1,109 @@
+"""GPU parity of the FP8 path over packed variable-length sequences: the
+pre-pass bit for bit against the oracle's packed pre-pass, the forward against
+the oracle's FP8 emulation (same bounds as the fixed-length FP8 tests), packed
+equal-length sequences against the fixed-length path, and the FP8 error gate on
+the GQA varlen configuration at full size."""
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs as gen
+import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_prepass(q, k, v, cu, mode, rotate, seed):
+    import exact_attention_45_gb300 as A
+    dcu = torch.as_tensor(cu, dtype=torch.int32).cuda()
+    pre = A.attn_fp8_prepass_varlen(q.cuda(), k.cuda(), v.cuda(), dcu, mode=mode, rotate=rotate, hadamard_seed=seed)
+    torch.cuda.synchronize()
+    assert A.attn_get_device_error() == 0
+    return pre
+
+
+@pytest.mark.parametrize("mode", ["block", "tensor"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_prepass_varlen_bit_exact(mode, d):
+    lengths = [1, 130, 257, 0, 128, 500]
+    q, k, v, cu = gen.qkv_varlen(lengths, 4, 2, d, seed=d, dist="outlier")
+    pre = _gpu_prepass(q, k, v, cu, mode, True, 3)
+    ref = O.fp8_prepass_varlen(q, k, v, cu, mode=mode, rotate=True, seed=3)
+    assert np.array_equal(pre["blk_off"].cpu().numpy(), ref["blk_off"])
+    assert np.array_equal(pre["q8"].cpu().numpy(), ref["q8"])
+    assert np.array_equal(pre["k8"].cpu().numpy(), ref["k8"])
+    used = 128 * int(ref["blk_off"][-1])
+    assert np.array_equal(pre["vt8"].cpu().numpy()[:, :, :used], ref["vt8"][:, :, :used])
+    nb = int(ref["blk_off"][-1])
+    if mode == "block":
+        assert np.array_equal(pre["sq"].cpu().numpy()[:, :nb], ref["sq"][:, :nb])
+        assert np.array_equal(pre["sk"].cpu().numpy()[:, :nb], ref["sk"][:, :nb])
+    for name in ("sv",) if mode == "block" else ("sq", "sk", "sv"):
+        assert np.array_equal(pre[name].cpu().numpy(), ref[name]), name
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("mode", ["block", "tensor"])
+def test_fp8_forward_varlen_matches_emulation(causal, mode):
+    import exact_attention_45_gb300 as A
+    lengths = [1, 130, 257, 0, 300, 129]
+    q, k, v, cu = gen.qkv_varlen(lengths, 4, 2, 128, seed=7 + causal, dist="outlier")
+    pre = _gpu_prepass(q, k, v, cu, mode, True, 1)
+    o, lse = A.attn_fwd_fp8_varlen(pre, causal=causal)
+    torch.cuda.synchronize()
+    assert A.attn_get_device_error() == 0
+    ref = O.fp8_prepass_varlen(q, k, v, cu, mode=mode, rotate=True, seed=1)
+    o_ref, l_ref = O.fp8_attention_emulated_varlen(ref, cu, causal=causal)
+    rs, rh, ri = [], [], []
+    for s, n in enumerate(lengths):
+        for h in range(4):
+            rs += [s] * n
+            rh += [h] * n
+            ri += list(range(n))
+    tok = np.asarray(cu)[np.array(rs)] + np.array(ri)
+    o_g = o.float().cpu().numpy()[tok, np.array(rh)]
+    l_g = lse.cpu().numpy()[np.array(rh), tok]
+    err = o_g - o_ref
+    bound = 1e-2 + 4e-3 * np.abs(o_ref)
+    assert float((np.abs(err) / bound).max()) <= 1.0 and float(np.sqrt((err ** 2).mean())) <= 2e-3
+    assert np.abs(l_g - l_ref).max() <= 2e-3
+
+
+def test_fp8_varlen_equal_lengths_equals_fixed():
+    import exact_attention_45_gb300 as A
+    B, N, H, Hkv, d = 3, 384, 4, 2, 128
+    q, k, v = gen.qkv_fixed(B, N, H, Hkv, d, seed=12, dist="outlier")
+    cu = np.arange(B + 1) * N
+    pre_v = _gpu_prepass(q.reshape(B * N, H, d), k.reshape(B * N, Hkv, d), v.reshape(B * N, Hkv, d), cu, "block",
+                         True, 4)
+    o_v, l_v = A.attn_fwd_fp8_varlen(pre_v, causal=True)
+    pre_f = A.attn_fp8_prepass(q.cuda(), k.cuda(), v.cuda(), mode="block", rotate=True, hadamard_seed=4)
+    o_f, l_f = A.attn_fwd_fp8(pre_f, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(pre_v["q8"].reshape(B, N, H, d), pre_f["q8"])
+    assert torch.equal(o_v.reshape(B, N, H, d), o_f)
+    assert torch.equal(l_v.reshape(H, B, N).permute(1, 0, 2), l_f)
+
+
+def test_fp8_gqa_varlen_full_size_error_gate():
+    # 8 sequences with lengths uniform in [1k, 32k], H=32, Hkv=8, d=128,
+    # outlier inputs: RMS against exact attention within the FP8 gate, and
+    # block scales with rotation below the plain per-tensor FP8 error
+    import exact_attention_45_gb300 as A
+    lengths = gen.varlen_lengths(8, 1024, 32768, seed=0)
+    q, k, v, cu = gen.qkv_varlen(lengths, 32, 8, 128, seed=0, dist="outlier")
+    dcu = torch.as_tensor(cu, dtype=torch.int32).cuda()
+    rs, rh, ri = gen.sample_rows(lengths, 32, 128, seed=0)
+    o_ref, _ = O.attention(q, k, v, causal=True, cu_seqlens=cu, rows=(rs, rh, ri))
+    tok = np.asarray(cu)[rs] + ri
+    rms = {}
+    for mode, rotate in (("block", True), ("tensor", False)):
+        pre = A.attn_fp8_prepass_varlen(q.cuda(), k.cuda(), v.cuda(), dcu, mode=mode, rotate=rotate)
+        o, lse = A.attn_fwd_fp8_varlen(pre, causal=True)
+        torch.cuda.synchronize()
+        assert A.attn_get_device_error() == 0
+        o_h = o.float().cpu().numpy()
+        assert np.isfinite(o_h).all()
+        rms[mode] = float(np.sqrt(((o_h[tok, rh] - o_ref) ** 2).mean()))
+    assert rms["block"] <= 2.5e-2, rms
+    assert rms["block"] < rms["tensor"], rms
