@@ -196,6 +196,13 @@ __device__ __forceinline__ int tile2_blocks(const Tile2& tl, int x) {
   return ceil_div(kend, BN);
 }
 
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
   uint16_t lo, hi;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
@@ -519,15 +526,17 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           for (int c = 0; c < BN; ++c)
             if (c >= limit) s[c] = -INFINITY;
         }
-        float mxa = fmaxf(s[0], s[1]), mxb = fmaxf(s[2], s[3]);
-        float mxc = fmaxf(s[4], s[5]), mxd = fmaxf(s[6], s[7]);
+        float mxa = fmax3(s[0], s[1], s[2]), mxb = fmax3(s[3], s[4], s[5]);
+        float mxc = fmax3(s[6], s[7], s[8]), mxd = fmax3(s[9], s[10], s[11]);
 #pragma unroll
-        for (int c = 8; c < BN; c += 8) {
-          mxa = fmaxf(mxa, fmaxf(s[c], s[c + 1]));
-          mxb = fmaxf(mxb, fmaxf(s[c + 2], s[c + 3]));
-          mxc = fmaxf(mxc, fmaxf(s[c + 4], s[c + 5]));
-          mxd = fmaxf(mxd, fmaxf(s[c + 6], s[c + 7]));
+        for (int c = 12; c < BN - 4; c += 8) {
+          mxa = fmax3(mxa, s[c], s[c + 1]);
+          mxb = fmax3(mxb, s[c + 2], s[c + 3]);
+          mxc = fmax3(mxc, s[c + 4], s[c + 5]);
+          mxd = fmax3(mxd, s[c + 6], s[c + 7]);
         }
+        mxa = fmax3(mxa, s[BN - 4], s[BN - 3]);
+        mxb = fmax3(mxb, s[BN - 2], s[BN - 1]);
         const float mx = fmaxf(fmaxf(mxa, mxb), fmaxf(mxc, mxd)) * sl2;
         // raise the running max only when it moved by more than the margin
         const bool raise = mx > m + lazy;
