@@ -371,7 +371,9 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
   p.timeout_ns = g_timeout_ns;
   p.err = dev->err;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode_f16(d, mq, mk, mv, p, dtype == ATTN_BF16, dev->sm_count, st);
+  cudaError_t e = decode_kt_supported(d, H / Hkv)
+                      ? launch_decode_kt(H / Hkv, mk, mv, q, p, dtype == ATTN_BF16, st)
+                      : launch_decode_f16(d, mq, mk, mv, p, dtype == ATTN_BF16, dev->sm_count, st);
   if (e != cudaSuccess) return cuda_fail(e, "attn_decode launch");
   e = launch_combine(o_parts, lse_parts, o, lse, num_splits, B * H, d, dtype == ATTN_BF16, st);
   if (e != cudaSuccess) return cuda_fail(e, "attn_decode combine launch");

@@ -48,12 +48,6 @@ struct BwdBars {
   int abort;
 };
 
-// kind::f16 instruction descriptor with either operand MN-major.
-__host__ __device__ constexpr uint32_t idesc_f16_ab(int M, int N, bool bf16, bool a_mn, bool b_mn) {
-  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn ? 1u : 0u) << 15) |
-         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
 struct BwdUnit {
   int b, hkv, j, i0, nI, nblk, rot;
 };
@@ -174,9 +168,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_kk = idesc_f16_ab(128, 128, BF16, false, false);   // S, dP
-      constexpr uint32_t id_mm = idesc_f16_ab(128, D, BF16, true, true);       // dV, dK
-      constexpr uint32_t id_km = idesc_f16_ab(128, D, BF16, false, true);      // dQ
+      constexpr uint32_t id_kk = idesc_kind_f16_ab(128, 128, BF16, false, false);   // S, dP
+      constexpr uint32_t id_mm = idesc_kind_f16_ab(128, D, BF16, true, true);       // dV, dK
+      constexpr uint32_t id_km = idesc_kind_f16_ab(128, D, BF16, false, true);      // dQ
       const uint32_t sk = smem_u32(smem + T::OFF_K), sv = smem_u32(smem + T::OFF_V);
       const uint32_t sq = smem_u32(smem + T::OFF_Q), sdo = smem_u32(smem + T::OFF_DO);
       const uint32_t sp = smem_u32(smem + T::OFF_P), sds = smem_u32(smem + T::OFF_DS);

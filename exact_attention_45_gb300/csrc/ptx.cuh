@@ -178,6 +178,10 @@ __host__ __device__ constexpr uint32_t idesc_kind_f16(int M, int N, bool bf16, b
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// Same with the A operand's majorness too (bit 15: A MN-major).
+__host__ __device__ constexpr uint32_t idesc_kind_f16_ab(int M, int N, bool bf16, bool a_mn_major, bool b_mn_major) {
+  return idesc_kind_f16(M, N, bf16, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
+}
 // Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0),
 // f32 accumulate, both K-major.
 __host__ __device__ constexpr uint32_t idesc_kind_f8_e4m3(int M, int N) {
@@ -246,6 +250,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 #undef ATTN45_R8
+
+// TMEM -> registers, 32 lanes x 16 columns, waiting inside the asm statement.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
 
 // TMEM -> registers, 32 lanes x 64 columns, one wait for the whole load.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {

@@ -198,9 +198,14 @@ ATTN45_API int attn_fwd_fp8_varlen(const void* q8, const void* k8, const void* v
  *   lse [B, H] fp32 (natural log, scale included).
  *   The cache of every sequence is cut into num_splits ranges of
  *   ceil(Nmax / num_splits) keys rounded up to 128; each (sequence, KV head,
- *   range) is one unit of the forward kernel, which writes a partial O (fp32,
- *   normalised by its own sum) and its lse into `workspace`; a second kernel
- *   merges the partials. num_splits <= 0 picks attn_decode_num_splits().
+ *   range) is one unit, which writes a partial O (fp32, normalised by its own
+ *   sum) and its lse into `workspace`; a second kernel merges the partials.
+ *   With d = 128 and H/Hkv <= 16 a unit is one CTA that puts the keys on the
+ *   tensor core's 128 rows (S^T = K Q^T, O^T += V^T P^T) and clears the V rows
+ *   at or past seqlens[b], so those rows may hold anything; otherwise units
+ *   run in the forward kernel with the query heads as rows, where such rows
+ *   meet P = 0 in the product and must be finite.
+ *   num_splits <= 0 picks attn_decode_num_splits().
  *   workspace: DEVICE, 256-byte aligned, >= attn_decode_workspace_size(B, H,
  *   d, num_splits) bytes, owned by the caller; its contents are scratch.
  */

@@ -67,6 +67,35 @@ def test_decode_gqa_long_cache_full_size():
     assert_close(o, o_ref, lse, l_ref, what="decode GQA 32k")
 
 
+@pytest.mark.parametrize("H,Hkv", [(2, 2), (8, 4), (16, 2), (24, 2), (32, 2), (64, 2)])
+def test_decode_query_groups(H, Hkv):
+    # groups of 1, 2, 8, 12 and 16 query heads per KV head (keys-as-rows
+    # units) and 32 (units with the query heads as rows), over several splits
+    B, nmax = 3, 700
+    seqlens = [700, 1, 385]
+    q, k, v = _inputs(B, H, Hkv, nmax, 128, seed=H * 10 + Hkv)
+    o, lse = _run(q, k, v, seqlens, 3)
+    o_ref, l_ref = O.attention_decode(q, k, v, seqlens)
+    assert_close(o, o_ref, lse, l_ref, what=f"decode group {H // Hkv}")
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (8, 2), (48, 4)])
+def test_decode_ignores_cache_rows_past_length(H, Hkv):
+    # head dim 128 with at most 16 query heads per KV head: rows at or past a
+    # sequence's length are cleared, so NaN there must not reach O
+    B, nmax = 2, 512
+    seqlens = [200, 333]
+    q, k, v = _inputs(B, H, Hkv, nmax, 128, seed=31 + H)
+    kn, vn = k.clone(), v.clone()
+    for b, n in enumerate(seqlens):
+        kn[b, n:] = float("nan")
+        vn[b, n:] = float("nan")
+    o, lse = _run(q, kn, vn, seqlens, 2)
+    o_ref, l_ref = O.attention_decode(q, k, v, seqlens)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert_close(o, o_ref, lse, l_ref, what="decode with NaN past the length")
+
+
 def test_combine_matches_oracle():
     import exact_attention_45_gb300 as A
     rng = np.random.default_rng(5)
