@@ -33,6 +33,15 @@ WORKLOAD = {"workload": "attn_fwd bf16 non-causal d128", "B": 4, "N": 4096, "H":
             "causal": False, "dtype": "bf16", "inputs": "N(0,1) seed 0"}
 METRIC = "attention fwd TFLOP/s (4BHN^2d, 1/2 causal)"
 L2_FLUSH_BYTES = 512 << 20
+L2_NOTE = "flushed between timed iterations (512 MiB written, then read back so no dirty line is written back inside the timed region)"
+
+
+def l2_flush(buf) -> None:
+    """Evicts the L2 before a timed call: writes a buffer larger than the L2
+    (129 MB) and reads it back, so the dirty lines the write leaves go to HBM
+    here and not while the timed kernel streams its own inputs."""
+    buf.zero_()
+    buf.max()
 
 
 def flops_of(w) -> float:
@@ -235,7 +244,7 @@ def run_ours(args):
             raise A.AttnError(rc, lib.attn_last_error_message().decode())
 
     for _ in range(args.warmup):
-        flush.zero_()
+        l2_flush(flush)
         launch()
     torch.cuda.synchronize()
     if A.attn_get_device_error() != 0:
@@ -247,7 +256,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier()
         for i in range(args.steps):
-            flush.zero_()                      # L2 flushed between timed iterations
+            l2_flush(flush)                    # L2 flushed between timed iterations
             starts[i].record(stream)
             launch()
             ends[i].record(stream)
@@ -299,7 +308,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(t_max / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {**w, "global_batch": B * world, "seq_len": N, "parallelism": f"replicas{world}",
-                   "l2": "flushed between timed iterations (512 MiB write)"},
+                   "l2": L2_NOTE},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
                      "traffic": profiled_traffic("attn_fwd2_bf16_d128_n4096_noncausal.md", FWD_BF16_KERNEL_SOURCES),
@@ -347,11 +356,11 @@ def bwd_measure(steps: int, warmup: int, seed: int = 0):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     call = lambda: A.attn_bwd(q, k, v, o, lse, do, workspace=ws, dq=dq, dk=dk, dv=dv)
     for _ in range(warmup):
-        flush.zero_()
+        l2_flush(flush)
         call()
     ev = []
     for _ in range(steps):
-        flush.zero_()
+        l2_flush(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         call()
@@ -395,11 +404,11 @@ def fp8_varlen_measure(steps: int, warmup: int, seed: int = 0):
 
     def timed(fn):
         for _ in range(warmup):
-            flush.zero_()
+            l2_flush(flush)
             fn()
         ev = []
         for _ in range(steps):
-            flush.zero_()
+            l2_flush(flush)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             fn()
@@ -455,11 +464,11 @@ def decode_measure(steps: int, warmup: int, seed: int = 0, splits: int = 0):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     call = lambda: A.attn_decode(q, k, v, sl, num_splits=splits, workspace=ws, out=o, lse=lse)
     for _ in range(warmup):
-        flush.zero_()
+        l2_flush(flush)
         call()
     ev = []
     for _ in range(steps):
-        flush.zero_()
+        l2_flush(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         call()
@@ -503,11 +512,11 @@ def fp8_measure(steps: int, warmup: int, seed: int = 0):
 
     def timed(fn):
         for _ in range(warmup):
-            flush.zero_()
+            l2_flush(flush)
             fn()
         ts = []
         for _ in range(steps):
-            flush.zero_()
+            l2_flush(flush)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             fn()
@@ -562,7 +571,7 @@ def run_sweep(args):
             fn()
         ts = []
         for _ in range(reps):
-            flush.zero_()
+            l2_flush(flush)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             fn()

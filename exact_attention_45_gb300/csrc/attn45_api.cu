@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -300,10 +302,18 @@ int attn_decode_num_splits(int B, int Hkv, int Nmax) {
   return (int)(s < 1 ? 1 : s);
 }
 
+namespace {
+// Partial rows the decode workspace holds: num_splits + 1 rows per output row
+// (the balanced division leaves at most units + grid - 1 pieces, grid <=
+// num_splits * units).
+size_t decode_part_rows(int B, int H, int num_splits) { return (size_t)(num_splits + 1) * B * H; }
+size_t pad256(size_t x) { return (x + 255) & ~size_t(255); }
+}  // namespace
+
 size_t attn_decode_workspace_size(int B, int H, int d, int num_splits) {
   if (B < 1 || H < 1 || d < 1 || num_splits < 1) return 0;
-  const size_t rows = (size_t)num_splits * B * H;
-  return ((rows * d * 4 + 255) & ~size_t(255)) + ((rows * 4 + 255) & ~size_t(255));
+  const size_t rows = decode_part_rows(B, H, num_splits);
+  return pad256(rows * d * 4) + pad256(rows * 4) + pad256((size_t)B * H * 8);
 }
 
 int attn_combine(const float* o_parts, const float* lse_parts, void* o, float* lse, int num_splits, int rows, int d,
@@ -343,14 +353,44 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
   DeviceInfo* dev = nullptr;
   if ((rc = device_info(&dev))) return rc;
   const CUtensorMapDataType dt = dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const bool bf16 = dtype == ATTN_BF16;
+  const int group = H / Hkv;
   CUtensorMap mq, mk, mv;
-  // q [B][H][d] as rows of one "head": the query heads of a KV head are rows
-  if ((rc = make_map(&mq, dt, 2, q, d, 1, H, B, 64, BLOCK_M))) return rc;
   if ((rc = make_map(&mk, dt, 2, k_cache, d, Hkv, Nmax, B, 64, 128))) return rc;
   if ((rc = make_map(&mv, dt, 2, v_cache, d, Hkv, Nmax, B, 64, 128))) return rc;
-  const size_t rows = (size_t)num_splits * B * H;
+  const size_t part_rows = decode_part_rows(B, H, num_splits);
   float* o_parts = static_cast<float*>(workspace);
-  float* lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * d * 4 + 255) & ~size_t(255)));
+  float* lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) + pad256(part_rows * d * 4));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (decode_kt_supported(d, group)) {
+    // q [B*H][128] in boxes of 16 rows: the group's rows (and zero-weighted neighbours)
+    if ((rc = make_map(&mq, dt, 2, q, d, 1, (uint64_t)B * H, 1, 64, 16))) return rc;
+    static std::atomic<unsigned int> epoch{0};
+    DecodeParams p;
+    memset(&p, 0, sizeof(p));
+    p.o_parts = o_parts;
+    p.lse_parts = lse_parts;
+    p.counters = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(lse_parts) + pad256(part_rows * 4));
+    p.o = o;
+    p.lse = lse;
+    p.seqlens = seqlens;
+    p.B = B;
+    p.H = H;
+    p.Hkv = Hkv;
+    p.group = group;
+    p.Nmax = Nmax;
+    do p.epoch = ++epoch; while (p.epoch == 0);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.timeout_ns = g_timeout_ns;
+    p.err = dev->err;
+    const long long units = (long long)B * Hkv;
+    const int grid = (int)std::min<long long>(std::min(dev->sm_count, DECODE_KT_MAX_GRID), (long long)num_splits * units);
+    cudaError_t e = launch_decode_kt(mq, mk, mv, p, grid, bf16, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_decode launch");
+    return ATTN_OK;
+  }
+  // q [B][H][d] as rows of one "head": the query heads of a KV head are rows
+  if ((rc = make_map(&mq, dt, 2, q, d, 1, H, B, 64, BLOCK_M))) return rc;
   int chunk = (Nmax + num_splits - 1) / num_splits;
   chunk = (chunk + 127) / 128 * 128;
   FwdParams p;
@@ -362,7 +402,7 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
   p.total = B * Nmax;
   p.H = H;
   p.Hkv = Hkv;
-  p.group = H / Hkv;
+  p.group = group;
   p.ntiles = B * Hkv * num_splits;
   p.seqlens = seqlens;
   p.num_splits = num_splits;
@@ -370,12 +410,9 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
   p.err = dev->err;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = decode_kt_supported(d, H / Hkv)
-                      ? launch_decode_kt(H / Hkv, mk, mv, q, p, dtype == ATTN_BF16, st)
-                      : launch_decode_f16(d, mq, mk, mv, p, dtype == ATTN_BF16, dev->sm_count, st);
+  cudaError_t e = launch_decode_f16(d, mq, mk, mv, p, bf16, dev->sm_count, st);
   if (e != cudaSuccess) return cuda_fail(e, "attn_decode launch");
-  e = launch_combine(o_parts, lse_parts, o, lse, num_splits, B * H, d, dtype == ATTN_BF16, st);
+  e = launch_combine(o_parts, lse_parts, o, lse, num_splits, B * H, d, bf16, st);
   if (e != cudaSuccess) return cuda_fail(e, "attn_decode combine launch");
   return ATTN_OK;
 }

@@ -196,18 +196,25 @@ ATTN45_API int attn_fwd_fp8_varlen(const void* q8, const void* k8, const void* v
  *   seqlens: DEVICE int32[B], keys cached per sequence (values are clamped to
  *   [0, Nmax]; 0 gives o = 0 and lse = -inf); o [B, H, d] in q's dtype;
  *   lse [B, H] fp32 (natural log, scale included).
- *   The cache of every sequence is cut into num_splits ranges of
- *   ceil(Nmax / num_splits) keys rounded up to 128; each (sequence, KV head,
- *   range) is one unit, which writes a partial O (fp32, normalised by its own
- *   sum) and its lse into `workspace`; a second kernel merges the partials.
- *   With d = 128 and H/Hkv <= 16 a unit is one CTA that puts the keys on the
- *   tensor core's 128 rows (S^T = K Q^T, O^T += V^T P^T) and clears the V rows
- *   at or past seqlens[b], so those rows may hold anything; otherwise units
- *   run in the forward kernel with the query heads as rows, where such rows
- *   meet P = 0 in the product and must be finite.
- *   num_splits <= 0 picks attn_decode_num_splits().
+ *   Head dim 128 with H/Hkv <= 16 (one kernel launch): the 128-key tiles of
+ *   all (sequence, KV head) pairs are divided evenly between min(SMs, 256,
+ *   num_splits * B * Hkv) persistent CTAs, whatever the length mix; each CTA
+ *   puts the keys on the tensor core's 128 rows (S^T = K Q^T,
+ *   O^T += V^T P^T) and clears the V rows at or past seqlens[b], so those
+ *   rows may hold anything. A pair held by one CTA is written directly;
+ *   otherwise each CTA leaves a partial result in `workspace` and the last
+ *   one to finish (a per-pair counter tagged with a per-call epoch) merges
+ *   them. Other shapes: the cache of every sequence is cut into num_splits
+ *   ranges of ceil(Nmax / num_splits) keys rounded up to 128, each (sequence,
+ *   KV head, range) a unit of the forward kernel with the query heads as
+ *   rows, where rows past seqlens[b] meet P = 0 in the product and must be
+ *   finite; a second kernel merges the partials. The merge is the
+ *   online-softmax rescaling: lse = m + ln sum_s e^(lse_s - m),
+ *   O = sum_s e^(lse_s - lse) O_s. num_splits <= 0 picks
+ *   attn_decode_num_splits().
  *   workspace: DEVICE, 256-byte aligned, >= attn_decode_workspace_size(B, H,
- *   d, num_splits) bytes, owned by the caller; its contents are scratch.
+ *   d, num_splits) bytes, owned by the caller, used by one call at a time;
+ *   its contents are scratch (no initialisation needed).
  */
 ATTN45_API int attn_decode(const void* q, const void* k_cache, const void* v_cache, const int* seqlens, void* o,
                            float* lse, void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int Nmax,
@@ -215,8 +222,9 @@ ATTN45_API int attn_decode(const void* q, const void* k_cache, const void* v_cac
 /* Splits attn_decode picks for num_splits <= 0: about four units per SM, at
  * most one split per 128 cached keys. */
 ATTN45_API int attn_decode_num_splits(int B, int Hkv, int Nmax);
-/* Bytes of attn_decode's workspace: fp32 partial O [splits][B][H][d] then
- * partial lse [splits][B][H], each padded to 256 bytes; 0 for bad sizes. */
+/* Bytes of attn_decode's workspace: fp32 partial O [(num_splits + 1) B H][d],
+ * partial lse [(num_splits + 1) B H], per-pair counters uint64 [B H], each
+ * padded to 256 bytes; 0 for bad sizes. */
 ATTN45_API size_t attn_decode_workspace_size(int B, int H, int d, int num_splits);
 /*
  * attn_combine -- merge results computed over disjoint key subsets:

@@ -96,6 +96,41 @@ def test_decode_ignores_cache_rows_past_length(H, Hkv):
     assert_close(o, o_ref, lse, l_ref, what="decode with NaN past the length")
 
 
+@pytest.mark.parametrize("splits", [1, 0])
+def test_decode_many_short_sequences(splits):
+    # 300 sequences (some empty) on one KV head each: more units than SMs, so
+    # a CTA's range crosses several units and leaves several partials
+    rng = np.random.default_rng(4)
+    B, H, Hkv, nmax = 300, 8, 1, 300
+    seqlens = rng.integers(0, nmax + 1, size=B)
+    seqlens[::37] = 0
+    q, k, v = _inputs(B, H, Hkv, nmax, 128, seed=41)
+    o, lse = _run(q, k, v, seqlens, splits)
+    o_ref, l_ref = O.attention_decode(q, k, v, seqlens)
+    empty = seqlens == 0
+    assert np.all(o[empty] == 0) and np.all(lse[empty] == -np.inf)
+    assert_close(o[~empty], o_ref[~empty], lse[~empty], l_ref[~empty], what="decode, 300 short sequences")
+
+
+def test_decode_dirty_workspace_reused():
+    # the per-pair merge counters carry a per-call epoch: a workspace full of
+    # arbitrary bytes needs no initialisation, and reusing it gives the same
+    # result bit for bit
+    import exact_attention_45_gb300 as A
+    B, H, Hkv, nmax, splits = 3, 8, 2, 2000, 2
+    seqlens = [2000, 700, 1500]
+    q, k, v = _inputs(B, H, Hkv, nmax, 128, seed=53)
+    ws = torch.full((A.attn_decode_workspace_size(B, H, 128, splits),), 0xFF, dtype=torch.uint8, device="cuda")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    sl = torch.as_tensor(seqlens, dtype=torch.int32).cuda()
+    outs = [A.attn_decode(qd, kd, vd, sl, num_splits=splits, workspace=ws) for _ in range(2)]
+    torch.cuda.synchronize()
+    assert A.attn_get_device_error() == 0
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    o_ref, l_ref = O.attention_decode(q, k, v, seqlens)
+    assert_close(outs[0][0].float().cpu().numpy(), o_ref, outs[0][1].cpu().numpy(), l_ref, what="decode, dirty workspace")
+
+
 def test_combine_matches_oracle():
     import exact_attention_45_gb300 as A
     rng = np.random.default_rng(5)
