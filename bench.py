@@ -51,6 +51,8 @@ def flops_of(w) -> float:
 
 FWD_BF16_KERNEL_SOURCES = ("attn_fwd2_kernel.cuh", "attn_common.cuh", "ptx.cuh", "fwd_launch.cuh", "attn_fwd_d128.cu",
                            "launchers.h")
+DECODE_KT_KERNEL_SOURCES = ("attn_decode_kt.cu", "attn_fwd2_kernel.cuh", "attn_common.cuh", "ptx.cuh", "fwd_launch.cuh",
+                            "launchers.h")
 
 
 def kernel_digest(files) -> str:
@@ -443,9 +445,11 @@ DECODE = {"workload": "split-KV decode bf16 d128", "B": 8, "H": 32, "Hkv": 8, "d
 def decode_measure(steps: int, warmup: int, seed: int = 0, splits: int = 0):
     """Split-KV decode (one query token per sequence and head over a KV cache)
     on the GQA shape of the varlen configuration: 8 sequences with cached
-    lengths uniform in [1k, 32k], H=32, Hkv=8, d=128, bf16. HBM-bound: the
-    algorithmic bytes are the cached K and V rows each sequence attends to,
-    plus q, o and lse. Timed with CUDA events, L2 flushed before each call."""
+    lengths uniform in [1k, 32k], H=32, Hkv=8, d=128, bf16. One launch per call
+    (cached-key tiles divided evenly between persistent CTAs, partials merged
+    in the kernel). HBM-bound: the algorithmic bytes are the cached K and V
+    rows each sequence attends to, plus q, o and lse. Timed with CUDA events,
+    L2 flushed before each call."""
     import torch
 
     import attn_inputs as gen
@@ -487,8 +491,9 @@ def decode_measure(steps: int, warmup: int, seed: int = 0, splits: int = 0):
         "tokens_per_s": round(B * H / t, 1),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(gbs / pk["hbm_gbs"], 4), "algorithmic_bytes": kv_bytes + io_bytes,
-                     "peak_source": f"{pk['source']} copy"},
-        "gpu_launches_per_step": 2,
+                     "peak_source": f"{pk['source']} copy", "kernel": f"decode_kt_kernel<{H // Hkv},bf16>",
+                     "traffic": profiled_traffic("attn_decode_bf16_d128_gqa32x8_32k.md", DECODE_KT_KERNEL_SOURCES)},
+        "gpu_launches_per_step": 1, "l2": L2_NOTE,
     }
 
 
