@@ -64,7 +64,10 @@ def kernel_digest(files) -> str:
     for f in files:
         with open(os.path.join(_b.CSRC, f), "rb") as fh:
             h.update(f.encode() + fh.read())
-    h.update(" ".join(_b.ARCH + _b.NVCC_FLAGS).encode())
+    # flags with paths made relative to the repository, so the digest is the
+    # same wherever the checkout lives
+    flags = [os.path.relpath(f, ROOT) if os.path.isabs(f) else f for f in _b.ARCH + _b.NVCC_FLAGS]
+    h.update(" ".join(flags).encode())
     return h.hexdigest()
 
 
