@@ -353,7 +353,7 @@ def attn_fp8_prepass_varlen(q, k, v, cu_seqlens, mode: str = "block", rotate: bo
     pre = {
         "q8": torch.empty((T, H, d), dtype=u8, device=dev),
         "k8": torch.empty((T, Hkv, d), dtype=u8, device=dev),
-        "vt8": torch.zeros((Hkv, d, 128 * tmax), dtype=u8, device=dev),
+        "vt8": torch.empty((Hkv, d, 128 * tmax), dtype=u8, device=dev),   # columns past the last block unused
         "sq": torch.empty((H, tmax) if blk else (1,), dtype=torch.float32, device=dev),
         "sk": torch.empty((Hkv, tmax) if blk else (1,), dtype=torch.float32, device=dev),
         "sv": torch.empty((nseq, Hkv, d) if blk else (1,), dtype=torch.float32, device=dev),

@@ -269,7 +269,15 @@ int attn_fp8_prepass_varlen(const void* q, const void* k, const void* v, const i
   a.tmax = tmax;
   a.cu = cu_seqlens;
   a.blk_off = blk_off;
-  cudaError_t e = launch_fp8_prepass_varlen(a, d, static_cast<cudaStream_t>(stream));
+  Prepass128Maps maps;
+  const Prepass128Maps* mp = nullptr;
+  if (d == 128 && total > 0) {
+    if ((rc = api_make_map(&maps.in_q, false, q, d, H, total, 1, 64, 128))) return rc;
+    if ((rc = api_make_map(&maps.in_k, false, k, d, Hkv, total, 1, 64, 128))) return rc;
+    if ((rc = api_make_map(&maps.in_v, false, v, d, Hkv, total, 1, 64, 128))) return rc;
+    mp = &maps;
+  }
+  cudaError_t e = launch_fp8_prepass_varlen(a, d, mp, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return api_cuda_fail(e, "attn_fp8_prepass_varlen launch");
   return ATTN_OK;
 }

@@ -298,6 +298,17 @@ __device__ void v_block(const PrepassArgs& a, size_t tok0, int nrows, int head, 
   }
 }
 
+// Packed sequences: the sequence holding global 128-row block gb (the last s
+// with blk_off[s] <= gb).
+__device__ __forceinline__ int varlen_seq(const PrepassArgs& a, int gb) {
+  int lo = 0, hi = a.nseq - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.blk_off + mid) <= gb) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 template <int E>
 __global__ void __launch_bounds__(THREADS) prepass_kernel(const PrepassArgs a, int phase, int block_offset) {
   constexpr int D = E * 32;
@@ -311,12 +322,7 @@ __global__ void __launch_bounds__(THREADS) prepass_kernel(const PrepassArgs a, i
     else { id -= a.Hkv * a.tmax; kind = 2; head = id / a.tmax; gb = id % a.tmax; }
     if (gb >= __ldg(a.blk_off + a.nseq)) return;
     if (kind < 2 && phase == 1 && a.block_mode) return;
-    int lo = 0, hi = a.nseq - 1;                        // last s with blk_off[s] <= gb
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(a.blk_off + mid) <= gb) lo = mid; else hi = mid - 1;
-    }
-    const int s = lo;
+    const int s = varlen_seq(a, gb);
     const int blk = gb - __ldg(a.blk_off + s);
     const size_t tok0 = (size_t)__ldg(a.cu + s);
     const int nrows = __ldg(a.cu + s + 1) - __ldg(a.cu + s);
@@ -408,13 +414,32 @@ __global__ void __launch_bounds__(256, 3) qk128_kernel(const __grid_constant__ C
   __shared__ int abort_flag;
   __shared__ float red[8];
   __shared__ uint32_t xmask[64];
-  const int nq = a.B * a.H * a.nblk;
+  // fixed length: [Q: B x H x nblk][K: B x Hkv x nblk]; packed sequences:
+  // [Q: H x tmax][K: Hkv x tmax] global blocks (those past the last exit)
+  const int nq = a.varlen ? a.H * a.tmax : a.B * a.H * a.nblk;
   int id = blockIdx.x;
   const bool is_q = id < nq;
   if (!is_q) id -= nq;
   const int Hx = is_q ? a.H : a.Hkv;
-  const int blk = id % a.nblk, bh = id / a.nblk;
-  const int b = bh / Hx, head = bh % Hx;
+  int b, head, row0, nvalid;                  // TMA batch, head; first row; rows of the sequence in the block
+  size_t sc_idx;
+  if (a.varlen) {
+    const int gb = id % a.tmax;
+    head = id / a.tmax;
+    if (gb >= __ldg(a.blk_off + a.nseq)) return;
+    const int sq_ = varlen_seq(a, gb);
+    row0 = __ldg(a.cu + sq_) + (gb - __ldg(a.blk_off + sq_)) * ROWS;
+    nvalid = min(ROWS, __ldg(a.cu + sq_ + 1) - row0);
+    b = 0;
+    sc_idx = (size_t)head * a.tmax + gb;
+  } else {
+    const int blk = id % a.nblk, bh = id / a.nblk;
+    b = bh / Hx;
+    head = bh % Hx;
+    row0 = blk * ROWS;
+    nvalid = min(ROWS, a.N - row0);
+    sc_idx = ((size_t)b * Hx + head) * a.nblk + blk;
+  }
   float* sc = is_q ? a.sq : a.sk;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int r = warp * 16 + (lane >> 1);      // row in the block
@@ -433,8 +458,8 @@ __global__ void __launch_bounds__(256, 3) qk128_kernel(const __grid_constant__ C
   if (t == 0) {
     const CUtensorMap* m = is_q ? &in_q : &in_k;
     mbar_expect_tx(&bar, 2 * 16384);
-    tma_load_4d(m, &bar, tile, 0, head, blk * ROWS, b);
-    tma_load_4d(m, &bar, tile + 16384, 64, head, blk * ROWS, b);
+    tma_load_4d(m, &bar, tile, 0, head, row0, b);
+    tma_load_4d(m, &bar, tile + 16384, 64, head, row0, b);
   }
   mbar_wait(&bar, 0, a.timeout_ns, &abort_flag, a.err);
   // element e (0..63 of this half) of row r: chunk `half`, piece e/8 swizzled by r%8
@@ -474,7 +499,7 @@ __global__ void __launch_bounds__(256, 3) qk128_kernel(const __grid_constant__ C
 #pragma unroll
     for (int i = 0; i < 64; i += 2) f2_unpack(f2_mul(f2_pack(x[i], x[i + 1]), c2), x[i], x[i + 1]);
   }
-  const bool valid = blk * ROWS + r < a.N;      // rows past N (zero filled) do not count
+  const bool valid = r < nvalid;                // rows past the sequence do not count
   float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
   if (valid) {
 #pragma unroll
@@ -498,7 +523,7 @@ __global__ void __launch_bounds__(256, 3) qk128_kernel(const __grid_constant__ C
   float s;
   if (a.block_mode) {
     s = scale_from_amax(amax);
-    if (t == 0) sc[((size_t)b * Hx + head) * a.nblk + blk] = s;
+    if (t == 0) sc[sc_idx] = s;
   } else if (phase == 0) {
     if (t == 0) atomicMax(reinterpret_cast<unsigned int*>(sc), __float_as_uint(amax));
     return;
@@ -520,6 +545,9 @@ __global__ void __launch_bounds__(256, 3) qk128_kernel(const __grid_constant__ C
 #pragma unroll
     for (int i = 0; i < 64; ++i) x[i] = __fdiv_rn(x[i], dv.s);
   }
+  // packed sequences: a block may end inside the next sequence's rows, so
+  // only this sequence's rows are stored, straight from registers
+  uint8_t* gdst = (is_q ? a.q8 : a.k8) + ((size_t)(row0 + r) * Hx + head) * 128 + half * 64;
   uint8_t* dst = codes + r * 128;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -527,13 +555,18 @@ __global__ void __launch_bounds__(256, 3) qk128_kernel(const __grid_constant__ C
     const uint4 w = make_uint4(e4m3x4(x[e], x[e + 1], x[e + 2], x[e + 3]), e4m3x4(x[e + 4], x[e + 5], x[e + 6], x[e + 7]),
                                e4m3x4(x[e + 8], x[e + 9], x[e + 10], x[e + 11]),
                                e4m3x4(x[e + 12], x[e + 13], x[e + 14], x[e + 15]));
-    const int piece = half * 4 + j;
-    *reinterpret_cast<uint4*>(dst + ((piece ^ (r & 7)) << 4)) = w;
+    if (a.varlen) {
+      if (valid) reinterpret_cast<uint4*>(gdst)[j] = w;
+    } else {
+      const int piece = half * 4 + j;
+      *reinterpret_cast<uint4*>(dst + ((piece ^ (r & 7)) << 4)) = w;
+    }
   }
+  if (a.varlen) return;
   fence_proxy_async_smem();
   __syncthreads();
   if (t == 0) {
-    tma_store_4d(is_q ? &out_q : &out_k, codes, 0, head, blk * ROWS, b);
+    tma_store_4d(is_q ? &out_q : &out_k, codes, 0, head, row0, b);
     tma_store_commit();
     tma_store_wait_all();
   }
@@ -551,8 +584,30 @@ __global__ void __launch_bounds__(128) v128_kernel(const __grid_constant__ CUten
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
   __shared__ float red[4];
-  const int blk = blockIdx.x % a.nblk, bh = blockIdx.x / a.nblk;
-  const int b = bh / a.Hkv, head = bh % a.Hkv;
+  // fixed length: B x Hkv x nblk blocks; packed sequences: Hkv x tmax global
+  // blocks (those past the last exit), V^T columns from 128 * gb
+  int b, head, row0, nvalid;
+  size_t sv_row, vt_row, vt_col;
+  if (a.varlen) {
+    const int gb = blockIdx.x % a.tmax;
+    head = blockIdx.x / a.tmax;
+    if (gb >= __ldg(a.blk_off + a.nseq)) return;
+    const int sq_ = varlen_seq(a, gb);
+    row0 = __ldg(a.cu + sq_) + (gb - __ldg(a.blk_off + sq_)) * ROWS;
+    nvalid = min(ROWS, __ldg(a.cu + sq_ + 1) - row0);
+    b = 0;
+    sv_row = ((size_t)sq_ * a.Hkv + head) * 128;
+    vt_row = (size_t)head * 128;
+    vt_col = (size_t)gb * ROWS;
+  } else {
+    const int blk = blockIdx.x % a.nblk, bh = blockIdx.x / a.nblk;
+    b = bh / a.Hkv;
+    head = bh % a.Hkv;
+    row0 = blk * ROWS;
+    nvalid = min(ROWS, a.N - row0);
+    sv_row = vt_row = ((size_t)b * a.Hkv + head) * 128;
+    vt_col = (size_t)blk * ROWS;
+  }
   const int c = threadIdx.x;
   if (c == 0) {
     mbar_init(&bar, 1);
@@ -562,15 +617,14 @@ __global__ void __launch_bounds__(128) v128_kernel(const __grid_constant__ CUten
   __syncthreads();
   if (c == 0) {
     mbar_expect_tx(&bar, 2 * 16384);
-    tma_load_4d(&in_v, &bar, tile, 0, head, blk * ROWS, b);
-    tma_load_4d(&in_v, &bar, tile + 16384, 64, head, blk * ROWS, b);
+    tma_load_4d(&in_v, &bar, tile, 0, head, row0, b);
+    tma_load_4d(&in_v, &bar, tile + 16384, 64, head, row0, b);
   }
   mbar_wait(&bar, 0, a.timeout_ns, &abort_flag, a.err);
   // channel c of row n: chunk c/64, 16-byte piece ((c%64)/8) ^ (n%8), element c%8
   const uint8_t* col = tile + (c >> 6) * 16384 + (c & 7) * 2;
   const int piece = (c & 63) >> 3;
-  const int nvalid = min(ROWS, a.N - blk * ROWS);
-  float* sv_c = a.block_mode ? a.sv + ((size_t)b * a.Hkv + head) * 128 + c : a.sv;
+  float* sv_c = a.block_mode ? a.sv + sv_row + c : a.sv;
   if (phase == 0) {
     float m0 = 0.f, m1 = 0.f;
 #pragma unroll 8
@@ -593,7 +647,7 @@ __global__ void __launch_bounds__(128) v128_kernel(const __grid_constant__ CUten
     return;
   }
   const Divider dv(scale_from_amax(__uint_as_float(*reinterpret_cast<volatile unsigned int*>(sv_c))));
-  uint4* dst = reinterpret_cast<uint4*>(a.vt8 + (((size_t)b * a.Hkv + head) * 128 + c) * a.ldv + (size_t)blk * ROWS);
+  uint4* dst = reinterpret_cast<uint4*>(a.vt8 + (vt_row + c) * a.ldv + vt_col);
 #pragma unroll
   for (int g = 0; g < 8; ++g) {             // 16 rows -> 16 codes -> one 16-byte store
     uint32_t w[4];
@@ -624,10 +678,10 @@ __global__ void finalize_kernel(float* sq, float* sk, float* sv, int nsv, int te
 
 }  // namespace
 
-// Packed sequences (a.varlen): block offsets, then the generic kernels over
-// H x tmax, Hkv x tmax and Hkv x tmax global blocks (those past the last
-// sequence exit at once).
-cudaError_t launch_fp8_prepass_varlen(const PrepassArgs& a, int d, cudaStream_t s) {
+// Packed sequences (a.varlen): block offsets, then the kernels over H x tmax,
+// Hkv x tmax and Hkv x tmax global blocks (those past the last sequence exit
+// at once): the head-dim-128 kernels when `maps` is given, else the generic.
+cudaError_t launch_fp8_prepass_varlen(const PrepassArgs& a, int d, const Prepass128Maps* maps, cudaStream_t s) {
   const size_t nsv = a.block_mode ? (size_t)a.nseq * a.Hkv * d : 1;
   cudaError_t e = cudaMemsetAsync(a.sv, 0, nsv * sizeof(float), s);
   if (e != cudaSuccess) return e;
@@ -640,7 +694,25 @@ cudaError_t launch_fp8_prepass_varlen(const PrepassArgs& a, int d, cudaStream_t 
   varlen_block_offsets_kernel<<<1, 1024, 0, s>>>(a.cu, a.nseq, a.blk_off);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int blocks = (a.H + 2 * a.Hkv) * a.tmax;
+  const bool fast = d == 128 && maps != nullptr;
+  if (fast) {
+    e = cudaFuncSetAttribute(qk128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QK128_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(v128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, V128_SMEM);
+    if (e != cudaSuccess) return e;
+  }
   for (int phase = 0; phase < 2; ++phase) {
+    if (fast) {
+      // codes leave by plain stores in this mode: the output maps are not used
+      if (phase == 0 || !a.block_mode) {
+        qk128_kernel<<<(a.H + a.Hkv) * a.tmax, 256, QK128_SMEM, s>>>(maps->in_q, maps->in_k, maps->in_q, maps->in_k,
+                                                                     a, phase);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      }
+      v128_kernel<<<a.Hkv * a.tmax, 128, V128_SMEM, s>>>(maps->in_v, a, phase);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      continue;
+    }
     switch (d) {
       case 64: prepass_kernel<2><<<blocks, THREADS, 0, s>>>(a, phase, 0); break;
       case 128: prepass_kernel<4><<<blocks, THREADS, 0, s>>>(a, phase, 0); break;

@@ -37,7 +37,9 @@ struct Prepass128Maps {
 // maps: required for the fast head-dim-128 path (nullptr selects the generic one).
 cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps* maps, int sm_count,
                                cudaStream_t s);
-// Packed sequences: block offsets, two passes of the generic kernels, finalise.
-cudaError_t launch_fp8_prepass_varlen(const PrepassArgs& a, int d, cudaStream_t s);
+// Packed sequences: block offsets, two passes, finalise. maps (head dim 128,
+// inputs only, over [total, heads, 128] with 64 x 128-row boxes): the fast
+// kernels; nullptr: the generic ones.
+cudaError_t launch_fp8_prepass_varlen(const PrepassArgs& a, int d, const Prepass128Maps* maps, cudaStream_t s);
 
 }  // namespace attn45

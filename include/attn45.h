@@ -166,11 +166,15 @@ ATTN45_API int attn_fwd_fp8_auto_noalloc(const void* q, const void* k, const voi
  * attn_fp8_prepass_varlen -- bf16 q [total,H,d], k, v [total,Hkv,d] ->
  *   q8 [total,H,d], k8 [total,Hkv,d] (e4m3 codes); vt8 [Hkv, d, 128*tmax]
  *   (V codes transposed, sequence s's keys from column 128*blk_off[s], the
- *   pad keys of its last block code 0); block mode: sq [H, tmax],
+ *   pad keys of its last block code 0; columns from 128*blk_off[nseq] on are
+ *   neither written nor read); block mode: sq [H, tmax],
  *   sk [Hkv, tmax] (sequence s's block b in column blk_off[s] + b),
  *   sv [nseq, Hkv, d]; tensor mode: sq, sk, sv one float each; blk_off:
  *   DEVICE int32 [nseq+1] written here, blk_off[s] = sum over s' < s of
  *   ceil(n_s'/128). d in {64, 128, 256}; cu_seqlens as in attn_fwd_varlen.
+ *   d = 128 runs the head-dim-128 kernels of attn_fp8_prepass (TMA loads of
+ *   128-row blocks starting at each sequence's rows, codes of the sequence's
+ *   own rows stored from registers); d = 64, 256 the generic kernels.
  * attn_fwd_fp8_varlen -- the FP8 forward over those outputs (d = 128):
  *   o [total, H, d] bf16, lse [H, total] fp32; causal masking per sequence.
  */
