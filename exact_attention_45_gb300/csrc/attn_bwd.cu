@@ -214,6 +214,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             umma_f16_ss(tmem + T::T_DK, sdesc_mnmajor_sw128(sds + k * 2048, T::CHUNK),
                         sdesc_mnmajor_sw128(sq + k * 2048, T::CHUNK), id_mm, (it > 0 || k > 0) ? 1u : 0u);
           }
+          // Q_i and dO_i are read by nothing after dK: the next block's copies
+          // may start while dQ is computed and staged
+          umma_commit(&bars->qdo_empty);
           // dQ_i = dS K_j: A = dS K-major (K = 128 keys), B = K_j MN-major (N = d)
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -222,7 +225,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         id_km, k > 0 ? 1u : 0u);
           }
           umma_commit(&bars->dq_full);
-          umma_commit(&bars->qdo_empty);
         }
         if (!ok) break;
         umma_commit(&bars->dkv_full);
