@@ -363,7 +363,7 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
   float* lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) + pad256(part_rows * d * 4));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (decode_kt_supported(d, group)) {
-    // q [B*H][128] in boxes of 16 rows: the group's rows (and zero-weighted neighbours)
+    // q [B*H][d] in boxes of 16 rows: the group's rows (and zero-weighted neighbours)
     if ((rc = make_map(&mq, dt, 2, q, d, 1, (uint64_t)B * H, 1, 64, 16))) return rc;
     static std::atomic<unsigned int> epoch{0};
     DecodeParams p;
@@ -385,7 +385,7 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
     p.err = dev->err;
     const long long units = (long long)B * Hkv;
     const int grid = (int)std::min<long long>(std::min(dev->sm_count, DECODE_KT_MAX_GRID), (long long)num_splits * units);
-    cudaError_t e = launch_decode_kt(mq, mk, mv, p, grid, bf16, st);
+    cudaError_t e = launch_decode_kt(mq, mk, mv, p, d, grid, bf16, st);
     if (e != cudaSuccess) return cuda_fail(e, "attn_decode launch");
     return ATTN_OK;
   }

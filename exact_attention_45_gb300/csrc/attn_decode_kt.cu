@@ -8,7 +8,7 @@
 //   S^T [128 keys x 16]  = K [128 x d] . Q^T            (A = K tile, K-major)
 //   O^T [d x 16]        += V^T [d x 128 keys] . P^T      (A = V tile, MN-major)
 // with K and V exactly as TMA stages them (64-channel boxes, 128-byte
-// swizzle).
+// swizzle), d = 64 or 128.
 //
 // Work division. Unit u = (sequence b, KV head) owns ceil(n_b / 128) tiles;
 // the tiles of all units, in unit order, are cut into `grid` equal contiguous
@@ -49,12 +49,21 @@ namespace {
 
 constexpr int KT_KEYS = 128;                       // keys per tile = TMEM lanes of S^T
 constexpr int KT_NQ = 16;                          // MMA N: the group's query heads, padded
-constexpr int KT_STAGES = 3;
 constexpr int KT_CHUNK = KT_KEYS * 128;            // 128 keys x 64 channels of 16 bits
-constexpr int KT_STAGE = 4 * KT_CHUNK;             // K (two channel halves), then V
-constexpr int KT_QBYTES = 2 * KT_NQ * 128;         // Q: 2 channel halves x 16 rows x 128 B
-constexpr int KT_OFF_Q = KT_STAGES * KT_STAGE;     // 2 Q buffers
-constexpr int KT_OFF_P = KT_OFF_Q + 2 * KT_QBYTES; // P: 2 buffers x 2 key chunks x 16 rows x 128 B
+constexpr int KT_MAX_STAGES = 6;
+
+// Head dim 64 or 128: a row is D/64 chunks of 64 channels; the ring holds
+// 192 KB either way (3 stages of 64 KB, or 6 of 32 KB).
+template <int D>
+struct KtCfg {
+  static constexpr int NCH = D / 64;
+  static constexpr int STAGES = D == 128 ? 3 : 6;
+  static constexpr int STAGE = 2 * NCH * KT_CHUNK;  // K chunks, then V chunks
+  static constexpr int QBYTES = NCH * KT_NQ * 128;  // Q: D/64 chunks x 16 rows x 128 B
+  static_assert(STAGES * STAGE == 3 * 4 * KT_CHUNK && STAGES <= KT_MAX_STAGES, "ring size");
+};
+constexpr int KT_OFF_Q = 3 * 4 * KT_CHUNK;         // 2 Q buffers of up to 4 KB
+constexpr int KT_OFF_P = KT_OFF_Q + 2 * 4096;      // P: 2 buffers x 2 key chunks x 16 rows x 128 B
 constexpr int KT_OFF_RED = KT_OFF_P + 2 * 4096;    // tile maxima [2][4][16], sums [4][16], flags
 constexpr int KT_OFF_LIST = KT_OFF_RED + 1024;    // CTAs holding pieces of the unit being merged
 constexpr int KT_OFF_BARS = KT_OFF_LIST + DECODE_KT_MAX_GRID * 4;
@@ -64,7 +73,7 @@ constexpr uint32_t KT_TMEM_COLS = 64;              // S^T buffers at columns 0 a
 constexpr uint32_t KT_COL_O = 32;
 
 struct KtBars {
-  uint64_t full[KT_STAGES], empty[KT_STAGES];
+  uint64_t full[KT_MAX_STAGES], empty[KT_MAX_STAGES];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], q_free[2], fin;
   long long start, end;                            // this CTA's tile range
   long long T;                                     // tiles of all units
@@ -112,7 +121,7 @@ __device__ __forceinline__ uint16_t to_bits(float x) {
 // [c T / grid, (c+1) T / grid), and the sequence holding its first tile, by a
 // scan over the sequences in chunks of 128 (threads 0-127). Sequences with no
 // cached key get o = 0 and lse = -inf here, sequence b from CTA b % grid.
-template <bool BF16>
+template <int D, bool BF16>
 __device__ void plan_range(const DecodeParams& p, KtBars* bars, int* wsum) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   int part = 0;
@@ -149,8 +158,8 @@ __device__ void plan_range(const DecodeParams& p, KtBars* bars, int* wsum) {
   }
   for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
     if (seq_len(p, b) > 0) continue;
-    uint16_t* o = static_cast<uint16_t*>(p.o) + (size_t)b * p.H * 128;
-    for (int i = t; i < p.H * 128; i += 128) o[i] = 0;
+    uint16_t* o = static_cast<uint16_t*>(p.o) + (size_t)b * p.H * D;
+    for (int i = t; i < p.H * D; i += 128) o[i] = 0;
     for (int h = t; h < p.H; h += 128) p.lse[(size_t)b * p.H + h] = -INFINITY;
   }
   if (t == 0) {
@@ -181,12 +190,13 @@ __device__ __forceinline__ unsigned int count_piece(unsigned long long* c, unsig
   return 0;
 }
 
-template <int G, bool BF16>
+template <int D, int G, bool BF16>
 __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                                   const __grid_constant__ CUtensorMap tmK,
                                                                   const __grid_constant__ CUtensorMap tmV,
                                                                   const DecodeParams p) {
   static_assert(G >= 1 && G <= KT_NQ, "query heads per KV head");
+  using C = KtCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   KtBars* bars = reinterpret_cast<KtBars*>(smem + KT_OFF_BARS);
@@ -194,13 +204,13 @@ __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_c
   float* red_l = red + 2 * 4 * 16;                                 // [4][16]
   int* flags = reinterpret_cast<int*>(red_l + 4 * 16);             // [2][4] per tile, [4] per piece
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < 4) plan_range<BF16>(p, bars, flags);
+  if (warp < 4) plan_range<D, BF16>(p, bars, flags);
   __syncthreads();
   const long long start = bars->start, end = bars->end;
   const int ntl = (int)(end - start);              // tiles of this CTA
   if (ntl <= 0) return;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < KT_STAGES; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
@@ -235,30 +245,29 @@ __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_c
     if (lane == 0) {
       int i = 0, k = -1;
       for (; i < ntl; ++i, pos.next(p)) {
-        const int st = i % KT_STAGES;
+        const int st = i % C::STAGES;
         const bool first = i == 0 || pos.j == 0;
         if (first) ++k;
-        if (i >= KT_STAGES && !mbar_wait(&bars->empty[st], ((i / KT_STAGES) + 1) & 1, tmo, &bars->abort_flag, p.err))
+        if (i >= C::STAGES && !mbar_wait(&bars->empty[st], ((i / C::STAGES) + 1) & 1, tmo, &bars->abort_flag, p.err))
           break;
         if (first && k >= 2 && !mbar_wait(&bars->q_free[k & 1], ((k - 2) >> 1) & 1, tmo, &bars->abort_flag, p.err))
           break;
-        uint8_t* base = smem + st * KT_STAGE;
+        uint8_t* base = smem + st * C::STAGE;
         const int row = pos.j * KT_KEYS;
-        mbar_expect_tx(&bars->full[st], KT_STAGE + (first ? KT_QBYTES : 0));
+        mbar_expect_tx(&bars->full[st], C::STAGE + (first ? C::QBYTES : 0));
         if (first) {
-          uint8_t* qb = smem + KT_OFF_Q + (k & 1) * KT_QBYTES;
+          uint8_t* qb = smem + KT_OFF_Q + (k & 1) * 4096;
           const int qrow = pos.b * p.H + pos.hkv * G;
-          tma_load_4d(&tmQ, &bars->full[st], qb, 0, 0, qrow, 0);
-          tma_load_4d(&tmQ, &bars->full[st], qb + KT_QBYTES / 2, 64, 0, qrow, 0);
+          for (int c = 0; c < C::NCH; ++c) tma_load_4d(&tmQ, &bars->full[st], qb + c * 2048, c * 64, 0, qrow, 0);
         }
-        tma_load_4d(&tmK, &bars->full[st], base, 0, pos.hkv, row, pos.b);
-        tma_load_4d(&tmK, &bars->full[st], base + KT_CHUNK, 64, pos.hkv, row, pos.b);
-        tma_load_4d(&tmV, &bars->full[st], base + 2 * KT_CHUNK, 0, pos.hkv, row, pos.b);
-        tma_load_4d(&tmV, &bars->full[st], base + 3 * KT_CHUNK, 64, pos.hkv, row, pos.b);
+        for (int c = 0; c < C::NCH; ++c) {
+          tma_load_4d(&tmK, &bars->full[st], base + c * KT_CHUNK, c * 64, pos.hkv, row, pos.b);
+          tma_load_4d(&tmV, &bars->full[st], base + (C::NCH + c) * KT_CHUNK, c * 64, pos.hkv, row, pos.b);
+        }
       }
       // every copy issued has landed before the CTA can exit (bounded)
-      for (int t = max(0, i - KT_STAGES); t < i; ++t)
-        mbar_wait_drain(&bars->full[t % KT_STAGES], (t / KT_STAGES) & 1, tmo, p.err);
+      for (int t = max(0, i - C::STAGES); t < i; ++t)
+        mbar_wait_drain(&bars->full[t % C::STAGES], (t / C::STAGES) & 1, tmo, p.err);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
@@ -276,20 +285,19 @@ __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_c
       while (np < ntl) {
         bool moved = false;
         if (ns < ntl) {
-          const int st = ns % KT_STAGES, sb = ns & 1;
-          if (mbar_try_wait(smem_u32(&bars->full[st]), (ns / KT_STAGES) & 1) &&
+          const int st = ns % C::STAGES, sb = ns & 1;
+          if (mbar_try_wait(smem_u32(&bars->full[st]), (ns / C::STAGES) & 1) &&
               (ns < 2 || mbar_try_wait(smem_u32(&bars->s_free[sb]), ((ns - 2) >> 1) & 1))) {
             const bool first = ns == 0 || pos.j == 0;
             const bool last = ns == ntl - 1 || pos.j == pos.nt - 1;
             if (first) ++k;
             piece_first = first ? (piece_first | (1u << (ns & 31))) : (piece_first & ~(1u << (ns & 31)));
             tc_fence_after();
-            const uint32_t sk = smem_u32(smem + st * KT_STAGE), sqb = sq + (k & 1) * KT_QBYTES;
+            const uint32_t sk = smem_u32(smem + st * C::STAGE), sqb = sq + (k & 1) * 4096;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
+            for (int kk = 0; kk < D / 16; ++kk)
               umma_f16_ss(tmem + sb * KT_NQ, sdesc_kmajor_sw128(sk + (kk >> 2) * KT_CHUNK + (kk & 3) * 32),
-                          sdesc_kmajor_sw128(sqb + (kk >> 2) * (KT_QBYTES / 2) + (kk & 3) * 32), id_s,
-                          kk > 0 ? 1u : 0u);
+                          sdesc_kmajor_sw128(sqb + (kk >> 2) * 2048 + (kk & 3) * 32), id_s, kk > 0 ? 1u : 0u);
             umma_commit(&bars->s_full[sb]);
             if (last) umma_commit(&bars->q_free[k & 1]);
             pos.next(p);
@@ -298,10 +306,12 @@ __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_c
           }
         }
         if (np < ns && mbar_try_wait(smem_u32(&bars->p_full[np & 1]), (np >> 1) & 1)) {
-          const int pb = np & 1, st = np % KT_STAGES;
+          const int pb = np & 1, st = np % C::STAGES;
           const bool pf = (piece_first >> (np & 31)) & 1u;
           tc_fence_after();
-          const uint32_t sv = smem_u32(smem + st * KT_STAGE + 2 * KT_CHUNK);
+          // V^T as A with M = 128: for D = 64 its second 64 rows read the next
+          // 16 KB of shared memory (in bounds) into O^T rows that are never used
+          const uint32_t sv = smem_u32(smem + st * C::STAGE + C::NCH * KT_CHUNK);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma_f16_ss(tmem + KT_COL_O, sdesc_mnmajor_sw128(sv + kk * 2048, KT_CHUNK),
@@ -411,9 +421,11 @@ __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_c
         if (!valid) {
           // a key past the end meets P = 0, but 0 * (Inf or NaN) is not 0 in
           // the product: clear its V row (the tile has landed: S^T(i) read it)
-          uint4* vr = reinterpret_cast<uint4*>(smem + (i % KT_STAGES) * KT_STAGE + 2 * KT_CHUNK + key * 128);
+          uint4* vr = reinterpret_cast<uint4*>(smem + (i % C::STAGES) * C::STAGE + C::NCH * KT_CHUNK + key * 128);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) vr[c] = vr[c + KT_CHUNK / 16] = make_uint4(0u, 0u, 0u, 0u);
+          for (int c = 0; c < C::NCH; ++c)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) vr[c * (KT_CHUNK / 16) + u] = make_uint4(0u, 0u, 0u, 0u);
         }
         uint8_t* prow = smem + KT_OFF_P + sb * 4096 + (key >> 6) * 2048;
         const int kb = (key & 63) * 2;              // byte of this key within a 128-byte row
@@ -454,10 +466,10 @@ __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_c
 #pragma unroll
           for (int h = 0; h < G; ++h) l[h] = red_l[h] + red_l[16 + h] + red_l[32 + h] + red_l[48 + h];
           if (g0 >= start && g1 <= end) {
-            // the whole unit is here: final O and lse
+            // the whole unit is here: final O and lse (thread = channel)
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-              o_out[(orow0 + h) * 128 + key] = to_bits<BF16>(__uint_as_float(o[h]) / l[h]);
+              if (key < D) o_out[(orow0 + h) * D + key] = to_bits<BF16>(__uint_as_float(o[h]) / l[h]);
               if (key == h) p.lse[orow0 + h] = (m[h] + lg2_approx(l[h])) * 0.69314718055994530942f;
             }
           } else {
@@ -465,7 +477,7 @@ __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_c
             const size_t row0 = ((size_t)u + blockIdx.x) * G;   // slot u + c
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-              p.o_parts[(row0 + h) * 128 + key] = __uint_as_float(o[h]) / l[h];
+              if (key < D) p.o_parts[(row0 + h) * D + key] = __uint_as_float(o[h]) / l[h];
               if (key == h) p.lse_parts[row0 + h] = (m[h] + lg2_approx(l[h])) * 0.69314718055994530942f;
             }
             __threadfence();                        // the partial is visible before it is counted
@@ -485,7 +497,7 @@ __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_c
             }
             named_bar_sync(1, 128);
             const int n_merge = flags[12];
-            if (n_merge > 0) {
+            if (n_merge > 0 && key < D) {
               // last piece: merge all of them in one online pass over the
               // pieces (running maximum and rescaled sums, as in the softmax),
               // the loads of every head of a piece issued together
@@ -503,7 +515,7 @@ __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_c
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                   lv[h] = __ldcg(p.lse_parts + r0 + h);
-                  ov[h] = __ldcg(p.o_parts + (r0 + h) * 128 + key);
+                  ov[h] = __ldcg(p.o_parts + (r0 + h) * D + key);
                 }
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
@@ -516,7 +528,7 @@ __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_c
               }
 #pragma unroll
               for (int h = 0; h < G; ++h) {
-                o_out[(orow0 + h) * 128 + key] = to_bits<BF16>(acc[h] / ss[h]);
+                o_out[(orow0 + h) * D + key] = to_bits<BF16>(acc[h] / ss[h]);
                 if (key == h) p.lse[orow0 + h] = mm[h] + logf(ss[h]);
               }
             }
@@ -536,10 +548,10 @@ __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_c
   }
 }
 
-template <int G, bool BF16>
+template <int D, int G, bool BF16>
 cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const DecodeParams& p,
                      int grid, cudaStream_t s) {
-  auto kern = decode_kt_kernel<G, BF16>;
+  auto kern = decode_kt_kernel<D, G, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, KT_BYTES);
   if (e != cudaSuccess) return e;
   kern<<<grid, KT_THREADS, KT_BYTES, s>>>(q, k, v, p);
@@ -548,12 +560,14 @@ cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorM
 
 }  // namespace
 
-bool decode_kt_supported(int d, int group) { return d == 128 && group >= 1 && group <= KT_NQ; }
+bool decode_kt_supported(int d, int group) { return (d == 64 || d == 128) && group >= 1 && group <= KT_NQ; }
 
-cudaError_t launch_decode_kt(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                             const DecodeParams& p, int grid, bool bf16, cudaStream_t s) {
+namespace {
+template <int D>
+cudaError_t launch_d(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const DecodeParams& p,
+                     int grid, bool bf16, cudaStream_t s) {
 #define ATTN45_G(G) \
-  case G: return bf16 ? launch_t<G, true>(q, k, v, p, grid, s) : launch_t<G, false>(q, k, v, p, grid, s)
+  case G: return bf16 ? launch_t<D, G, true>(q, k, v, p, grid, s) : launch_t<D, G, false>(q, k, v, p, grid, s)
   switch (p.group) {
     ATTN45_G(1); ATTN45_G(2); ATTN45_G(3); ATTN45_G(4); ATTN45_G(5); ATTN45_G(6); ATTN45_G(7); ATTN45_G(8);
     ATTN45_G(9); ATTN45_G(10); ATTN45_G(11); ATTN45_G(12); ATTN45_G(13); ATTN45_G(14); ATTN45_G(15);
@@ -561,6 +575,12 @@ cudaError_t launch_decode_kt(const CUtensorMap& q, const CUtensorMap& k, const C
     default: return cudaErrorInvalidValue;
   }
 #undef ATTN45_G
+}
+}  // namespace
+
+cudaError_t launch_decode_kt(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                             const DecodeParams& p, int d, int grid, bool bf16, cudaStream_t s) {
+  return d == 64 ? launch_d<64>(q, k, v, p, grid, bf16, s) : launch_d<128>(q, k, v, p, grid, bf16, s);
 }
 
 }  // namespace attn45

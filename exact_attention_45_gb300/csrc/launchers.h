@@ -23,7 +23,7 @@ cudaError_t launch_fwd_f16_d128(const CUtensorMap& q, const CUtensorMap& k, cons
 // partial O [splits][B][H][d] to p.o and partial lse [splits][B][H] to p.lse.
 cudaError_t launch_decode_f16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                               const FwdParams& p, bool bf16, int sm_count, cudaStream_t s);
-// Decode with the keys on the TMEM lanes (head dim 128, group = H/Hkv <= 16).
+// Decode with the keys on the TMEM lanes (head dim 64/128, group = H/Hkv <= 16).
 // The tiles of all (sequence, KV head) units, in that order, are cut into
 // `grid` equal contiguous ranges, one per CTA. A CTA holding a whole unit
 // writes its O and lse; otherwise each run of a range inside unit u leaves a
@@ -32,10 +32,10 @@ cudaError_t launch_decode_f16(int d, const CUtensorMap& q, const CUtensorMap& k,
 // count merges them. Counters hold (epoch << 32) | pieces counted, so a new
 // epoch per call needs no reset.
 struct DecodeParams {
-  float* o_parts;                 // [slots * group][128]
+  float* o_parts;                 // [slots * group][d]
   float* lse_parts;               // [slots * group]
   unsigned long long* counters;   // [B * Hkv]
-  void* o;                        // [B, H, 128], bf16 / fp16
+  void* o;                        // [B, H, d], bf16 / fp16
   float* lse;                     // [B, H]
   const int* seqlens;             // [B], clamped to [0, Nmax]
   int B, H, Hkv, group, Nmax;
@@ -46,10 +46,10 @@ struct DecodeParams {
 };
 constexpr int DECODE_KT_MAX_GRID = 256;
 bool decode_kt_supported(int d, int group);
-// q: [B*H, 128] map with 64 x 16-row boxes; k, v: cache maps with 64 x 128-row
-// boxes; 1 <= grid <= DECODE_KT_MAX_GRID.
+// q: [B*H, d] map with 64 x 16-row boxes; k, v: cache maps with 64 x 128-row
+// boxes; d = 64 or 128; 1 <= grid <= DECODE_KT_MAX_GRID.
 cudaError_t launch_decode_kt(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                             const DecodeParams& p, int grid, bool bf16, cudaStream_t s);
+                             const DecodeParams& p, int d, int grid, bool bf16, cudaStream_t s);
 // Merge of per-split partials into O (bf16/fp16) and lse; splits with lse =
 // -inf are skipped without reading their O.
 cudaError_t launch_combine(const float* o_parts, const float* lse_parts, void* o, float* lse, int splits, int rows,

@@ -67,25 +67,27 @@ def test_decode_gqa_long_cache_full_size():
     assert_close(o, o_ref, lse, l_ref, what="decode GQA 32k")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("H,Hkv", [(2, 2), (8, 4), (16, 2), (24, 2), (32, 2), (64, 2)])
-def test_decode_query_groups(H, Hkv):
+def test_decode_query_groups(H, Hkv, d):
     # groups of 1, 2, 8, 12 and 16 query heads per KV head (keys-as-rows
     # units) and 32 (units with the query heads as rows), over several splits
     B, nmax = 3, 700
     seqlens = [700, 1, 385]
-    q, k, v = _inputs(B, H, Hkv, nmax, 128, seed=H * 10 + Hkv)
+    q, k, v = _inputs(B, H, Hkv, nmax, d, seed=H * 10 + Hkv + d)
     o, lse = _run(q, k, v, seqlens, 3)
     o_ref, l_ref = O.attention_decode(q, k, v, seqlens)
     assert_close(o, o_ref, lse, l_ref, what=f"decode group {H // Hkv}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("H,Hkv", [(4, 4), (8, 2), (48, 4)])
-def test_decode_ignores_cache_rows_past_length(H, Hkv):
-    # head dim 128 with at most 16 query heads per KV head: rows at or past a
-    # sequence's length are cleared, so NaN there must not reach O
+def test_decode_ignores_cache_rows_past_length(H, Hkv, d):
+    # at most 16 query heads per KV head: rows at or past a sequence's length
+    # are cleared, so NaN there must not reach O
     B, nmax = 2, 512
     seqlens = [200, 333]
-    q, k, v = _inputs(B, H, Hkv, nmax, 128, seed=31 + H)
+    q, k, v = _inputs(B, H, Hkv, nmax, d, seed=31 + H + d)
     kn, vn = k.clone(), v.clone()
     for b, n in enumerate(seqlens):
         kn[b, n:] = float("nan")
@@ -96,15 +98,15 @@ def test_decode_ignores_cache_rows_past_length(H, Hkv):
     assert_close(o, o_ref, lse, l_ref, what="decode with NaN past the length")
 
 
-@pytest.mark.parametrize("splits", [1, 0])
-def test_decode_many_short_sequences(splits):
+@pytest.mark.parametrize("d,splits", [(128, 1), (128, 0), (64, 0)])
+def test_decode_many_short_sequences(d, splits):
     # 300 sequences (some empty) on one KV head each: more units than SMs, so
     # a CTA's range crosses several units and leaves several partials
     rng = np.random.default_rng(4)
     B, H, Hkv, nmax = 300, 8, 1, 300
     seqlens = rng.integers(0, nmax + 1, size=B)
     seqlens[::37] = 0
-    q, k, v = _inputs(B, H, Hkv, nmax, 128, seed=41)
+    q, k, v = _inputs(B, H, Hkv, nmax, d, seed=41 + d)
     o, lse = _run(q, k, v, seqlens, splits)
     o_ref, l_ref = O.attention_decode(q, k, v, seqlens)
     empty = seqlens == 0
