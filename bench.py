@@ -64,9 +64,14 @@ def kernel_digest(files) -> str:
     for f in files:
         with open(os.path.join(_b.CSRC, f), "rb") as fh:
             h.update(f.encode() + fh.read())
-    # flags with paths made relative to the repository, so the digest is the
+    # flags without include paths (-I and its argument), so the digest is the
     # same wherever the checkout lives
-    flags = [os.path.relpath(f, ROOT) if os.path.isabs(f) else f for f in _b.ARCH + _b.NVCC_FLAGS]
+    flags, skip = [], False
+    for f in _b.ARCH + _b.NVCC_FLAGS:
+        if skip or f == "-I":
+            skip = f == "-I"
+            continue
+        flags.append(f)
     h.update(" ".join(flags).encode())
     return h.hexdigest()
 
@@ -317,6 +322,7 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
                      "traffic": profiled_traffic("attn_fwd2_bf16_d128_n4096_noncausal.md", FWD_BF16_KERNEL_SOURCES),
+                     "source_digest": kernel_digest(FWD_BF16_KERNEL_SOURCES)[:16],
                      "peak_source": f"{pk['source']} bf16 burst (cuBLAS)", "kernel": "attn_fwd2_kernel<128,128,2,false,false,BF16>"},
         "e2e": {"value": round(e2e_flops / e2e_max / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2,
@@ -494,8 +500,9 @@ def decode_measure(steps: int, warmup: int, seed: int = 0, splits: int = 0):
         "tokens_per_s": round(B * H / t, 1),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(gbs / pk["hbm_gbs"], 4), "algorithmic_bytes": kv_bytes + io_bytes,
-                     "peak_source": f"{pk['source']} copy", "kernel": f"decode_kt_kernel<{H // Hkv},bf16>",
-                     "traffic": profiled_traffic("attn_decode_bf16_d128_gqa32x8_32k.md", DECODE_KT_KERNEL_SOURCES)},
+                     "peak_source": f"{pk['source']} copy", "kernel": f"decode_kt_kernel<{d},{H // Hkv},bf16>",
+                     "traffic": profiled_traffic("attn_decode_bf16_d128_gqa32x8_32k.md", DECODE_KT_KERNEL_SOURCES),
+                     "source_digest": kernel_digest(DECODE_KT_KERNEL_SOURCES)[:16]},
         "gpu_launches_per_step": 1, "l2": L2_NOTE,
     }
 
