@@ -427,9 +427,9 @@ __global__ void __launch_bounds__(256, 3) qk128_kernel(const __grid_constant__ C
     const int gb = id % a.tmax;
     head = id / a.tmax;
     if (gb >= __ldg(a.blk_off + a.nseq)) return;
-    const int sq_ = varlen_seq(a, gb);
-    row0 = __ldg(a.cu + sq_) + (gb - __ldg(a.blk_off + sq_)) * ROWS;
-    nvalid = min(ROWS, __ldg(a.cu + sq_ + 1) - row0);
+    const int seq = varlen_seq(a, gb);
+    row0 = __ldg(a.cu + seq) + (gb - __ldg(a.blk_off + seq)) * ROWS;
+    nvalid = min(ROWS, __ldg(a.cu + seq + 1) - row0);
     b = 0;
     sc_idx = (size_t)head * a.tmax + gb;
   } else {
@@ -592,11 +592,11 @@ __global__ void __launch_bounds__(128) v128_kernel(const __grid_constant__ CUten
     const int gb = blockIdx.x % a.tmax;
     head = blockIdx.x / a.tmax;
     if (gb >= __ldg(a.blk_off + a.nseq)) return;
-    const int sq_ = varlen_seq(a, gb);
-    row0 = __ldg(a.cu + sq_) + (gb - __ldg(a.blk_off + sq_)) * ROWS;
-    nvalid = min(ROWS, __ldg(a.cu + sq_ + 1) - row0);
+    const int seq = varlen_seq(a, gb);
+    row0 = __ldg(a.cu + seq) + (gb - __ldg(a.blk_off + seq)) * ROWS;
+    nvalid = min(ROWS, __ldg(a.cu + seq + 1) - row0);
     b = 0;
-    sv_row = ((size_t)sq_ * a.Hkv + head) * 128;
+    sv_row = ((size_t)seq * a.Hkv + head) * 128;
     vt_row = (size_t)head * 128;
     vt_col = (size_t)gb * ROWS;
   } else {

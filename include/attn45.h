@@ -223,8 +223,10 @@ ATTN45_API int attn_fwd_fp8_varlen(const void* q8, const void* k8, const void* v
 ATTN45_API int attn_decode(const void* q, const void* k_cache, const void* v_cache, const int* seqlens, void* o,
                            float* lse, void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int Nmax,
                            int d, int num_splits, float scale, int dtype, void* stream);
-/* Splits attn_decode picks for num_splits <= 0: about four units per SM, at
- * most one split per 128 cached keys. */
+/* Splits attn_decode picks for num_splits <= 0: about four (sequence, KV
+ * head, range) units per SM, at most one split per 128 cached keys. With the
+ * persistent keys-as-rows kernel the value only bounds its grid
+ * (min(SMs, 256, num_splits * B * Hkv)) and the workspace. */
 ATTN45_API int attn_decode_num_splits(int B, int Hkv, int Nmax);
 /* Bytes of attn_decode's workspace: fp32 partial O [(num_splits + 1) B H][d],
  * partial lse [(num_splits + 1) B H], per-pair counters uint64 [B H], each
