@@ -618,6 +618,57 @@ def run_sweep(args):
                       "frac": round(fl / t / 1e12 / pk["bf16_tflops"], 4)}), flush=True)
 
 
+def run_sweep_fp8(args):
+    """FP8 forward over the FP8 benchmark set (one GPU): d=128, H=16,
+    N = 1024..16384 with B*N = 16384, outlier inputs, the four quantisation
+    variants (per-block or per-tensor scales, with or without the Hadamard
+    rotation), non-causal, and causal for per-block + rotation. Pre-pass and
+    forward timed separately (median of --sweep-reps, L2 flushed). One JSON
+    object per line on stdout."""
+    import torch
+
+    import attn_inputs as gen
+    import exact_attention_45_gb300 as A
+    torch.cuda.set_device(0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    pk = peaks()
+    fp8_peak = 2.0 * pk["bf16_tflops"]
+
+    def timeit(fn, reps):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            l2_flush(flush)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ts) / 1e3
+
+    H, d = 16, 128
+    variants = [("block", True, False), ("block", False, False), ("tensor", True, False), ("tensor", False, False),
+                ("block", True, True)]
+    for N in (1024, 2048, 4096, 8192, 16384):
+        B = 16384 // N
+        q, k, v = (t.cuda() for t in gen.qkv_fixed(B, N, H, H, d, seed=0, dist="outlier"))
+        o = torch.empty((B, N, H, d), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        for mode, rot, causal in variants:
+            pre = A.attn_fp8_prepass(q, k, v, mode=mode, rotate=rot)
+            t_pre = timeit(lambda: A.attn_fp8_prepass(q, k, v, mode=mode, rotate=rot), args.sweep_reps)
+            t_fwd = timeit(lambda: A.attn_fwd_fp8(pre, causal=causal, out=o, lse=lse), args.sweep_reps)
+            fl = 4.0 * B * H * N * N * d / (2 if causal else 1)
+            print(json.dumps({"d": d, "H": H, "N": N, "B": B, "mode": mode, "rotate": rot, "causal": causal,
+                              "prepass_ms": round(t_pre * 1e3, 4), "fwd_ms": round(t_fwd * 1e3, 4),
+                              "fwd_tflops": round(fl / t_fwd / 1e12, 1),
+                              "frac_of_2x_bf16": round(fl / t_fwd / 1e12 / fp8_peak, 4)}), flush=True)
+    if A.attn_get_device_error() != 0:
+        raise RuntimeError("device error in the FP8 sweep")
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -660,6 +711,7 @@ def main(argv=None):
     ap.add_argument("--workload", choices=("bf16", "fp8", "decode", "bwd"), default="bf16",
                     help="fp8 / decode: run only that path (e.g. for profiling)")
     ap.add_argument("--sweep", action="store_true", help="time every BF16 configuration instead")
+    ap.add_argument("--sweep-fp8", action="store_true", help="time the FP8 configurations and quantisation variants")
     ap.add_argument("--sweep-reps", type=int, default=20)
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)      # at least 3 untimed warm-up steps
@@ -677,6 +729,8 @@ def main(argv=None):
         print(json.dumps({"decode": decode_measure(args.steps, args.warmup, splits=args.decode_splits)}), flush=True)
     elif args.sweep:
         run_sweep(args)
+    elif args.sweep_fp8:
+        run_sweep_fp8(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
