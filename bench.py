@@ -51,8 +51,8 @@ def flops_of(w) -> float:
 
 FWD_BF16_KERNEL_SOURCES = ("attn_fwd2_kernel.cuh", "attn_common.cuh", "ptx.cuh", "fwd_launch.cuh", "attn_fwd_d128.cu",
                            "launchers.h")
-DECODE_KT_KERNEL_SOURCES = ("attn_decode_kt.cu", "attn_fwd2_kernel.cuh", "attn_common.cuh", "ptx.cuh", "fwd_launch.cuh",
-                            "launchers.h")
+DECODE_KT_KERNEL_SOURCES = ("attn_decode_kt.cuh", "attn_decode_kt.cu", "attn_fwd2_kernel.cuh", "attn_common.cuh",
+                            "ptx.cuh", "fwd_launch.cuh", "launchers.h")
 
 
 def kernel_digest(files) -> str:

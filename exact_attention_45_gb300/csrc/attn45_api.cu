@@ -363,8 +363,8 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
   float* lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) + pad256(part_rows * d * 4));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (decode_kt_supported(d, group)) {
-    // q [B*H][d] in boxes of 16 rows: the group's rows (and zero-weighted neighbours)
-    if ((rc = make_map(&mq, dt, 2, q, d, 1, (uint64_t)B * H, 1, 64, 16))) return rc;
+    // q [B*H][d] in boxes of 16 or 32 rows: the group's rows (and zero-weighted neighbours)
+    if ((rc = make_map(&mq, dt, 2, q, d, 1, (uint64_t)B * H, 1, 64, decode_kt_q_rows(group)))) return rc;
     static std::atomic<unsigned int> epoch{0};
     DecodeParams p;
     memset(&p, 0, sizeof(p));

@@ -23,7 +23,7 @@ cudaError_t launch_fwd_f16_d128(const CUtensorMap& q, const CUtensorMap& k, cons
 // partial O [splits][B][H][d] to p.o and partial lse [splits][B][H] to p.lse.
 cudaError_t launch_decode_f16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                               const FwdParams& p, bool bf16, int sm_count, cudaStream_t s);
-// Decode with the keys on the TMEM lanes (head dim 64/128, group = H/Hkv <= 16).
+// Decode with the keys on the TMEM lanes (head dim 64/128, group = H/Hkv <= 32).
 // The tiles of all (sequence, KV head) units, in that order, are cut into
 // `grid` equal contiguous ranges, one per CTA. A CTA holding a whole unit
 // writes its O and lse; otherwise each run of a range inside unit u leaves a
@@ -45,9 +45,12 @@ struct DecodeParams {
   unsigned int* err;
 };
 constexpr int DECODE_KT_MAX_GRID = 256;
+// Shapes the kernel takes: d = 64 or 128, group in 1..16, 24 or 32.
 bool decode_kt_supported(int d, int group);
-// q: [B*H, d] map with 64 x 16-row boxes; k, v: cache maps with 64 x 128-row
-// boxes; d = 64 or 128; 1 <= grid <= DECODE_KT_MAX_GRID.
+// Rows of the q map's boxes: the group's heads padded to the MMA's N (16 or 32).
+int decode_kt_q_rows(int group);
+// q: [B*H, d] map with 64 x decode_kt_q_rows(group)-row boxes; k, v: cache
+// maps with 64 x 128-row boxes; 1 <= grid <= DECODE_KT_MAX_GRID.
 cudaError_t launch_decode_kt(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                              const DecodeParams& p, int d, int grid, bool bf16, cudaStream_t s);
 // Merge of per-split partials into O (bf16/fp16) and lse; splits with lse =

@@ -200,7 +200,7 @@ ATTN45_API int attn_fwd_fp8_varlen(const void* q8, const void* k8, const void* v
  *   seqlens: DEVICE int32[B], keys cached per sequence (values are clamped to
  *   [0, Nmax]; 0 gives o = 0 and lse = -inf); o [B, H, d] in q's dtype;
  *   lse [B, H] fp32 (natural log, scale included).
- *   H/Hkv <= 16 (one kernel launch, head dim 64 or 128): the 128-key tiles of
+ *   H/Hkv in 1..16, 24 or 32 (one kernel launch, head dim 64 or 128): the 128-key tiles of
  *   all (sequence, KV head) pairs are divided evenly between min(SMs, 256,
  *   num_splits * B * Hkv) persistent CTAs, whatever the length mix; each CTA
  *   puts the keys on the tensor core's 128 rows (S^T = K Q^T,
@@ -208,7 +208,7 @@ ATTN45_API int attn_fwd_fp8_varlen(const void* q8, const void* k8, const void* v
  *   rows may hold anything. A pair held by one CTA is written directly;
  *   otherwise each CTA leaves a partial result in `workspace` and the last
  *   one to finish (a per-pair counter tagged with a per-call epoch) merges
- *   them. H/Hkv > 16: the cache of every sequence is cut into num_splits
+ *   them. Other groups: the cache of every sequence is cut into num_splits
  *   ranges of ceil(Nmax / num_splits) keys rounded up to 128, each (sequence,
  *   KV head, range) a unit of the forward kernel with the query heads as
  *   rows, where rows past seqlens[b] meet P = 0 in the product and must be

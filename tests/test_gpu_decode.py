@@ -68,10 +68,11 @@ def test_decode_gqa_long_cache_full_size():
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("H,Hkv", [(2, 2), (8, 4), (16, 2), (24, 2), (32, 2), (64, 2)])
+@pytest.mark.parametrize("H,Hkv", [(2, 2), (8, 4), (16, 2), (24, 2), (32, 2), (48, 2), (64, 2), (40, 2)])
 def test_decode_query_groups(H, Hkv, d):
-    # groups of 1, 2, 8, 12 and 16 query heads per KV head (keys-as-rows
-    # units) and 32 (units with the query heads as rows), over several splits
+    # groups of 1, 2, 8, 12, 16 (keys-as-rows kernel, N = 16), 24 and 32 (N =
+    # 32) query heads per KV head, and 20 (units with the query heads as
+    # rows), over several splits
     B, nmax = 3, 700
     seqlens = [700, 1, 385]
     q, k, v = _inputs(B, H, Hkv, nmax, d, seed=H * 10 + Hkv + d)
