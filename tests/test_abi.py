@@ -56,6 +56,51 @@ def test_host_checks_need_no_gpu(lib):
     assert lib.attn_set_wait_timeout_ns(2_000_000_000) == 0
 
 
+def _pad256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_workspace_sizes_and_block_bounds(lib):
+    # decode: fp32 partial O and lse for (splits + 1) rows per output row, then
+    # one 8-byte merge counter per (sequence, head)
+    B, H, d, S = 3, 8, 128, 4
+    rows = (S + 1) * B * H
+    assert lib.attn_decode_workspace_size(B, H, d, S) == _pad256(rows * d * 4) + _pad256(rows * 4) + _pad256(B * H * 8)
+    assert lib.attn_decode_workspace_size(0, H, d, S) == 0 and lib.attn_decode_workspace_size(B, H, d, 0) == 0
+    # backward: fp32 dQ accumulator and the row sums D
+    B, H, N = 2, 4, 300
+    r = B * N * H
+    assert lib.attn_bwd_workspace_size(B, H, N, 64) == _pad256(r * 64 * 4) + _pad256(r * 4)
+    assert lib.attn_bwd_workspace_size(B, H, 0, 64) == 0
+    # packed FP8: 128-row blocks over all sequences never exceed ceil(T/128) + nseq
+    assert lib.attn_fp8_varlen_tmax(0, 3) == 3
+    assert lib.attn_fp8_varlen_tmax(1000, 3) == 8 + 3
+    assert lib.attn_fp8_varlen_tmax(10, 0) == 0
+
+
+def test_host_checks_of_decode_backward_and_packed_fp8(lib):
+    # rejected before any CUDA call is made
+    args = [None] * 7 + [0]
+    rc = lib.attn_decode(*args, 1, 2, 1, 128, 256, 2, 0.1, 0, None)
+    assert rc == 2 and b"head dim" in lib.attn_last_error_message()
+    assert lib.attn_decode(*args, 1, 3, 2, 128, 128, 2, 0.1, 0, None) == 1      # H % Hkv != 0
+    assert lib.attn_decode(*args, 1, 256, 1, 128, 128, 2, 0.1, 0, None) == 2    # more than 128 heads per KV head
+    assert lib.attn_decode(*args, 0, 2, 1, 128, 128, 2, 0.1, 0, None) == 1      # B = 0
+    rc = lib.attn_decode(*args, 1, 2, 1, 128, 128, 2, 0.1, 0, None)
+    assert rc == 1 and b"null" in lib.attn_last_error_message()
+    assert lib.attn_combine(None, None, None, None, 0, 4, 64, 0, None) == 1     # no splits
+    assert lib.attn_combine(None, None, None, None, 2, 0, 64, 0, None) == 0     # no rows: nothing to do
+    bargs = [None] * 10 + [0]
+    assert lib.attn_bwd(*bargs, 1, 2, 2, 128, 256, 0, 0.1, 0, None) == 2          # head dim 256
+    assert lib.attn_bwd(*bargs, 1, 2, 2, 128, 64, 2, 0.1, 0, None) == 1           # causal must be 0 or 1
+    rc = lib.attn_bwd(*bargs, 1, 2, 2, 128, 64, 0, 0.1, 0, None)
+    assert rc == 1 and b"null" in lib.attn_last_error_message()
+    vargs = [None] * 11
+    assert lib.attn_fp8_prepass_varlen(*vargs, 0, 10, 2, 2, 128, 1, 1, 0, None) == 1   # no sequences
+    assert lib.attn_fp8_prepass_varlen(*vargs, 2, 10, 2, 2, 96, 1, 1, 0, None) == 2    # head dim 96
+    assert lib.attn_fp8_prepass_varlen(*vargs, 2, 10, 2, 2, 128, 7, 1, 0, None) == 1   # unknown mode
+
+
 def test_vt_ld(lib):
     assert lib.attn_fp8_vt_ld(1) == 128 and lib.attn_fp8_vt_ld(128) == 128 and lib.attn_fp8_vt_ld(129) == 256
 
