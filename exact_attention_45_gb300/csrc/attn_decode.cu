@@ -1,7 +1,8 @@
 // attn_decode.cu -- split-KV decode (one query token per sequence and query
 // head over a key/value cache) for the shapes the keys-as-rows kernel
-// (attn_decode_kt.cu: head dim 128, at most 16 query heads per KV head) does
-// not take, and the merge of per-split partial results.
+// (attn_decode_kt.cu: head dim 64 or 128 with 1-16, 24 or 32 query heads per
+// KV head, see decode_kt_supported) does not take, and the merge of per-split
+// partial results.
 //
 // Decode units run on the two-tile forward kernel: the H/Hkv query heads that
 // share one KV head form the rows of tile A (tile B stays empty) and stream

@@ -88,6 +88,18 @@ int check_shape(int B, int H, int Hkv, int N, int d, int mode) {
   return ATTN_OK;
 }
 
+// Checks of the forward step's own arguments, made by the combined calls
+// before the pre-pass runs, so a call that is bound to fail writes nothing.
+int check_fwd_fp8_args(int d, int causal, float scale, const void* o, const float* lse) {
+  if (d != 128) return api_fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward is built for head dim 128");
+  if (causal != 0 && causal != 1) return api_fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return api_fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (!o || !lse) return api_fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(o, 16) || !aligned(lse, 4))
+    return api_fail(ATTN_ERR_INVALID_ARG, "o must be 16-byte aligned, lse 4-byte aligned");
+  return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -202,6 +214,7 @@ int attn_fwd_fp8_auto(const void* q, const void* k, const void* v, void* o, floa
                       int mode, int rotate, uint64_t hadamard_seed, void* stream) {
   int rc = check_shape(B, H, Hkv, N, d, mode);
   if (rc) return rc;
+  if ((rc = check_fwd_fp8_args(d, causal, scale, o, lse))) return rc;
   const Fp8Layout L = fp8_layout(B, H, Hkv, N, d, mode);
   if (!workspace || !aligned(workspace, 256)) return api_fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if (workspace_bytes < L.total) return api_fail(ATTN_ERR_INVALID_ARG, "workspace smaller than attn_fp8_workspace_size()");
@@ -355,6 +368,8 @@ int attn_fwd_fp8_auto_noalloc(const void* q, const void* k, const void* v, void*
              need, kNoAllocScratchBytes);
     return api_fail(ATTN_ERR_INVALID_ARG, msg);
   }
+  // reject what the forward step would reject before the shared scratch is touched
+  if ((rc = check_fwd_fp8_args(d, causal, scale, o, lse))) return rc;
   void* scratch = nullptr;
   if ((rc = noalloc_scratch(&scratch))) return rc;
   return attn_fwd_fp8_auto(q, k, v, o, lse, scratch, kNoAllocScratchBytes, B, H, Hkv, N, d, causal, scale, mode,

@@ -117,8 +117,11 @@ ATTN45_API int attn_fp8_prepass(const void* q, const void* k, const void* v, voi
 /*
  * attn_fwd_fp8 -- forward on pre-pass outputs (same layouts as above).
  *   o [B,N,H,d] BF16 and lse [B,H,N] fp32 (of the scaled, dequantised scores).
- *   P is rounded to e4m3 after multiplication by 256 for the P*V product;
- *   the row normaliser uses the unrounded P. d must be 128 in this build.
+ *   Online softmax over 128-key blocks with a lazy running maximum m: m is
+ *   raised only when a block's maximum exceeds it by more than 8 (log2
+ *   units), so every p = 2^(t - m) is <= 2^8. p is rounded to e4m3 with no
+ *   extra multiplier (codes <= 256 < 448, never saturated) for the P*V
+ *   product; the row normaliser sums the unrounded p. d must be 128.
  */
 ATTN45_API int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* sq, const float* sk,
                  const float* sv, void* o, float* lse, int B, int H, int Hkv, int N, int d, int causal,
@@ -127,7 +130,9 @@ ATTN45_API int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, con
 /*
  * attn_fwd_fp8_auto -- pre-pass + FP8 forward in one call, with the
  * quantised tensors placed in a caller-provided device workspace of at least
- * attn_fp8_workspace_size() bytes (256-byte aligned).
+ * attn_fp8_workspace_size() bytes (256-byte aligned). Every argument the
+ * forward step checks (d = 128, causal, scale, o, lse) is checked before the
+ * pre-pass runs, so a rejected call writes nothing.
  */
 ATTN45_API size_t attn_fp8_workspace_size(int B, int H, int Hkv, int N, int d, int mode);
 ATTN45_API int attn_fwd_fp8_auto(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
@@ -153,6 +158,8 @@ ATTN45_API int attn_fwd_fp8_auto(const void* q, const void* k, const void* v, vo
  *   serialised by the caller. Parts that must start at zero are cleared by
  *   each call. Allocates nothing.
  */
+/*   Arguments are checked as in attn_fwd_fp8_auto before the scratch is
+ *   looked up or written. */
 ATTN45_API int attn_fwd_fp8_auto_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                                          int H, int Hkv, int N, int d, int causal, float scale, int mode, int rotate,
                                          uint64_t hadamard_seed, void* stream);

@@ -101,6 +101,21 @@ def test_host_checks_of_decode_backward_and_packed_fp8(lib):
     assert lib.attn_fp8_prepass_varlen(*vargs, 2, 10, 2, 2, 128, 7, 1, 0, None) == 1   # unknown mode
 
 
+def test_fp8_combined_calls_reject_forward_arguments_before_the_prepass(lib):
+    # the FP8 forward takes head dim 128 only: the combined calls say so before
+    # running the pre-pass (which accepts 64 and 256), so nothing is written;
+    # the pointers are never dereferenced, so None is enough here
+    for d in (64, 256):
+        rc = lib.attn_fwd_fp8_auto(None, None, None, None, None, None, 0, 1, 2, 2, 256, d, 0, 0.1, 1, 1, 0, None)
+        assert rc == 2 and b"head dim 128" in lib.attn_last_error_message()
+        rc = lib.attn_fwd_fp8_auto_noalloc(None, None, None, None, None, 1, 2, 2, 256, d, 0, 0.1, 1, 1, 0, None)
+        assert rc == 2 and b"head dim 128" in lib.attn_last_error_message()
+    rc = lib.attn_fwd_fp8_auto_noalloc(None, None, None, None, None, 1, 2, 2, 256, 128, 2, 0.1, 1, 1, 0, None)
+    assert rc == 1 and b"causal" in lib.attn_last_error_message()
+    rc = lib.attn_fwd_fp8_auto_noalloc(None, None, None, None, None, 1, 2, 2, 256, 128, 0, 0.1, 1, 1, 0, None)
+    assert rc == 1 and b"null" in lib.attn_last_error_message()
+
+
 def test_vt_ld(lib):
     assert lib.attn_fp8_vt_ld(1) == 128 and lib.attn_fp8_vt_ld(128) == 128 and lib.attn_fp8_vt_ld(129) == 256
 

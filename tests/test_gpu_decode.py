@@ -82,10 +82,11 @@ def test_decode_query_groups(H, Hkv, d):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("H,Hkv", [(4, 4), (8, 2), (48, 4)])
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (8, 2), (48, 4), (48, 2), (64, 2)])
 def test_decode_ignores_cache_rows_past_length(H, Hkv, d):
-    # at most 16 query heads per KV head: rows at or past a sequence's length
-    # are cleared, so NaN there must not reach O
+    # groups 1, 4 and 12 (keys-as-rows kernel with 16 columns), 24 and 32 (32
+    # columns): rows at or past a sequence's length are cleared, so NaN there
+    # must not reach O
     B, nmax = 2, 512
     seqlens = [200, 333]
     q, k, v = _inputs(B, H, Hkv, nmax, d, seed=31 + H + d)
@@ -99,15 +100,16 @@ def test_decode_ignores_cache_rows_past_length(H, Hkv, d):
     assert_close(o, o_ref, lse, l_ref, what="decode with NaN past the length")
 
 
-@pytest.mark.parametrize("d,splits", [(128, 1), (128, 0), (64, 0)])
-def test_decode_many_short_sequences(d, splits):
+@pytest.mark.parametrize("d,splits,H", [(128, 1, 8), (128, 0, 8), (64, 0, 8), (128, 0, 32), (64, 0, 24)])
+def test_decode_many_short_sequences(d, splits, H):
     # 300 sequences (some empty) on one KV head each: more units than SMs, so
-    # a CTA's range crosses several units and leaves several partials
+    # a CTA's range crosses several units and leaves several partials; groups
+    # of 8 (16-column kernel), 24 and 32 (32-column kernel)
     rng = np.random.default_rng(4)
-    B, H, Hkv, nmax = 300, 8, 1, 300
+    B, Hkv, nmax = 300, 1, 300
     seqlens = rng.integers(0, nmax + 1, size=B)
     seqlens[::37] = 0
-    q, k, v = _inputs(B, H, Hkv, nmax, d, seed=41 + d)
+    q, k, v = _inputs(B, H, Hkv, nmax, d, seed=41 + d + H)
     o, lse = _run(q, k, v, seqlens, splits)
     o_ref, l_ref = O.attention_decode(q, k, v, seqlens)
     empty = seqlens == 0

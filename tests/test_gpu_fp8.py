@@ -3,7 +3,9 @@
 * pre-pass (rotation + quantisation): bit-exact codes and scales against the
   oracle's statement of the same definition;
 * FP8 forward on those codes: against the oracle's fp64 emulation of the
-  method's steps (online softmax over 128-key blocks, P*256 rounded to e4m3);
+  method's steps (online softmax over 128-key blocks with a lazy running
+  maximum, margin 2^8; p = 2^(t - m) <= 2^8 rounded to e4m3 with multiplier 1
+  for P V; the normaliser from the unrounded p);
 * end to end on the outlier distribution: RMS error against exact fp64
   attention of the bf16 inputs <= 2.5e-2, and the rotated per-block path
   more accurate than the plain per-tensor path.
