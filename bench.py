@@ -199,7 +199,28 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle (CPU baseline)
-def cpu_oracle_rate(w, budget_s: float = 12.0, seed: int = 0):
+def cpu_model() -> str:
+    """The host CPU's model name (x86 /proc/cpuinfo, else lscpu, else the
+    machine type)."""
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine() or "unknown"
+
+
+def cpu_oracle_rate(w, budget_s: float = 12.0, seed: int = 0, threads: int | None = None):
     """Time the fp64 oracle on a seeded sample of rows of the workload; returns
     (TFLOP/s extrapolated to the metric's flop count, threads, sample text)."""
     import numpy as np
@@ -207,7 +228,7 @@ def cpu_oracle_rate(w, budget_s: float = 12.0, seed: int = 0):
     import attn_inputs as gen
     import oracle as O
     q, k, v = gen.qkv_fixed(w["B"], w["N"], w["H"], w["Hkv"], w["d"], seed=seed)
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     per_row = 4.0 * w["N"] * w["d"] * (0.5 if w["causal"] else 1.0)
     rows = 256
     t_used = 0.0
@@ -222,6 +243,16 @@ def cpu_oracle_rate(w, budget_s: float = 12.0, seed: int = 0):
     n = len(rs)
     rate = per_row * n / t_used / 1e12
     return rate, threads, f"{n} seeded (b,h,row) query rows of the workload, {t_used:.1f} s"
+
+
+def cpu_baseline(w, budget_s: float):
+    """The oracle timed on all host cores (the reported figure) and on one
+    thread, with the CPU model named."""
+    rate, threads, sample = cpu_oracle_rate(w, budget_s=budget_s)
+    rate1, _, sample1 = cpu_oracle_rate(w, budget_s=max(2.0, budget_s / 3), threads=1)
+    return {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample,
+            "cpu_model": cpu_model(),
+            "one_thread": {"value": round(rate1, 6), "unit": "TFLOP/s", "cores": 1, "sample": sample1}}
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -370,9 +401,7 @@ def run_ours(args):
     if rank == 0 and not args.no_fp8:
         line["fp8_varlen"] = fp8_varlen_measure(min(args.steps, 20), args.warmup)
     if rank == 0 and not args.no_cpu_baseline:
-        rate, threads, sample = cpu_oracle_rate(w, budget_s=args.cpu_budget)
-        line["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                                "sample": sample}
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1 and dist.is_initialized():
@@ -633,8 +662,12 @@ def run_sweep(args):
         lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
         t = timeit(lambda: A.attn_fwd(q, k, v, causal=causal, out=o, lse=lse), args.sweep_reps)
         fl = 4.0 * B * H * N * N * d / (2 if causal else 1)
+        # algorithmic HBM bytes: read Q, K, V once, write O and the lse
+        nbytes = B * N * (2 * H + 2 * H) * d * 2 + B * H * N * 4
         print(json.dumps({"d": d, "H": H, "N": N, "B": B, "causal": causal, "ms": round(t * 1e3, 4),
-                          "tflops": round(fl / t / 1e12, 1), "frac": round(fl / t / 1e12 / pk["bf16_tflops"], 4)}),
+                          "tflops": round(fl / t / 1e12, 1), "frac": round(fl / t / 1e12 / pk["bf16_tflops"], 4),
+                          "hbm_gbs": round(nbytes / t / 1e9, 1), "hbm_frac": round(nbytes / t / 1e9 / pk["hbm_gbs"], 4),
+                          "bytes": nbytes}),
               flush=True)
     lengths = gen.varlen_lengths(8, 1024, 32768, seed=0)
     q, k, v, cu = gen.qkv_varlen(lengths, 32, 8, 128, seed=0)
@@ -721,7 +754,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {**w, "global_batch": w["B"], "seq_len": w["N"], "parallelism": "cpu"},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": sample + " per step (extrapolated to the full workload's flops)"},
+                         "sample": sample + " per step (extrapolated to the full workload's flops)",
+                         "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -106,6 +106,16 @@ def test_invalid_arguments_raise():
         A.attn_fwd(q, k, v)
 
 
+# ---- every output element at a size where each persistent CTA walks several
+# work units (ring phases, TMEM reuse and the epilogue staging of later units):
+# 4 x 2048 tokens, hidden 2048 -> 512 units of 256 rows (d = 64, 128) or 1024
+# units of 128 rows (d = 256) over at most 152 CTAs
+@pytest.mark.parametrize("d,H", [(128, 16), (64, 32), (256, 8)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_multi_unit_per_cta_every_element(d, H, causal):
+    check_fixed_full(4, 2048, H, H, d, causal, seed=17 + d)
+
+
 # ---- full benchmark sizes: BF16 sweep (hidden 2048, B*N = 16384 tokens)
 SWEEP = [(d, H, N, causal) for d, H in ((64, 32), (128, 16)) for N in (512, 1024, 2048, 4096, 8192, 16384)
          for causal in (False, True)]

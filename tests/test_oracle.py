@@ -403,6 +403,105 @@ def test_fp8_emulation_lazy_maximum_raise_rescales():
     assert np.abs(lq - ref_l[0, 0]).max() <= 1e-5
 
 
+# ---------------------------------------------------------------- FP8 P quantisation, closed forms
+#
+# One query row against a few keys, built so that every quantity is exact:
+# per-tensor scales, no rotation, Q = 7 e_0 (scale 7/448 = 2^-6, code 448),
+# K = k_j e_0 plus one 14 in channel 1 of key 0 (scale 14/448 = 2^-5, codes
+# 32 k_j), V = 7 e_j (scale 2^-6, code 448). The dequantised score of key j is
+# 7 * k_j, so with softmax scale `sc` its base-2 exponent is t_j = 7 k_j sc /
+# ln 2. Expected values below are written out by hand from the e4m3 value set
+# of "FP8 Formats for Deep Learning" (Table 1: bias 7, 3 mantissa bits,
+# subnormal step 2^-9, round to nearest with ties to the even code) and from
+# the FP8 reading of the pages' block quantisation: online softmax with a lazy
+# running maximum that is raised only when a block maximum exceeds it by more
+# than 8 (log2 units), p = 2^(t - m) rounded to e4m3 with no multiplier for
+# P V, the normaliser l summing the unrounded p. Each plausible mistake in the
+# emulation (multiplier 256, l from the rounded p, margin 4 or a non-strict
+# comparison, P from the pre-raise maximum, no rescale of the accumulator)
+# changes at least one expected value here by far more than the tolerance.
+
+def _fp8_closed_form_problem(kvals, d=64):
+    n = len(kvals)
+    assert n <= d
+    q = torch.zeros(1, n, 1, d, dtype=torch.bfloat16)
+    q[0, 0, 0, 0] = 7.0
+    k = torch.zeros(1, n, 1, d, dtype=torch.bfloat16)
+    k[0, :, 0, 0] = torch.tensor([float(x) for x in kvals])
+    k[0, 0, 0, 1] = 14.0
+    v = torch.zeros(1, n, 1, d, dtype=torch.bfloat16)
+    for j in range(n):
+        v[0, j, 0, j] = 7.0
+    pre = O.fp8_prepass(q, k, v, mode="tensor", rotate=False)
+    # every scale a power of two and every code exact (dequantisation is lossless)
+    assert (pre["sq"][0], pre["sk"][0], pre["sv"][0]) == (2.0 ** -6, 2.0 ** -5, 2.0 ** -6)
+    tab = O.e4m3_table()
+    assert np.array_equal(tab[pre["k8"][0, :, 0, 0]] * 2.0 ** -5, np.array(kvals, dtype=np.float64))
+    assert tab[pre["q8"][0, 0, 0, 0]] == 448.0 and np.all(tab[pre["vt8"][0, 0, np.arange(n), np.arange(n)]] == 448.0)
+    return pre
+
+
+def _fp8_one_row(kvals, sc, block_n):
+    pre = _fp8_closed_form_problem(kvals)
+    o, lse = O.fp8_attention_emulated(pre, scale=sc, block_n=block_n, rows=([0], [0], [0]))
+    return o[0], float(lse[0])
+
+
+@pytest.mark.parametrize("p,rounded", [
+    (0.59375, 0.625),            # midpoint of 0.5625 (code 0x31) and 0.625 (0x32): ties to the even code
+    (0.53125, 0.5),              # midpoint of 0.5 (0x30) and 0.5625 (0x31): ties to the even code
+    (0.3, 0.3125),               # nearest of 0.28125 and 0.3125 (step 2^-5 in [0.25, 0.5))
+    (2.0 ** -10, 0.0),           # half the smallest subnormal 2^-9: ties to code 0
+    (1.5 * 2.0 ** -10, 2.0 ** -9),   # 0.75 of the subnormal step rounds up
+    (3.0 * 2.0 ** -10, 2.0 ** -8),   # midpoint of 2^-9 (code 1) and 2^-8 (code 2): even code
+])
+def test_fp8_emulation_p_rounding_closed_form(p, rounded):
+    # keys 0 and -1 in one block: t = (0, -s) with s = -log2(p) through the
+    # softmax scale sc = -ln(p)/7, so the row maximum is 0, p_0 = 1 and p_1 = p
+    o, lse = _fp8_one_row([0.0, -1.0], -math.log(p) / 7.0, block_n=128)
+    l = 1.0 + p                               # normaliser from the unrounded p
+    want = np.zeros(64)
+    want[0], want[1] = 7.0 / l, 7.0 * rounded / l
+    assert np.abs(o - want).max() <= 1e-12, (o[:2], want[:2])
+    assert abs(lse - math.log(l)) <= 1e-12
+
+
+def test_fp8_emulation_block_maximum_at_the_margin_keeps_m():
+    # single-key blocks with t = 0, 8, -2 (sc = ln2/7): the second block's
+    # maximum is exactly m + 8, which does not raise m (strict comparison), so
+    # p = 1, 256, 1/4, all e4m3 values (256 = code 0x78, not saturated)
+    o, lse = _fp8_one_row([0.0, 8.0, -2.0], math.log(2.0) / 7.0, block_n=1)
+    l = 1.0 + 256.0 + 0.25
+    want = np.zeros(64)
+    want[:3] = 7.0 * np.array([1.0, 256.0, 0.25]) / l
+    assert np.abs(o - want).max() <= 1e-12, o[:3]
+    assert abs(lse - math.log(l)) <= 1e-12
+
+
+def test_fp8_emulation_raise_past_the_margin_rescales():
+    # t = 0, 9, -2: 9 > 0 + 8 raises m to 9; the first key's contribution and
+    # l are rescaled by 2^-9, the second key gets p = 1, the third p = 2^-11,
+    # which rounds to e4m3 zero (below half the subnormal step) yet still
+    # counts in l
+    o, lse = _fp8_one_row([0.0, 9.0, -2.0], math.log(2.0) / 7.0, block_n=1)
+    l = 2.0 ** -9 + 1.0 + 2.0 ** -11
+    want = np.zeros(64)
+    want[0], want[1] = 7.0 * 2.0 ** -9 / l, 7.0 / l
+    assert np.abs(o - want).max() <= 1e-12, o[:3]
+    assert abs(lse - (9.0 * math.log(2.0) + math.log(l))) <= 1e-12
+
+
+def test_fp8_emulation_keys_in_one_block_share_the_block_maximum():
+    # the same keys as the margin case in one block: the block maximum 8 sets
+    # m (first block), so p = 2^-8, 1, 2^-10 and the last rounds to zero
+    o, lse = _fp8_one_row([0.0, 8.0, -2.0], math.log(2.0) / 7.0, block_n=128)
+    l = 2.0 ** -8 + 1.0 + 2.0 ** -10
+    want = np.zeros(64)
+    want[0], want[1] = 7.0 * 2.0 ** -8 / l, 7.0 / l
+    assert np.abs(o - want).max() <= 1e-12, o[:3]
+    assert abs(lse - (8.0 * math.log(2.0) + math.log(l))) <= 1e-12
+
+
 # ---------------------------------------------------------------- decode and split-KV combine
 
 def _decode_case(B=3, H=8, Hkv=2, nmax=700, d=64, seed=0):
