@@ -640,6 +640,9 @@ def run_sweep(args):
     cases = [(d, H, N, c) for d, H in ((64, 32), (128, 16)) for N in (512, 1024, 2048, 4096, 8192, 16384)
              for c in (False, True)]
     cases += [(256, 8, N, c) for N in (1024, 2048, 4096, 8192, 16384) for c in (False, True)]
+    if args.sweep_dims:
+        keep = {int(x) for x in args.sweep_dims.split(",")}
+        cases = [c for c in cases if c[0] in keep]
 
     def timeit(fn, reps):
         for _ in range(3):
@@ -669,6 +672,8 @@ def run_sweep(args):
                           "hbm_gbs": round(nbytes / t / 1e9, 1), "hbm_frac": round(nbytes / t / 1e9 / pk["hbm_gbs"], 4),
                           "bytes": nbytes}),
               flush=True)
+    if args.sweep_dims and 128 not in keep:
+        return
     lengths = gen.varlen_lengths(8, 1024, 32768, seed=0)
     q, k, v, cu = gen.qkv_varlen(lengths, 32, 8, 128, seed=0)
     q, k, v = q.cuda(), k.cuda(), v.cuda()
@@ -778,6 +783,7 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="time every BF16 configuration instead")
     ap.add_argument("--sweep-fp8", action="store_true", help="time the FP8 configurations and quantisation variants")
     ap.add_argument("--sweep-reps", type=int, default=20)
+    ap.add_argument("--sweep-dims", default="", help="comma-separated head dims the BF16 sweep keeps (default all)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)      # at least 3 untimed warm-up steps
     if args.workload == "fp8":

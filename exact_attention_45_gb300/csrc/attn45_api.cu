@@ -222,7 +222,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   CUtensorMap mq, mk, mv, mo;
   if ((rc = make_map(&mq, dt, 2, q, d, H, N, B, 64, BLOCK_M))) return rc;
   if ((rc = make_map(&mk, dt, 2, k, d, Hkv, N, B, 64, bn))) return rc;
-  if ((rc = make_map(&mv, dt, 2, v, d, Hkv, N, B, 64, bn))) return rc;
+  if ((rc = make_map(&mv, dt, 2, v, d, Hkv, N, B, 64, f16_v_box_rows(d)))) return rc;
   // output: 64 columns x 32 rows per bulk store (one warp's rows)
   if ((rc = make_map(&mo, dt, 2, o, d, H, N, B, 64, 32))) return rc;
   FwdParams p;
@@ -266,7 +266,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   CUtensorMap mq, mk, mv;
   if ((rc = make_map(&mq, dt, 2, q, d, H, total, 1, 64, BLOCK_M))) return rc;
   if ((rc = make_map(&mk, dt, 2, k, d, Hkv, total, 1, 64, bn))) return rc;
-  if ((rc = make_map(&mv, dt, 2, v, d, Hkv, total, 1, 64, bn))) return rc;
+  if ((rc = make_map(&mv, dt, 2, v, d, Hkv, total, 1, 64, f16_v_box_rows(d)))) return rc;
   FwdParams p;
   memset(&p, 0, sizeof(p));
   p.o = o;

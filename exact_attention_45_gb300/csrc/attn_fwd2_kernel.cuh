@@ -1,7 +1,11 @@
-// attn_fwd2_kernel.cuh -- BF16/FP16 forward, two 128-row query tiles per CTA.
+// attn_fwd2_kernel.cuh -- BF16/FP16 (and FP8) forward, two 128-row query tiles
+// per CTA (head dims 64 and 128).
 //
-// Same computation as attn_fwd_kernel.cuh, organised so the tensor core never
-// waits for a softmax: a CTA owns a 256-row "super tile" of one (sequence,
+// Fused exact attention forward, O = softmax(Q K^T * scale [+ causal mask]) V
+// with the per-row logsumexp, tiled over query rows and streamed over key
+// blocks so the N x N scores never leave the chip ("FlashAttention: Fast and
+// Memory-Efficient Exact Attention with IO-Awareness", abstract), organised so
+// the tensor core never waits for a softmax: a CTA owns a 256-row "super tile" of one (sequence,
 // head), split into tile A (rows 0-127) and tile B (rows 128-255), which share
 // every K/V block loaded into shared memory. Each tile has one TMEM S buffer
 // (P is written back over it) and one TMEM O accumulator. The MMA thread
@@ -28,10 +32,20 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include "attn_common.cuh"
-#include "attn_fwd_kernel.cuh"
 #include "ptx.cuh"
 
 namespace attn45 {
+
+// two floats -> one 32-bit word of bf16 or fp16 (round to nearest even)
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
+  if (bf16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
 
 constexpr int SUPER_M = 2 * BLOCK_M;          // query rows per CTA work unit
 // Raise m only past this margin (log2 units). P <= 2^8 then fits 16-bit P and

@@ -1,0 +1,436 @@
+// attn_fwd_pair_kernel.cuh -- BF16/FP16 forward for head dim 256 on pairs of
+// CTAs that share their tensor-core work (tcgen05 cta_group::2).
+//
+// Same computation as the other forward kernels (tiling so the scores never
+// reach HBM: "FlashAttention: Fast and Memory-Efficient Exact Attention with
+// IO-Awareness", abstract; online softmax with a running maximum and
+// normaliser: "Related papers: FlashAttention-4" page, online-softmax teaser).
+// The variant is the 2-CTA one the FlashAttention-3 page lists after its
+// Hopper kernel (reference list, appendix B.3 fragment, "3-Stage Pipelining"):
+// at head dim 256 a single CTA fits only 64-key blocks (Q, K and V tiles of
+// 256 columns fill its shared memory), and its N = 64 products keep the tensor
+// core waiting on the issuing thread. Two CTAs of a cluster own one 256-row
+// unit of one (sequence, head): the even CTA ("leader") rows 0-127, the odd
+// CTA rows 128-255. Each key block has 128 keys:
+//   S = Q K^T   one M = 256, N = 128 pair MMA per 16 channels: each CTA feeds
+//               its own 128 Q rows and 64 of the 128 keys (its K half);
+//   O += P V    one M = 256, N = 256 pair MMA per 16 keys: P from each CTA's
+//               TMEM, V's channels split 128 / 128 between the CTAs.
+// Per CTA, TMEM holds two S buffers (2 x 128 columns) and O (256 columns), so
+// S of block j+1 is computed while the softmax turns block j into P. Shared
+// memory per CTA: Q 64 KB + 2 ring slots x (K half 32 KB + V half 32 KB) +
+// output staging 16 KB.
+//
+// Roles per CTA (192 threads): warps 0-3 softmax / correction / epilogue of
+// this CTA's 128 rows (thread r owns row r = TMEM lane r); warp 4 TMA
+// producer; warp 5 allocates TMEM (both CTAs) and, in the leader, issues every
+// MMA of the pair. Barrier protocol:
+//   q_full, slot_full  (leader)  both CTAs' copies count their bytes on the
+//                      leader's barrier; only the leader posts the total;
+//   q_empty, slot_empty, s_full, o_done  (both)  multicast commits of the
+//                      leader's MMAs;
+//   p_full[2] (leader) one arrival per softmax warp of both CTAs (8) once
+//                      its P stores are complete, after the previous P V has
+//                      landed (so O is stable for the rare correction).
+// Every wait is bounded (timeout -> abort flag + device error word).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include "attn_common.cuh"
+#include "attn_fwd2_kernel.cuh"
+#include "ptx.cuh"
+
+namespace attn45 {
+
+template <int D>
+struct PairTraits {
+  static constexpr int BN = 128;                      // keys per block (over the pair)
+  static constexpr int NC = D / 64;                   // 128-byte chunks per Q / K row
+  static constexpr int Q_CHUNK = BLOCK_M * 128;       // 128 rows x 64 channels
+  static constexpr int Q_BYTES = BLOCK_M * D * 2;
+  static constexpr int K_ROWS = BN / 2;               // keys of a block held by one CTA
+  static constexpr int K_CHUNK = K_ROWS * 128;
+  static constexpr int K_BYTES = K_ROWS * D * 2;
+  static constexpr int V_COLS = D / 2;                // channels of V held by one CTA
+  static constexpr int V_NC = V_COLS / 64;
+  static constexpr int V_CHUNK = BN * 128;            // 128 keys x 64 channels, MN-major
+  static constexpr int V_BYTES = BN * V_COLS * 2;
+  static constexpr int SLOT_BYTES = K_BYTES + V_BYTES;
+  static constexpr int STAGES = 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_SLOT = Q_BYTES;
+  static constexpr int OFF_STAGE = OFF_SLOT + STAGES * SLOT_BYTES;  // 4 softmax warps x 4 KB
+  static constexpr int STAGE_BYTES = 4 * 4096;
+  static constexpr int OFF_BARS = OFF_STAGE + STAGE_BYTES;
+  static constexpr int BARS_BYTES = 256;
+  static constexpr int OFF_PREFIX = OFF_BARS + BARS_BYTES;
+  static constexpr int SMEM_FIXED = OFF_PREFIX + 1024;  // + 1024 for base alignment
+  static constexpr int TMEM_S = 0;                    // + 128 * buffer
+  static constexpr int TMEM_O = 2 * BN;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(2 * BN + D <= TMEM_COLS, "TMEM budget");
+  static_assert(D % 128 == 0, "V channels split in 64-channel chunks between the pair");
+};
+
+struct BarsPair {
+  uint64_t q_full, q_empty;
+  uint64_t slot_full[2], slot_empty[2];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_done;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(BarsPair) <= 256, "barrier block");
+
+template <int D, bool CAUSAL, bool VARLEN, bool BF16>
+__global__ void __launch_bounds__(192, 1)
+attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                     const FwdParams p) {
+  using T = PairTraits<D>;
+  constexpr int BN = T::BN;
+  constexpr bool STAGE_OUT = !VARLEN;
+  extern __shared__ uint8_t smem_raw[];
+  // the same offset in both CTAs: pair MMAs address both CTAs' operands by
+  // one shared-memory offset
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sQ = smem + T::OFF_Q;
+  uint8_t* sSlot = smem + T::OFF_SLOT;
+  BarsPair* bars = reinterpret_cast<BarsPair*>(smem + T::OFF_BARS);
+  int* prefix = reinterpret_cast<int*>(smem + T::OFF_PREFIX);
+  volatile int* abort_flag = &bars->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();            // 0 = leader (issues the MMAs)
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < T::STAGES; ++s) {
+      mbar_init(&bars->slot_full[s], 1);
+      mbar_init(&bars->slot_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->p_full[b], 8);
+    }
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc_pair(&bars->tmem_base, T::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    if (STAGE_OUT) tma_prefetch_desc(&tmO);
+  }
+  int ntiles = p.ntiles;
+  if constexpr (VARLEN) {
+    build_varlen_prefix2(p, prefix);                   // contains __syncthreads
+    ntiles = prefix[p.nseq];
+  }
+  // both CTAs' barriers are initialised and their TMEM allocated before any
+  // copy, arrival or MMA of the pair can touch them
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const uint64_t tmo = p.timeout_ns;
+  const int cluster_id = blockIdx.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+
+  auto get_tile = [&](int t) -> Tile2 {
+    if constexpr (VARLEN) return tile2_varlen(p, prefix, t);
+    else return tile2_fixed<CAUSAL>(p, t);
+  };
+  // key blocks the pair visits for a unit: those of its longer (later) tile
+  auto pair_blocks = [&](const Tile2& tl) -> int {
+    return max(tile2_blocks<CAUSAL, BN>(tl, 0), tile2_blocks<CAUSAL, BN>(tl, 1));
+  };
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      const uint32_t q_full_l = mapa_shared(&bars->q_full, 0);
+      uint32_t slot_full_l[T::STAGES];
+      for (int s = 0; s < T::STAGES; ++s) slot_full_l[s] = mapa_shared(&bars->slot_full[s], 0);
+      int slot_it = 0, tile_i = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < ntiles && ok; t += nclusters) {
+        const Tile2 tl = get_tile(t);
+        const int hk = tl.h / p.group;
+        const int nkv = pair_blocks(tl);
+        if (nkv == 0) continue;
+        ok = mbar_wait(&bars->q_empty, (tile_i & 1) ^ 1, tmo, abort_flag, p.err);
+        if (!ok) break;
+        ++tile_i;
+        if (leader) mbar_expect_tx(&bars->q_full, 2 * T::Q_BYTES);
+#pragma unroll
+        for (int c = 0; c < T::NC; ++c)
+          tma_load_4d_pair(&tmQ, q_full_l, sQ + c * T::Q_CHUNK, c * 64, tl.h,
+                           tl.tma_row0 + tl.sblk * SUPER_M + (int)rank * BLOCK_M, tl.tma_b);
+        // slot j: K_j (j < nkv; this CTA's 64 keys) and V_{j-1} (j >= 1; this
+        // CTA's 128 channels of all 128 keys)
+        for (int j = 0; j <= nkv; ++j, ++slot_it) {
+          const int st = slot_it % T::STAGES;
+          ok = mbar_wait(&bars->slot_empty[st], ((slot_it / T::STAGES) & 1) ^ 1, tmo, abort_flag, p.err);
+          if (!ok) break;
+          uint8_t* slot = sSlot + st * T::SLOT_BYTES;
+          if (leader)
+            mbar_expect_tx(&bars->slot_full[st], (j < nkv ? 2 * T::K_BYTES : 0) + (j >= 1 ? 2 * T::V_BYTES : 0));
+          if (j < nkv) {
+#pragma unroll
+            for (int c = 0; c < T::NC; ++c)
+              tma_load_4d_pair(&tmK, slot_full_l[st], slot + c * T::K_CHUNK, c * 64, hk,
+                               tl.tma_row0 + j * BN + (int)rank * T::K_ROWS, tl.tma_b);
+          }
+          if (j >= 1) {
+#pragma unroll
+            for (int c = 0; c < T::V_NC; ++c)
+              tma_load_4d_pair(&tmV, slot_full_l[st], slot + T::K_BYTES + c * T::V_CHUNK,
+                               (int)rank * T::V_COLS + c * 64, hk, tl.tma_row0 + (j - 1) * BN, tl.tma_b);
+          }
+        }
+      }
+      // the leader's barriers count both CTAs' copies: never leave with one in
+      // flight (already complete on the normal path)
+      if (leader) {
+        for (int it = (slot_it > T::STAGES ? slot_it - T::STAGES : 0); it < slot_it; ++it)
+          mbar_wait_drain(&bars->slot_full[it % T::STAGES], (it / T::STAGES) & 1, tmo, p.err);
+        if (tile_i > 0) mbar_wait_drain(&bars->q_full, (tile_i - 1) & 1, tmo, p.err);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    // Per slot j: S(j) = Q K_j^T into S buffer (j-th S overall) & 1, then
+    // O += P(j-1) V_{j-1} once both CTAs' P(j-1) is stored, so the tensor core
+    // computes the next scores while the softmax warps work.
+    if (leader && lane == 0) {
+      constexpr uint32_t idesc_s = idesc_kind_f16(2 * BLOCK_M, BN, BF16, false);
+      constexpr uint32_t idesc_o = idesc_kind_f16(2 * BLOCK_M, D, BF16, true);
+      constexpr uint16_t both = 3;
+      const uint32_t qa = smem_u32(sQ);
+      const uint32_t slot_a = smem_u32(sSlot);
+      int slot_it = 0, tile_i = 0, s_it = 0, pv_it = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < ntiles && ok; t += nclusters) {
+        const Tile2 tl = get_tile(t);
+        const int nkv = pair_blocks(tl);
+        if (nkv == 0) continue;
+        ok = mbar_wait(&bars->q_full, tile_i & 1, tmo, abort_flag, p.err);
+        ++tile_i;
+        if (!ok) break;
+        for (int j = 0; j <= nkv && ok; ++j, ++slot_it) {
+          const int st = slot_it % T::STAGES;
+          const uint32_t kb = slot_a + st * T::SLOT_BYTES;
+          const uint32_t vb = kb + T::K_BYTES;
+          ok = mbar_wait(&bars->slot_full[st], (slot_it / T::STAGES) & 1, tmo, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          if (j < nkv) {
+            const uint32_t s_tmem = tmem + T::TMEM_S + (s_it & 1) * BN;
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t qo = (k >> 2) * T::Q_CHUNK + (k & 3) * 32;
+              const uint32_t ko = (k >> 2) * T::K_CHUNK + (k & 3) * 32;
+              umma_f16_ss_pair(s_tmem, sdesc_kmajor_sw128(qa + qo), sdesc_kmajor_sw128(kb + ko), idesc_s,
+                               k > 0 ? 1u : 0u);
+            }
+            umma_commit_pair(&bars->s_full[s_it & 1], both);
+            ++s_it;
+          }
+          if (j >= 1) {
+            // P(j-1) lives in the S buffer of the pv_it-th S
+            ok = mbar_wait_cluster(&bars->p_full[pv_it & 1], (pv_it >> 1) & 1, tmo, abort_flag, p.err);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t a_tmem = tmem + T::TMEM_S + (pv_it & 1) * BN;
+#pragma unroll
+            for (int k = 0; k < BN / 16; ++k)
+              umma_f16_ts_pair(tmem + T::TMEM_O, a_tmem + k * 8, sdesc_mnmajor_sw128(vb + k * 2048, T::V_CHUNK),
+                               idesc_o, (j > 1 || k > 0) ? 1u : 0u);
+            umma_commit_pair(&bars->o_done, both);
+            ++pv_it;
+          }
+          umma_commit_pair(&bars->slot_empty[st], both);
+          if (j == nkv - 1) umma_commit_pair(&bars->q_empty, both);
+        }
+      }
+      umma_commit_pair(&bars->mma_done, 1);
+      mbar_wait_drain(&bars->mma_done, 0, tmo, p.err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------- softmax / correction / epilogue (both CTAs)
+    const int r = threadIdx.x;                         // row within this CTA's tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t to = tmem + lane_off + T::TMEM_O;
+    const uint32_t p_full_l[2] = {mapa_shared(&bars->p_full[0], 0), mapa_shared(&bars->p_full[1], 0)};
+    constexpr float lazy = LAZY_RESCALE_LOG2;
+    int s_cnt = 0, o_cnt = 0;
+    bool ok = true;
+    for (int t = cluster_id; t < ntiles && ok; t += nclusters) {
+      const Tile2 tl = get_tile(t);
+      const int nkv = pair_blocks(tl);
+      if (nkv == 0) continue;
+      const int row0 = tl.sblk * SUPER_M + (int)rank * BLOCK_M;   // first row of this CTA's tile
+      const int i_row = row0 + r;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nkv; ++j) {
+        const int sb = s_cnt & 1;
+        const float sl2 = p.scale_log2;
+        ok = mbar_wait(&bars->s_full[sb], (s_cnt >> 1) & 1, tmo, abort_flag, p.err);
+        ++s_cnt;
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t ts = tmem + lane_off + T::TMEM_S + sb * BN;
+        float s[BN];
+        {
+          uint32_t u[BN];
+          tmem_ld128(ts, u);
+#pragma unroll
+          for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(u[i]);
+        }
+        // keys past the sequence end, and (causal) keys after the row; blocks
+        // past this tile's diagonal (the pair runs its later tile's blocks)
+        // mask every key, which leaves m, l and O unchanged
+        const int col0 = j * BN;
+        if ((col0 + BN > tl.n) || (CAUSAL && col0 + BN - 1 > row0)) {
+          int limit = tl.n - col0;
+          if (CAUSAL) limit = min(limit, i_row - col0 + 1);
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c >= limit) s[c] = -INFINITY;
+        }
+        float mxa = fmax3(s[0], s[1], s[2]), mxb = fmax3(s[3], s[4], s[5]);
+        float mxc = fmax3(s[6], s[7], s[8]), mxd = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+        for (int c = 12; c < BN - 4; c += 8) {
+          mxa = fmax3(mxa, s[c], s[c + 1]);
+          mxb = fmax3(mxb, s[c + 2], s[c + 3]);
+          mxc = fmax3(mxc, s[c + 4], s[c + 5]);
+          mxd = fmax3(mxd, s[c + 6], s[c + 7]);
+        }
+        mxa = fmax3(mxa, s[BN - 4], s[BN - 3]);
+        mxb = fmax3(mxb, s[BN - 2], s[BN - 1]);
+        const float mx = fmaxf(fmaxf(mxa, mxb), fmaxf(mxc, mxd)) * sl2;
+        // the running maximum moves only past the lazy margin (2^8)
+        const bool raise = mx > m + lazy;
+        const float m_new = raise ? mx : m;
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = raise ? ex2_approx(m - m_use) : 1.f;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        const uint64_t negm2 = f2_pack(-m_use, -m_use);
+        uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+        uint32_t pk[BN / 2];
+#pragma unroll
+        for (int c = 0; c < BN; c += 4) {
+          float a0, a1, b0, b1;
+          f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, negm2), a0, a1);
+          f2_unpack(f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, negm2), b0, b1);
+          a0 = ex2_approx(a0);
+          a1 = ex2_approx(a1);
+          b0 = ex2_approx(b0);
+          b1 = ex2_approx(b1);
+          acc0 = f2_add(acc0, f2_pack(a0, a1));
+          acc1 = f2_add(acc1, f2_pack(b0, b1));
+          pk[c / 2] = pack2(a0, a1, BF16);
+          pk[c / 2 + 1] = pack2(b0, b1, BF16);
+          if (c == 60) tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        }
+        float sum0, sum1, sum2, sum3;
+        f2_unpack(acc0, sum0, sum1);
+        f2_unpack(acc1, sum2, sum3);
+        l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
+        m = m_new;
+        tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        tmem_st_wait();
+        if (j > 0) {
+          // O += P(j-1) V_{j-1} was issued after S(j): wait for it before the
+          // correction (and before P(j) may be consumed)
+          ok = mbar_wait(&bars->o_done, o_cnt & 1, tmo, abort_flag, p.err);
+          ++o_cnt;
+          if (!ok) break;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll 1
+            for (int c = 0; c < D / 64; ++c) {
+              uint32_t u[64];
+              tmem_ld64(to + c * 64, u);
+#pragma unroll
+              for (int i = 0; i < 64; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+              tmem_st32(to + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+              tmem_st32(to + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+            }
+            tmem_st_wait();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(p_full_l[sb]);
+      }
+      if (!ok) break;
+      ok = mbar_wait(&bars->o_done, o_cnt & 1, tmo, abort_flag, p.err);
+      ++o_cnt;
+      if (!ok) break;
+      tc_fence_after();
+      const bool valid = i_row < tl.nq;
+      const float inv_l = 1.f / l;
+      const size_t tok = (size_t)tl.tok0 + (size_t)(valid ? i_row : 0);
+      uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.o) + (tok * p.H + tl.h) * D);
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t u[64];
+        tmem_ld64(to + c * 64, u);
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          w[i] = pack2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l, BF16);
+        if constexpr (STAGE_OUT) {
+          // this warp's 32 rows x 64 columns, 128-byte swizzled, one bulk
+          // tensor store (rows past the sequence end are clipped by the copy)
+          const uint32_t stg = smem_u32(smem + T::OFF_STAGE + warp * 4096);
+          if (lane == 0) tma_store_wait_read();
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            st_shared_v4(stg + lane * 128 + ((i ^ (lane & 7)) << 4), w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(&tmO, smem + T::OFF_STAGE + warp * 4096, c * 64, tl.h, row0 + warp * 32, tl.tma_b);
+            tma_store_commit();
+          }
+        } else if (valid) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            orow[c * 8 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (valid) {
+        const float lse = (m + lg2_approx(l)) * 0.69314718055994530942f;
+        if constexpr (VARLEN) p.lse[(size_t)tl.h * p.total + tok] = lse;
+        else p.lse[((size_t)tl.seq * p.H + tl.h) * p.N + i_row] = lse;
+      }
+    }
+    if (STAGE_OUT && lane == 0) tma_store_wait_all();
+  }
+
+  // neither CTA leaves (or frees TMEM) while the pair's MMAs, copies or
+  // arrivals may still reach it
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc_pair(tmem, T::TMEM_COLS);
+}
+
+}  // namespace attn45

@@ -1,7 +1,7 @@
 // fwd_launch.cuh -- launch helpers for the BF16/FP16 forward instantiations.
 #pragma once
 #include "attn_fwd2_kernel.cuh"
-#include "attn_fwd_kernel.cuh"
+#include "attn_fwd_pair_kernel.cuh"
 #include "launchers.h"
 
 namespace attn45 {
@@ -17,22 +17,6 @@ inline int persistent_grid(const FwdParams& p, bool varlen, int rows_per_unit, i
     *ntiles = (int)units;
   }
   return (int)(units < sm_count ? units : sm_count);
-}
-
-// One 128-row query tile per CTA (used for head dim 256; O leaves through plain
-// stores, so it takes no output map).
-template <int D, int BN, int ST, bool CAUSAL, bool VARLEN, bool BF16>
-cudaError_t launch_f16_single(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, FwdParams p,
-                              int sm_count, cudaStream_t stream) {
-  static_assert(BN == f16_block_n(D), "tensor-map box height and kernel BN must agree");
-  using T = Bf16Traits<D, BN, ST>;
-  auto kern = attn_fwd_f16_kernel<D, BN, ST, CAUSAL, VARLEN, BF16>;
-  const int grid = persistent_grid(p, VARLEN, BLOCK_M, sm_count, &p.ntiles);
-  const int smem = T::SMEM_FIXED + (VARLEN ? 4 * (p.nseq + 1) : 0);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, 192, smem, stream>>>(q, k, v, p);
-  return cudaGetLastError();
 }
 
 // Two 128-row query tiles per CTA (head dims 64 and 128).
@@ -52,18 +36,50 @@ cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtens
   return cudaGetLastError();
 }
 
-template <int D, int BN, int ST, bool PAIR, bool CA, bool VL, bool BF>
-cudaError_t launch_f16_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
-                           const FwdParams& p, int sm_count, cudaStream_t s) {
-  if constexpr (PAIR) return launch_pair<D, BN, ST, CA, VL, BF ? KIND_BF16 : KIND_FP16>(q, k, v, o, p, sm_count, s);
-  else return launch_f16_single<D, BN, ST, CA, VL, BF>(q, k, v, p, sm_count, s);
+// CTA pairs (clusters of 2, head dim 256): persistent clusters, at most as
+// many as fit on the device at once (cudaOccupancyMaxActiveClusters, looked up
+// once per device and instantiation), each walking 256-row units.
+template <int D, bool CAUSAL, bool VARLEN, bool BF16>
+cudaError_t launch_cta_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
+                            FwdParams p, int sm_count, cudaStream_t stream) {
+  using T = PairTraits<D>;
+  auto kern = attn_fwd_pair_kernel<D, CAUSAL, VARLEN, BF16>;
+  const int smem = T::SMEM_FIXED + (VARLEN ? 4 * (p.nseq + 1) : 0);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  static int max_clusters[64] = {};     // 0 = not looked up yet
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_clusters[dev] == 0) {
+    int n = 0;
+    cfg.gridDim = dim3(2 * (sm_count / 2), 1, 1);
+    if ((e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg)) != cudaSuccess) return e;
+    if (n < 1) return cudaErrorLaunchOutOfResources;
+    max_clusters[dev] = n;
+  }
+  int clusters = persistent_grid(p, VARLEN, SUPER_M, max_clusters[dev], &p.ntiles);
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, p);
 }
 
-template <int D, int BN, int ST, bool PAIR>
+template <int D, int BN, int ST>
 cudaError_t launch_f16_dispatch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                 const CUtensorMap& o, const FwdParams& p, bool causal, bool varlen, bool bf16, int sm_count,
                                 cudaStream_t s) {
-#define ATTN45_L(CA, VL, BF) return launch_f16_one<D, BN, ST, PAIR, CA, VL, BF>(q, k, v, o, p, sm_count, s)
+#define ATTN45_L(CA, VL, BF) return launch_pair<D, BN, ST, CA, VL, BF ? KIND_BF16 : KIND_FP16>(q, k, v, o, p, sm_count, s)
   if (causal) {
     if (varlen) { if (bf16) ATTN45_L(true, true, true); else ATTN45_L(true, true, false); }
     else        { if (bf16) ATTN45_L(true, false, true); else ATTN45_L(true, false, false); }

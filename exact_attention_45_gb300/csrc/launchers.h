@@ -6,10 +6,13 @@
 
 namespace attn45 {
 
-// Key-block rows (BN) of the BF16/FP16 forward kernel for head dim d; the
-// K/V tensor maps use this as their box height.
+// Rows of the K tensor map's boxes of the BF16/FP16 forward for head dim d:
+// the key block (BN = 128) for d = 64, 128; for d = 256 (CTA pairs, 128-key
+// blocks) each CTA loads 64 of a block's keys.
 constexpr int f16_block_n(int d) { return d == 256 ? 64 : 128; }
-constexpr int F16_THREADS = 192;
+// Rows of the V tensor map's boxes: 128 keys (d = 256: each CTA of a pair
+// loads 128 keys x its 128 channels).
+constexpr int f16_v_box_rows(int d) { return d == 256 ? 128 : f16_block_n(d); }
 
 // o: output map {d, heads, rows, batch} with 64-element x 32-row boxes (bulk
 // stores of the epilogue; fixed-length launches only).
