@@ -666,6 +666,357 @@ __global__ void __launch_bounds__(128) v128_kernel(const __grid_constant__ CUten
   }
 }
 
+// ---------------------------------------------------------------- head dim 128, persistent (block scales)
+// Two persistent launches replace the per-block kernels for fixed-length
+// block quantisation at head dim 128 (two CTAs of 8 warps per SM; tiles of
+// 128 rows x 128 channels arrive by TMA into a ring; thread 0 issues the copy
+// of tile k + stages as soon as the CTA barrier that follows the reads of
+// tile k has passed, so no producer warp takes registers away):
+//  prep128_main_kernel: work list ordered by 128-row block (batch, block) and
+//    inside it [Q heads][K heads][V heads], so the V tiles (per-channel amax,
+//    atomicMax into sv) keep HBM busy while other CTAs do the Q/K arithmetic:
+//    sign flips, Walsh-Hadamard butterflies, block amax -> scale, e4m3 codes
+//    stored from registers (each thread writes its 64-byte half row). The Q/K
+//    arithmetic bounds this kernel.
+//  prep128_vcodes_kernel: re-reads the V tiles (part of V is still in L2) and
+//    writes the codes transposed (keys contiguous): each thread turns 4 rows x
+//    16 channels into 16 words of 4 keys by byte permutes in a swizzled code
+//    tile that leaves by a TMA store.
+constexpr int P128_THREADS = 256;
+constexpr int P128M_STAGES = 3;                                 // main kernel ring
+constexpr int P128M_SMEM = 1024 + P128M_STAGES * 32768;
+constexpr int P128V_STAGES = 2;                                 // V codes kernel ring
+constexpr int P128V_SMEM = 1024 + P128V_STAGES * 32768 + 2 * 16384;   // + two code tiles
+
+template <int S>
+struct P128Ring {
+  uint64_t full[S];
+  int abort;
+};
+
+enum : int { ORDER_MAIN = 0, ORDER_V = 1 };
+
+// item -> kind (0 Q, 1 K, 2 V), batch, head, 128-row block; by (batch, row
+// block), heads fastest. ORDER_MAIN: [Q heads][K heads][V heads] per row
+// block; ORDER_V: V heads only.
+__device__ __forceinline__ void p128_item(const PrepassArgs& a, int id, int order, int& kind, int& b, int& head,
+                                          int& blk) {
+  const int per = order == ORDER_V ? a.Hkv : a.H + 2 * a.Hkv;
+  const int rb = id / per;
+  int w = id - rb * per;
+  blk = rb % a.nblk;
+  b = rb / a.nblk;
+  if (order == ORDER_V) { kind = 2; head = w; return; }
+  if (w < a.H) { kind = 0; head = w; }
+  else if ((w -= a.H) < a.Hkv) { kind = 1; head = w; }
+  else { kind = 2; head = w - a.Hkv; }
+}
+
+// Copy of the CTA's k-th tile (item blockIdx.x + k * gridDim.x) into stage k % S.
+template <int S>
+__device__ __forceinline__ void p128_load(const PrepassArgs& a, P128Ring<S>& sh, uint8_t* ring, int k, int total,
+                                          int order, const CUtensorMap* mq, const CUtensorMap* mk,
+                                          const CUtensorMap* mv) {
+  const int id = blockIdx.x + k * gridDim.x;
+  if (id >= total) return;
+  int kind, b, head, blk;
+  p128_item(a, id, order, kind, b, head, blk);
+  const CUtensorMap* m = kind == 0 ? mq : (kind == 1 ? mk : mv);
+  const int st = k % S;
+  uint8_t* tile = ring + st * 32768;
+  mbar_expect_tx(&sh.full[st], 32768);
+  tma_load_4d(m, &sh.full[st], tile, 0, head, blk * ROWS, b);
+  tma_load_4d(m, &sh.full[st], tile + 16384, 64, head, blk * ROWS, b);
+}
+
+// On the way out after an abort: wait (bounded) for copies still in flight.
+template <int S>
+__device__ __forceinline__ void p128_drain(const PrepassArgs& a, P128Ring<S>& sh, int k_done, int total) {
+  for (int k = k_done; k < k_done + S; ++k)
+    if ((int)blockIdx.x + k * (int)gridDim.x < total)
+      mbar_wait_drain(&sh.full[k % S], (k / S) & 1, a.timeout_ns, a.err);
+}
+
+__global__ void __launch_bounds__(P128_THREADS, 2) prep128_main_kernel(
+    const __grid_constant__ CUtensorMap in_q, const __grid_constant__ CUtensorMap in_k,
+    const __grid_constant__ CUtensorMap in_v, const PrepassArgs a) {
+  constexpr int S = P128M_STAGES;
+  extern __shared__ uint8_t raw[];
+  uint8_t* ring = raw + ((1024 - (smem_u32(raw) & 1023)) & 1023);   // stages x 2 x [128 rows][128 B], swizzled
+  __shared__ P128Ring<S> sh;
+  __shared__ float red[2][8];
+  __shared__ float vred[2][8][128];                // V amax: per warp (16 rows) and channel
+  __shared__ uint32_t xmask[64];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int total = (a.B * a.H + 2 * a.B * a.Hkv) * a.nblk;
+  if (t == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&sh.full[s], 1);
+    sh.abort = 0;
+    fence_mbar_init();
+  }
+  if (t < 64) {
+    // sign flips as XOR masks on bf16 pairs (elements 2t, 2t+1)
+    const uint32_t w = a.sign_bits[(2 * t) >> 5] >> ((2 * t) & 31);
+    xmask[t] = a.rotate ? (((w & 1u) << 15) | (((w >> 1) & 1u) << 31)) : 0u;
+  }
+  __syncthreads();
+  if (t == 0) {
+    for (int k = 0; k < S; ++k) p128_load(a, sh, ring, k, total, ORDER_MAIN, &in_q, &in_k, &in_v);
+  }
+  // Q/K: lanes 2i, 2i+1 of a warp hold elements 0-63 / 64-127 of row warp * 16 + i
+  const int r = warp * 16 + (lane >> 1);
+  const int half = lane & 1;
+  int k = 0;
+  bool ok = true;
+  for (int id = blockIdx.x; id < total; id += gridDim.x, ++k) {
+    const int st = k % S;
+    const int pb = k & 1;
+    ok = mbar_wait(&sh.full[st], (k / S) & 1, a.timeout_ns, &sh.abort, a.err);
+    if (!ok) break;
+    int kind, b, head, blk;
+    p128_item(a, id, ORDER_MAIN, kind, b, head, blk);
+    const uint8_t* tile = ring + st * 32768;
+    const int row0 = blk * ROWS;
+    const int nvalid = min(ROWS, a.N - row0);
+    if (kind == 2) {
+      // V: per-channel amax of the block's valid rows. Thread t reads channels
+      // 8*o .. 8*o+7 (o = t % 16: 16-byte unit o % 8 of chunk o / 8) of rows
+      // 8*g .. 8*g+7 (g = t / 16); lanes t and t^16 combine their rows by a
+      // shuffle, the 8 warps through shared memory.
+      const int o = t & 15, g8 = t >> 4;
+      const uint8_t* base = tile + (o >> 3) * 16384;
+      float cm[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cm[i] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int n = g8 * 8 + i;
+        if (n < nvalid) {
+          const uint4 v = *reinterpret_cast<const uint4*>(base + n * 128 + (((o & 7) ^ (n & 7)) << 4));
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            cm[2 * m] = fmaxf(cm[2 * m], fabsf(__uint_as_float(w4[m] << 16)));
+            cm[2 * m + 1] = fmaxf(cm[2 * m + 1], fabsf(__uint_as_float(w4[m] & 0xFFFF0000u)));
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], 16));
+      if (lane < 16) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vred[pb][warp][8 * o + i] = cm[i];
+      }
+      __syncthreads();                                  // every thread has read the tile
+      if (t == 0) p128_load(a, sh, ring, k + S, total, ORDER_MAIN, &in_q, &in_k, &in_v);
+      if (t < 128) {
+        float m = vred[pb][0][t];
+#pragma unroll
+        for (int w8 = 1; w8 < 8; ++w8) m = fmaxf(m, vred[pb][w8][t]);
+        atomicMax(reinterpret_cast<unsigned int*>(a.sv + ((size_t)b * a.Hkv + head) * 128 + t), __float_as_uint(m));
+      }
+      continue;
+    }
+    // Q/K: rotate, block amax -> scale, codes
+    const bool is_q = kind == 0;
+    float x[64];
+    const uint8_t* src = tile + half * 16384 + r * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src + ((j ^ (r & 7)) << 4));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e = j * 8 + 2 * i;
+        const uint32_t u = w[i] ^ xmask[(half * 64 + e) >> 1];
+        x[e] = __uint_as_float(u << 16);
+        x[e + 1] = __uint_as_float(u & 0xFFFF0000u);
+      }
+    }
+    if (a.rotate) {
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        const float p0 = x[i], p1 = x[i + 1];
+        x[i] = __fadd_rn(p0, p1);
+        x[i + 1] = __fsub_rn(p0, p1);
+      }
+      butterfly_pairs64(x, 2);
+      butterfly_pairs64(x, 4);
+      butterfly_pairs64(x, 8);
+      butterfly_pairs64(x, 16);
+      butterfly_pairs64(x, 32);
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float o = __shfl_xor_sync(0xffffffffu, x[i], 1);
+        x[i] = half ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
+      }
+      const uint64_t c2 = f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) f2_unpack(f2_mul(f2_pack(x[i], x[i + 1]), c2), x[i], x[i + 1]);
+    }
+    float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
+    if (r < nvalid) {
+#pragma unroll
+      for (int i = 0; i < 64; i += 4) {
+        m0 = fmaxf(m0, fabsf(x[i]));
+        m1 = fmaxf(m1, fabsf(x[i + 1]));
+        m2 = fmaxf(m2, fabsf(x[i + 2]));
+        m3 = fmaxf(m3, fabsf(x[i + 3]));
+      }
+    }
+    float amax = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) red[pb][warp] = amax;
+    __syncthreads();                                    // every thread has read the tile
+    if (t == 0) p128_load(a, sh, ring, k + S, total, ORDER_MAIN, &in_q, &in_k, &in_v);
+    amax = red[pb][0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[pb][w]);
+    const float s = scale_from_amax(amax);
+    if (t == 0) {
+      const int Hx = is_q ? a.H : a.Hkv;
+      (is_q ? a.sq : a.sk)[((size_t)b * Hx + head) * a.nblk + blk] = s;
+    }
+    const Divider dv(s);
+    if (dv.fast) {
+      const uint64_t r2 = f2_pack(dv.r, dv.r), ns2 = f2_pack(-dv.s, -dv.s);
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        const uint64_t xv = f2_pack(x[i], x[i + 1]);
+        const uint64_t q0 = f2_mul(xv, r2);
+        const uint64_t e = f2_fma(q0, ns2, xv);
+        f2_unpack(f2_fma(e, r2, q0), x[i], x[i + 1]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) x[i] = __fdiv_rn(x[i], dv.s);
+    }
+    if (r < nvalid) {
+      const int Hx = is_q ? a.H : a.Hkv;
+      uint4* dst = reinterpret_cast<uint4*>((is_q ? a.q8 : a.k8) + (((size_t)b * a.N + row0 + r) * Hx + head) * 128 +
+                                            half * 64);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = j * 16;
+        dst[j] = make_uint4(e4m3x4(x[e], x[e + 1], x[e + 2], x[e + 3]), e4m3x4(x[e + 4], x[e + 5], x[e + 6], x[e + 7]),
+                            e4m3x4(x[e + 8], x[e + 9], x[e + 10], x[e + 11]),
+                            e4m3x4(x[e + 12], x[e + 13], x[e + 14], x[e + 15]));
+      }
+    }
+  }
+  if (t == 0 && !ok) p128_drain(a, sh, k, total);
+}
+
+__global__ void __launch_bounds__(P128_THREADS, 2) prep128_vcodes_kernel(const __grid_constant__ CUtensorMap in_v,
+                                                                          const __grid_constant__ CUtensorMap out_vt,
+                                                                          const PrepassArgs a) {
+  constexpr int S = P128V_STAGES;
+  extern __shared__ uint8_t raw[];
+  uint8_t* ring = raw + ((1024 - (smem_u32(raw) & 1023)) & 1023);   // stages x 2 x [128 rows][128 B], swizzled
+  uint8_t* codes = ring + S * 32768;               // 2 x [128 channels][128 keys] u8, 128-byte swizzled
+  __shared__ P128Ring<S> sh;
+  __shared__ float vdiv_s[2][128], vdiv_r[2][128];  // per-channel scale and RN(1/scale)
+  __shared__ int vdiv_slow[2];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int total = a.B * a.Hkv * a.nblk;
+  if (t == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&sh.full[s], 1);
+    sh.abort = 0;
+    fence_mbar_init();
+  }
+  if (t == 32) tma_prefetch_desc(&out_vt);
+  __syncthreads();
+  if (t == 0) {
+    for (int k = 0; k < S; ++k) p128_load(a, sh, ring, k, total, ORDER_V, &in_v, &in_v, &in_v);
+  }
+  // thread (warp w, lane q): rows 4q .. 4q+3 and the 16 channels of 16-byte
+  // unit o = (w + q) % 8 in both 64-channel chunks; over the CTA every (row
+  // quad, unit) pair is taken once, and both the unit loads and the
+  // transposed 32-bit stores are free of shared-memory bank conflicts
+  const int q = lane, o = (warp + lane) & 7;
+  int k = 0, n_v = 0;
+  bool ok = true;
+  for (int id = blockIdx.x; id < total; id += gridDim.x, ++k) {
+    const int st = k % S;
+    const int pb = k & 1;
+    ok = mbar_wait(&sh.full[st], (k / S) & 1, a.timeout_ns, &sh.abort, a.err);
+    if (!ok) break;
+    int kind, b, head, blk;
+    p128_item(a, id, ORDER_V, kind, b, head, blk);
+    const uint8_t* tile = ring + st * 32768;
+    const int nvalid = min(ROWS, a.N - blk * ROWS);
+    if (t < 128) {
+      // divisor of channel t: scale from the channel amax, and its reciprocal
+      const Divider dv(scale_from_amax(
+          __uint_as_float(*reinterpret_cast<volatile const unsigned int*>(a.sv + ((size_t)b * a.Hkv + head) * 128 + t))));
+      vdiv_s[pb][t] = dv.s;
+      vdiv_r[pb][t] = dv.r;
+      if (t == 0) vdiv_slow[pb] = 0;
+    }
+    uint8_t* ct = codes + (n_v & 1) * 16384;
+    ++n_v;
+    if (t == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // ct's previous store has read it
+    __syncthreads();
+    if (t < 128 && !Divider(vdiv_s[pb][t]).fast) vdiv_slow[pb] = 1;
+    __syncthreads();
+    const bool slow = vdiv_slow[pb] != 0;
+#pragma unroll
+    for (int ck = 0; ck < 2; ++ck) {
+      const int c0 = ck * 64 + 8 * o;                 // first of this thread's 8 channels
+      uint32_t cw[4][4];                              // [row i][channel pair m]: e4m3 codes (lo, hi)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int n = 4 * q + i;
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + ck * 16384 + n * 128 + ((o ^ (n & 7)) << 4));
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          float y0 = __uint_as_float(w4[m] << 16), y1 = __uint_as_float(w4[m] & 0xFFFF0000u);
+          const float s0 = vdiv_s[pb][c0 + 2 * m], s1 = vdiv_s[pb][c0 + 2 * m + 1];
+          if (!slow) {
+            const uint64_t xv = f2_pack(y0, y1);
+            const uint64_t r2 = f2_pack(vdiv_r[pb][c0 + 2 * m], vdiv_r[pb][c0 + 2 * m + 1]);
+            const uint64_t q0 = f2_mul(xv, r2);
+            const uint64_t e = f2_fma(q0, f2_pack(-s0, -s1), xv);
+            f2_unpack(f2_fma(e, r2, q0), y0, y1);
+          } else {
+            y0 = __fdiv_rn(y0, s0);
+            y1 = __fdiv_rn(y1, s1);
+          }
+          if (n >= nvalid) y0 = y1 = 0.f;              // pad keys past N hold code 0
+          uint16_t c2;
+          asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c2) : "f"(y1), "f"(y0));
+          cw[i][m] = c2;
+        }
+      }
+      // transpose: channel c0 + 2m gets the low bytes of rows 0-3, c0 + 2m + 1
+      // the high bytes; one 32-bit word (4 keys) per channel row
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint32_t lo01 = cw[0][m] | (cw[1][m] << 16), lo23 = cw[2][m] | (cw[3][m] << 16);
+        uint32_t even, odd;
+        asm("prmt.b32 %0, %1, %2, 0x6420;" : "=r"(even) : "r"(lo01), "r"(lo23));
+        asm("prmt.b32 %0, %1, %2, 0x7531;" : "=r"(odd) : "r"(lo01), "r"(lo23));
+        const int ce = c0 + 2 * m, co = ce + 1;
+        *reinterpret_cast<uint32_t*>(ct + ce * 128 + ((((4 * q) >> 4) ^ (ce & 7)) << 4) + ((4 * q) & 15)) = even;
+        *reinterpret_cast<uint32_t*>(ct + co * 128 + ((((4 * q) >> 4) ^ (co & 7)) << 4) + ((4 * q) & 15)) = odd;
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();                                  // tile read, code tile written
+    if (t == 0) {
+      p128_load(a, sh, ring, k + S, total, ORDER_V, &in_v, &in_v, &in_v);
+      tma_store_4d(&out_vt, ct, blk * ROWS, 0, b * a.Hkv + head, 0);
+      tma_store_commit();
+    }
+  }
+  if (t == 0) {
+    if (!ok) p128_drain(a, sh, k, total);
+    tma_store_wait_all();
+  }
+}
+
 // Turns the amax values left in the scale outputs into scales.
 __global__ void finalize_kernel(float* sq, float* sk, float* sv, int nsv, int tensor_mode) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -737,6 +1088,21 @@ cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps
   const int nqk = (a.B * a.H + a.B * a.Hkv) * a.nblk;
   const int nv = a.B * a.Hkv * a.nblk;
   const bool fast_qk = d == 128 && maps != nullptr;
+  if (fast_qk && a.block_mode) {
+    // persistent kernels: Q/K codes and V channel amax in one pass, V codes in
+    // a second one, then the amax values become scales
+    e = cudaFuncSetAttribute(prep128_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P128M_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prep128_vcodes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P128V_SMEM);
+    if (e != cudaSuccess) return e;
+    const int g1 = min(nqk + nv, 2 * sm_count), g2 = min(nv, 2 * sm_count);
+    prep128_main_kernel<<<g1, P128_THREADS, P128M_SMEM, s>>>(maps->in_q, maps->in_k, maps->in_v, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    prep128_vcodes_kernel<<<g2, P128_THREADS, P128V_SMEM, s>>>(maps->in_v, maps->out_vt, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    finalize_kernel<<<(int)((nsv + 255) / 256), 256, 0, s>>>(a.sq, a.sk, a.sv, (int)nsv, 0);
+    return cudaGetLastError();
+  }
   if (fast_qk) {
     e = cudaFuncSetAttribute(qk128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QK128_SMEM);
     if (e != cudaSuccess) return e;

@@ -28,9 +28,10 @@ struct PrepassArgs {
 
 // Tensor maps of the head-dim-128 path: bf16 inputs (Q, K, V) {128, heads, N, B}
 // with 64 x 128-row boxes, e4m3 outputs {128, heads, N, B} with 128 x 128-row
-// boxes, 128-byte swizzle.
+// boxes (per-tensor scales), and (fixed length) the transposed V codes {ldv,
+// 128, B * Hkv} with 128 keys x 128 channel-row boxes; 128-byte swizzle.
 struct Prepass128Maps {
-  CUtensorMap in_q, in_k, in_v, out_q, out_k;
+  CUtensorMap in_q, in_k, in_v, out_q, out_k, out_vt;
 };
 
 // memsets of the scale outputs, two passes of the pre-pass kernels, finalise.
