@@ -49,8 +49,12 @@ def flops_of(w) -> float:
     return f / 2 if w["causal"] else f
 
 
-FWD_BF16_KERNEL_SOURCES = ("attn_fwd2_kernel.cuh", "attn_common.cuh", "ptx.cuh", "fwd_launch.cuh", "attn_fwd_d128.cu",
-                           "launchers.h")
+FWD_BF16_KERNEL_SOURCES = ("attn_fwd2_kernel.cuh", "attn_fwd_pair_kernel.cuh", "attn_common.cuh", "ptx.cuh",
+                           "fwd_launch.cuh", "attn_fwd_d128.cu", "launchers.h")
+FWD_FP8_KERNEL_SOURCES = ("attn_fwd2_kernel.cuh", "attn_fwd_pair_kernel.cuh", "attn_common.cuh", "ptx.cuh",
+                          "fwd_launch.cuh", "attn_fwd_fp8.cu", "fp8_launchers.h", "launchers.h")
+PREPASS_KERNEL_SOURCES = ("attn_fp8_prepass.cu", "fp8_prepass.h", "ptx.cuh")
+BWD_KERNEL_SOURCES = ("attn_bwd.cu", "api_internal.h", "attn_common.cuh", "bwd_launchers.h", "ptx.cuh")
 DECODE_KT_KERNEL_SOURCES = ("attn_decode_kt.cuh", "attn_decode_kt.cu", "attn_fwd2_kernel.cuh", "attn_common.cuh",
                             "ptx.cuh", "fwd_launch.cuh", "launchers.h")
 
@@ -448,7 +452,9 @@ def bwd_measure(steps: int, warmup: int, seed: int = 0):
         "ms": round(t * 1e3, 4), "tflops": round(fl / t / 1e12, 2),
         "roofline": {"bound": "tensor", "achieved": round(fl / t / 1e12, 2), "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(fl / t / 1e12 / pk["bf16_tflops"], 4),
-                     "flops": fl, "peak_source": f"{pk['source']} bf16 burst (cuBLAS)"},
+                     "flops": fl, "peak_source": f"{pk['source']} bf16 burst (cuBLAS)",
+                     "traffic": profiled_traffic("attn_bwd_bf16_d128_n4096_noncausal.md", BWD_KERNEL_SOURCES),
+                     "source_digest": kernel_digest(BWD_KERNEL_SOURCES)[:16]},
         "gpu_launches_per_step": 4,
     }
 
@@ -511,7 +517,7 @@ DECODE = {"workload": "split-KV decode bf16 d128", "B": 8, "H": 32, "Hkv": 8, "d
           "seqlens": "uniform integers in [1024, 32768], seed 0"}
 
 
-def decode_measure(steps: int, warmup: int, seed: int = 0, splits: int = 0):
+def decode_measure(steps: int, warmup: int, seed: int = 0, splits: int = 0, group: int = 0):
     """Split-KV decode (one query token per sequence and head over a KV cache)
     on the GQA shape of the varlen configuration: 8 sequences with cached
     lengths uniform in [1k, 32k], H=32, Hkv=8, d=128, bf16. One launch per call
@@ -523,7 +529,9 @@ def decode_measure(steps: int, warmup: int, seed: int = 0, splits: int = 0):
 
     import attn_inputs as gen
     import exact_attention_45_gb300 as A
-    w = DECODE
+    w = dict(DECODE)
+    if group > 0:
+        w["H"] = group * w["Hkv"]
     B, H, Hkv, d, nmax = w["B"], w["H"], w["Hkv"], w["d"], w["Nmax"]
     seqlens = gen.varlen_lengths(B, 1024, nmax, seed=seed)
     q, _, _ = gen.qkv_fixed(B, 1, H, Hkv, d, seed=seed)
@@ -560,7 +568,8 @@ def decode_measure(steps: int, warmup: int, seed: int = 0, splits: int = 0):
         "tokens_per_s": round(B * H / t, 1),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(gbs / pk["hbm_gbs"], 4), "algorithmic_bytes": kv_bytes + io_bytes,
-                     "peak_source": f"{pk['source']} copy", "kernel": f"decode_kt_kernel<{d},{H // Hkv},bf16>",
+                     "peak_source": f"{pk['source']} copy", "kernel": (f"decode_kt_kernel<{d},{H // Hkv},bf16>" if (H // Hkv <= 16 or H // Hkv in (24, 32))
+                                else "attn_fwd2_kernel decode units + combine"),
                      "traffic": profiled_traffic("attn_decode_bf16_d128_gqa32x8_32k.md", DECODE_KT_KERNEL_SOURCES),
                      "source_digest": kernel_digest(DECODE_KT_KERNEL_SOURCES)[:16]},
         "gpu_launches_per_step": 1, "l2": L2_NOTE,
@@ -615,11 +624,15 @@ def fp8_measure(steps: int, warmup: int, seed: int = 0):
         "fwd_tflops": round(fl / t_fwd / 1e12, 2), "fwd_ms": round(t_fwd * 1e3, 4),
         "fwd_roofline": {"bound": "tensor", "achieved": round(fl / t_fwd / 1e12, 2), "peak": fp8_peak,
                          "unit": "TFLOP/s", "frac": round(fl / t_fwd / 1e12 / fp8_peak, 4),
-                         "peak_source": f"2 x {pk['source']} bf16 burst"},
+                         "peak_source": f"2 x {pk['source']} bf16 burst",
+                         "traffic": profiled_traffic("attn_fwd2_fp8_d128_n4096_noncausal.md", FWD_FP8_KERNEL_SOURCES),
+                         "source_digest": kernel_digest(FWD_FP8_KERNEL_SOURCES)[:16]},
         "prepass_ms": round(t_pre * 1e3, 4),
         "prepass_roofline": {"bound": "hbm", "achieved": round(pre_bytes / t_pre / 1e9, 1), "peak": pk["hbm_gbs"],
                              "unit": "GB/s", "frac": round(pre_bytes / t_pre / 1e9 / pk["hbm_gbs"], 4),
-                             "algorithmic_bytes": pre_bytes},
+                             "algorithmic_bytes": pre_bytes,
+                             "traffic": profiled_traffic("attn_fp8_prepass_d128_n4096.md", PREPASS_KERNEL_SOURCES),
+                             "source_digest": kernel_digest(PREPASS_KERNEL_SOURCES)[:16]},
         "prepass_plus_fwd_tflops": round(fl / t_all / 1e12, 2),
         "gpu_launches_per_step": 5,
     }
@@ -778,6 +791,8 @@ def main(argv=None):
     ap.add_argument("--no-decode", action="store_true", help="skip the split-KV decode sub-measurement")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward sub-measurement")
     ap.add_argument("--decode-splits", type=int, default=0, help="decode key-range splits (0 = automatic)")
+    ap.add_argument("--decode-group", type=int, default=0,
+                    help="--workload decode: query heads per KV head (default the workload's 4)")
     ap.add_argument("--workload", choices=("bf16", "fp8", "decode", "bwd"), default="bf16",
                     help="fp8 / decode: run only that path (e.g. for profiling)")
     ap.add_argument("--sweep", action="store_true", help="time every BF16 configuration instead")
@@ -797,7 +812,8 @@ def main(argv=None):
     elif args.workload == "decode":
         import torch
         torch.cuda.set_device(0)
-        print(json.dumps({"decode": decode_measure(args.steps, args.warmup, splits=args.decode_splits)}), flush=True)
+        print(json.dumps({"decode": decode_measure(args.steps, args.warmup, splits=args.decode_splits,
+                                                   group=args.decode_group)}), flush=True)
     elif args.sweep:
         run_sweep(args)
     elif args.sweep_fp8:

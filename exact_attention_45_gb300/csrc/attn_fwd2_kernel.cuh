@@ -512,14 +512,19 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const size_t sblk0 = VARLEN ? (size_t)(FP8 ? __ldg(p.blk_off + tl.seq) : 0) : 0;
       const size_t sq_row = VARLEN ? (size_t)tl.h * nb128 + sblk0 : ((size_t)tl.seq * p.H + tl.h) * nb128;
       const size_t sk_row = VARLEN ? (size_t)hk * nb128 + sblk0 : ((size_t)tl.seq * p.Hkv + hk) * nb128;
-      float sq_x = 1.f;
-      if constexpr (FP8)
+      float sq_x = 1.f, sk_j = 1.f;
+      if constexpr (FP8) {
         sq_x = p.fp8_block ? __ldg(p.sq + sq_row + (row0 >> 7)) : __ldg(p.sq);
+        sk_j = p.fp8_block ? __ldg(p.sk + sk_row) : __ldg(p.sk);
+      }
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nblk; ++j) {
         float sl2 = p.scale_log2;
-        if constexpr (FP8)
-          sl2 *= sq_x * (p.fp8_block ? __ldg(p.sk + sk_row + j) : __ldg(p.sk));
+        if constexpr (FP8) {
+          sl2 *= sq_x * sk_j;
+          // the next key block's scale is loaded one block ahead
+          if (p.fp8_block && j + 1 < nblk) sk_j = __ldg(p.sk + sk_row + j + 1);
+        }
         ok = mbar_wait(&bars->s_full[x], s_cnt & 1, tmo, abort_flag, p.err);
         ++s_cnt;
         if (!ok) break;
