@@ -18,8 +18,13 @@
 // lane r: query row r for S/dP/dQ, key r for dV/dK; warpgroup 0 takes the
 // first half of the columns, warpgroup 1 the second), warp 8 lane 0 loads by
 // TMA, warp 9 lane 0 issues the MMAs. TMEM: S (128 cols, reused for dQ), dP (128), dV (d),
-// dK (d). Shared memory: K_j, V_j, Q_i, dO_i tiles and the bf16 P and dS tiles
-// that feed the last three products (MN-major for P^T / dS^T, K-major for dS).
+// dK (d). Shared memory: K_j, V_j, two Q tiles (Q_{i+1} arrives while block i
+// runs), the dO_i tile and the bf16 P and dS tiles that feed the last three
+// products (MN-major for P^T / dS^T, K-major for dS).
+// Per query block the MMA thread issues dP = dO_i V^T first (its TMEM columns
+// are free once the softmax warps have read the previous dP) and S = Q_i K^T
+// once the previous dQ has been read out of S's columns; dO_i is released
+// after dV, Q_i after dK, so both next copies overlap the rest of the block.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include "api_internal.h"
@@ -35,15 +40,17 @@ struct BwdTraits {
   static constexpr int CHUNK = 128 * 128;            // 128 rows x 128 bytes
   static constexpr int TILE = 128 * D * 2;           // one 128-row bf16 tile of width d
   static constexpr int PTILE = 128 * 128 * 2;        // P or dS: 128 queries x 128 keys
-  static constexpr int OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE, OFF_DO = 3 * TILE;
-  static constexpr int OFF_P = 4 * TILE, OFF_DS = OFF_P + PTILE;
+  static constexpr int OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE;   // Q: two tiles (block parity)
+  static constexpr int OFF_DO = 4 * TILE;
+  static constexpr int OFF_P = 5 * TILE, OFF_DS = OFF_P + PTILE;
   static constexpr int OFF_BARS = OFF_DS + PTILE;
   static constexpr int SMEM = OFF_BARS + 256 + 1024;  // + alignment slack
   static constexpr int T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
 };
 
 struct BwdBars {
-  uint64_t kv_full, kv_empty, qdo_full, qdo_empty, s_full, p_full, dq_full, dq_empty, dkv_full, dkv_empty, done;
+  uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, p_full, dq_full, dq_empty, dkv_full,
+      dkv_empty, done;
   uint32_t tmem_base;
   int abort;
 };
@@ -104,8 +111,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
     mbar_init(&bars->kv_empty, 1);
-    mbar_init(&bars->qdo_full, 1);
-    mbar_init(&bars->qdo_empty, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars->q_full[x], 1);
+      mbar_init(&bars->q_empty[x], 1);
+    }
+    mbar_init(&bars->do_full, 1);
+    mbar_init(&bars->do_empty, 1);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->p_full, BWD_COMPUTE);
     mbar_init(&bars->dq_full, 1);
@@ -151,17 +162,25 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int it = 0; it < u.nblk; ++it, ++blk_it) {
           const int h = u.hkv * p.group + it / u.nI;
           const int i = bwd_qblock(u, it);
-          ok = mbar_wait(&bars->qdo_empty, (blk_it & 1) ^ 1, tmo, abort_flag, p.err);
+          // Q_i into tile blk_it & 1 (free since block blk_it - 2's dK), then dO_i
+          // (free since the previous block's dV)
+          const int qs = blk_it & 1;
+          ok = mbar_wait(&bars->q_empty[qs], ((blk_it >> 1) & 1) ^ 1, tmo, abort_flag, p.err);
           if (!ok) break;
-          mbar_expect_tx(&bars->qdo_full, 2 * T::TILE);
-          for (int c = 0; c < NC; ++c) {
-            tma_load_4d(&tmQ, &bars->qdo_full, smem + T::OFF_Q + c * T::CHUNK, c * 64, h, i * 128, u.b);
-            tma_load_4d(&tmDO, &bars->qdo_full, smem + T::OFF_DO + c * T::CHUNK, c * 64, h, i * 128, u.b);
-          }
+          mbar_expect_tx(&bars->q_full[qs], T::TILE);
+          for (int c = 0; c < NC; ++c)
+            tma_load_4d(&tmQ, &bars->q_full[qs], smem + T::OFF_Q + qs * T::TILE + c * T::CHUNK, c * 64, h, i * 128, u.b);
+          ok = mbar_wait(&bars->do_empty, (blk_it & 1) ^ 1, tmo, abort_flag, p.err);
+          if (!ok) { ++blk_it; break; }
+          mbar_expect_tx(&bars->do_full, T::TILE);
+          for (int c = 0; c < NC; ++c)
+            tma_load_4d(&tmDO, &bars->do_full, smem + T::OFF_DO + c * T::CHUNK, c * 64, h, i * 128, u.b);
         }
       }
       // never leave with copies in flight
-      if (blk_it > 0) mbar_wait_drain(&bars->qdo_full, (blk_it - 1) & 1, tmo, p.err);
+      for (int it = (blk_it > 2 ? blk_it - 2 : 0); it < blk_it; ++it)
+        mbar_wait_drain(&bars->q_full[it & 1], (it >> 1) & 1, tmo, p.err);
+      if (blk_it > 0) mbar_wait_drain(&bars->do_full, (blk_it - 1) & 1, tmo, p.err);
       if (unit_i > 0) mbar_wait_drain(&bars->kv_full, (unit_i - 1) & 1, tmo, p.err);
     }
     __syncwarp();
@@ -172,7 +191,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       constexpr uint32_t id_mm = idesc_kind_f16_ab(128, D, BF16, true, true);       // dV, dK
       constexpr uint32_t id_km = idesc_kind_f16_ab(128, D, BF16, false, true);      // dQ
       const uint32_t sk = smem_u32(smem + T::OFF_K), sv = smem_u32(smem + T::OFF_V);
-      const uint32_t sq = smem_u32(smem + T::OFF_Q), sdo = smem_u32(smem + T::OFF_DO);
+      const uint32_t sq0 = smem_u32(smem + T::OFF_Q), sdo = smem_u32(smem + T::OFF_DO);
       const uint32_t sp = smem_u32(smem + T::OFF_P), sds = smem_u32(smem + T::OFF_DS);
       int unit_i = 0, blk_it = 0;
       bool ok = true;
@@ -180,21 +199,28 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const BwdUnit u = bwd_unit(p, t, CAUSAL);
         ok = mbar_wait(&bars->kv_full, unit_i & 1, tmo, abort_flag, p.err);
         for (int it = 0; it < u.nblk && ok; ++it, ++blk_it) {
-          ok = mbar_wait(&bars->qdo_full, blk_it & 1, tmo, abort_flag, p.err);
-          // S / dQ columns free once the previous block's dQ has been read
-          if (ok && blk_it > 0) ok = mbar_wait(&bars->dq_empty, (blk_it - 1) & 1, tmo, abort_flag, p.err);
+          const int qs = blk_it & 1;
+          const uint32_t sq = sq0 + qs * T::TILE;
+          // dP = dO_i V_j^T first: its columns were read before the previous
+          // P-ready arrival (K-major operands, K = d)
+          ok = mbar_wait(&bars->do_full, blk_it & 1, tmo, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
-          // S = Q_i K_j^T and dP = dO_i V_j^T (K-major operands, K = d)
-#pragma unroll
-          for (int k = 0; k < KS; ++k) {
-            const uint32_t off = (k >> 2) * T::CHUNK + (k & 3) * 32;
-            umma_f16_ss(tmem + T::T_S, sdesc_kmajor_sw128(sq + off), sdesc_kmajor_sw128(sk + off), id_kk, k > 0);
-          }
 #pragma unroll
           for (int k = 0; k < KS; ++k) {
             const uint32_t off = (k >> 2) * T::CHUNK + (k & 3) * 32;
             umma_f16_ss(tmem + T::T_DP, sdesc_kmajor_sw128(sdo + off), sdesc_kmajor_sw128(sv + off), id_kk, k > 0);
+          }
+          // S = Q_i K_j^T once Q_i has landed and the previous block's dQ has
+          // been read out of S's columns
+          ok = mbar_wait(&bars->q_full[qs], (blk_it >> 1) & 1, tmo, abort_flag, p.err);
+          if (ok && blk_it > 0) ok = mbar_wait(&bars->dq_empty, (blk_it - 1) & 1, tmo, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < KS; ++k) {
+            const uint32_t off = (k >> 2) * T::CHUNK + (k & 3) * 32;
+            umma_f16_ss(tmem + T::T_S, sdesc_kmajor_sw128(sq + off), sdesc_kmajor_sw128(sk + off), id_kk, k > 0);
           }
           umma_commit(&bars->s_full);
           ok = mbar_wait(&bars->p_full, blk_it & 1, tmo, abort_flag, p.err);
@@ -209,14 +235,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             umma_f16_ss(tmem + T::T_DV, sdesc_mnmajor_sw128(sp + k * 2048, T::CHUNK),
                         sdesc_mnmajor_sw128(sdo + k * 2048, T::CHUNK), id_mm, (it > 0 || k > 0) ? 1u : 0u);
           }
+          umma_commit(&bars->do_empty);                   // dO_i is read by nothing after dV
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             umma_f16_ss(tmem + T::T_DK, sdesc_mnmajor_sw128(sds + k * 2048, T::CHUNK),
                         sdesc_mnmajor_sw128(sq + k * 2048, T::CHUNK), id_mm, (it > 0 || k > 0) ? 1u : 0u);
           }
-          // Q_i and dO_i are read by nothing after dK: the next block's copies
-          // may start while dQ is computed and staged
-          umma_commit(&bars->qdo_empty);
+          // Q_i is read by nothing after dK
+          umma_commit(&bars->q_empty[qs]);
           // dQ_i = dS K_j: A = dS K-major (K = 128 keys), B = K_j MN-major (N = d)
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -284,15 +310,35 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           uint32_t su[64], du[64];
           tmem_ld64_pair(tmem + lane_off + T::T_S + c * 64, su, tmem + lane_off + T::T_DP + c * 64, du);
           uint32_t pw[32], dw[32];
+          if (kmax >= (c + 1) * 64) {
+            // no key of this half is masked for this row: packed pairs, the same
+            // roundings as below (p = 2^(s * scale * log2 e - lse * log2 e);
+            // dS = (scale * p) * (dP - D))
+            const uint64_t sl2x2 = f2_pack(sl2, sl2), nlse2 = f2_pack(-lse2, -lse2);
+            const uint64_t sc2 = f2_pack(scale, scale), d2 = f2_pack(Drow, Drow);
 #pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            const int key = c * 64 + e;
-            const float p0 = key < kmax ? ex2_approx(to_f(su[e]) * sl2 - lse2) : 0.f;
-            const float p1 = key + 1 < kmax ? ex2_approx(to_f(su[e + 1]) * sl2 - lse2) : 0.f;
-            const float d0 = scale * p0 * (to_f(du[e]) - Drow);
-            const float d1 = scale * p1 * (to_f(du[e + 1]) - Drow);
-            pw[e / 2] = pack16<BF16>(p0, p1);
-            dw[e / 2] = pack16<BF16>(d0, d1);
+            for (int e = 0; e < 64; e += 2) {
+              float p0, p1;
+              f2_unpack(f2_fma(f2_pack(to_f(su[e]), to_f(su[e + 1])), sl2x2, nlse2), p0, p1);
+              p0 = ex2_approx(p0);
+              p1 = ex2_approx(p1);
+              const uint64_t pp = f2_pack(p0, p1);
+              float d0, d1;
+              f2_unpack(f2_mul(f2_mul(pp, sc2), f2_sub(f2_pack(to_f(du[e]), to_f(du[e + 1])), d2)), d0, d1);
+              pw[e / 2] = pack16<BF16>(p0, p1);
+              dw[e / 2] = pack16<BF16>(d0, d1);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 64; e += 2) {
+              const int key = c * 64 + e;
+              const float p0 = key < kmax ? ex2_approx(to_f(su[e]) * sl2 - lse2) : 0.f;
+              const float p1 = key + 1 < kmax ? ex2_approx(to_f(su[e + 1]) * sl2 - lse2) : 0.f;
+              const float d0 = scale * p0 * (to_f(du[e]) - Drow);
+              const float d1 = scale * p1 * (to_f(du[e + 1]) - Drow);
+              pw[e / 2] = pack16<BF16>(p0, p1);
+              dw[e / 2] = pack16<BF16>(d0, d1);
+            }
           }
           // the previous block's dQ reduction reads the P/dS tiles as its
           // staging: wait for it only now, after the loads and the arithmetic
@@ -323,6 +369,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           uint32_t qu[HC];
           if constexpr (HC == 64) tmem_ld64(tmem + lane_off + T::T_S + half * HC, qu);
           else tmem_ld32(tmem + lane_off + T::T_S + half * HC, qu);
+          // dQ is in registers (the loads wait for completion): S's columns are
+          // free for the next block's S while the staging and reduction go on
+          tc_fence_before();
+          mbar_arrive(&bars->dq_empty);
 #pragma unroll
           for (int v4 = 0; v4 < HC / 4; ++v4) {
             const int cc = half * (HC / 32) + (v4 >> 3);
@@ -338,8 +388,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tma_reduce_add_4d(&tmDQ, tp + cc * T::CHUNK, cc * 32, h, i * 128, u.b);
           tma_store_commit();
         }
-        tc_fence_before();
-        mbar_arrive(&bars->dq_empty);
       }
       if (!ok) break;
       // unit epilogue: dK_j, dV_j rows (thread r = key j*128 + r)
