@@ -498,7 +498,7 @@ def fp8_prepass(q, k, v, mode: str = "block", rotate: bool = True, seed: int = 0
 
 
 def fp8_attention_emulated(pre: dict, causal: bool = False, scale: float | None = None,
-                           block_n: int = 128, rows=None, quantize_p: bool = True):
+                           block_n: int = 128, rows=None, quantize_p: bool = True, flip_tol: float | None = None):
     """FP8 attention on pre-pass codes, following the method's own steps.
 
     Online softmax ("Related papers: FlashAttention-4" page, teaser on online
@@ -520,6 +520,14 @@ def fp8_attention_emulated(pre: dict, causal: bool = False, scale: float | None 
     ``rows`` = (b, h, i) arrays; default all rows. Returns o [R,d], lse [R].
     ``quantize_p=False`` keeps p unquantised (then the result is the exact
     softmax attention of the dequantised inputs, for any ``block_n``).
+
+    ``flip_tol`` (a relative distance) adds a third output ``flip`` [R, d]:
+    for every p whose M p lies within ``flip_tol`` of a midpoint between two
+    neighbouring e4m3 values, the change in O that rounding it the other way
+    would make, |one e4m3 step| * 2^(m_block - m_final) * |V8_j| * sv / (M l),
+    summed over such p. Both roundings of such a p are the method's result:
+    which one a computation takes depends on the last bits of its score
+    arithmetic (fp32 against fp64 here). o and lse are unchanged.
     """
     q8 = e4m3_decode(pre["q8"])
     k8 = e4m3_decode(pre["k8"])
@@ -539,6 +547,7 @@ def fp8_attention_emulated(pre: dict, causal: bool = False, scale: float | None 
     R = rb.size
     o = np.zeros((R, d))
     lse = np.zeros(R)
+    flip = np.zeros((R, d)) if flip_tol is not None else None
     for r in range(R):
         b, h, i = int(rb[r]), int(rh[r]), int(ri[r])
         hk = h // g
@@ -547,6 +556,7 @@ def fp8_attention_emulated(pre: dict, causal: bool = False, scale: float | None 
         svec = sv[b, hk, :] if block else np.full(d, sv[0])
         m, l = -np.inf, 0.0
         acc = np.zeros(d)
+        facc = np.zeros(d)
         for j0 in range(0, nk, block_n):
             j1 = min(nk, j0 + block_n)
             keys = np.arange(j0, j1)
@@ -563,9 +573,21 @@ def fp8_attention_emulated(pre: dict, causal: bool = False, scale: float | None 
             else:
                 p8 = p * P_FP8_MULT
             acc = acc * alpha + p8 @ vt8[b, hk, :, j0:j1].T
+            if flip_tol is not None:
+                pm = p * P_FP8_MULT
+                # e4m3 spacing at pm: 2^(e-3) in the normal range [2^e, 2^(e+1)),
+                # 2^-9 below 2^-6 (subnormals, and the step from 0 to 2^-9)
+                step = np.where(pm >= 2.0 ** -6, 2.0 ** (np.floor(np.log2(np.maximum(pm, 2.0 ** -6))) - 3), 2.0 ** -9)
+                frac = pm / step - np.floor(pm / step)
+                dist = np.abs(frac - 0.5) * step / np.maximum(pm, 1e-300)
+                facc = facc * alpha + np.where(dist <= flip_tol, step, 0.0) @ np.abs(vt8[b, hk, :, j0:j1]).T
             m = m_new
         o[r] = acc * svec / (P_FP8_MULT * l)
         lse[r] = (m + math.log2(l)) * math.log(2.0)
+        if flip_tol is not None:
+            flip[r] = facc * np.abs(svec) / (P_FP8_MULT * l)
+    if flip_tol is not None:
+        return o, lse, flip
     return o, lse
 
 
@@ -633,11 +655,12 @@ def fp8_prepass_varlen(q, k, v, cu_seqlens, mode: str = "block", rotate: bool = 
 
 
 def fp8_attention_emulated_varlen(pre: dict, cu_seqlens, causal: bool = False, scale: float | None = None,
-                                  rows=None):
+                                  rows=None, flip_tol: float | None = None):
     """``fp8_attention_emulated`` of every sequence of a packed pre-pass result
     (each sequence is its own problem; causal masking is per sequence).
     ``rows`` = (sequence, head, local row) arrays; default every row. Returns
-    o [R, d] and lse [R] in that row order."""
+    o [R, d] and lse [R] in that row order (and ``flip`` [R, d] when
+    ``flip_tol`` is given)."""
     cu = np.asarray(cu_seqlens, dtype=np.int64)
     nseq = cu.size - 1
     boff = pre["blk_off"]
@@ -654,6 +677,7 @@ def fp8_attention_emulated_varlen(pre: dict, cu_seqlens, causal: bool = False, s
     rs, rh, ri = (np.asarray(x, np.int64) for x in rows)
     o = np.zeros((rs.size, d))
     lse = np.zeros(rs.size)
+    flip = np.zeros((rs.size, d))
     for s in np.unique(rs):
         a, b = int(cu[s]), int(cu[s + 1])
         n = b - a
@@ -665,7 +689,11 @@ def fp8_attention_emulated_varlen(pre: dict, cu_seqlens, causal: bool = False, s
               "sq": pre["sq"][None, :, boff[s]:boff[s] + nb] if blk else pre["sq"],
               "sk": pre["sk"][None, :, boff[s]:boff[s] + nb] if blk else pre["sk"],
               "sv": pre["sv"][s:s + 1] if blk else pre["sv"], "mode": pre["mode"]}
-        os_, ls_ = fp8_attention_emulated(ps, causal=causal, scale=scale,
-                                          rows=(np.zeros(sel.size, np.int64), rh[sel], ri[sel]))
-        o[sel], lse[sel] = os_, ls_
+        res = fp8_attention_emulated(ps, causal=causal, scale=scale,
+                                     rows=(np.zeros(sel.size, np.int64), rh[sel], ri[sel]), flip_tol=flip_tol)
+        o[sel], lse[sel] = res[0], res[1]
+        if flip_tol is not None:
+            flip[sel] = res[2]
+    if flip_tol is not None:
+        return o, lse, flip
     return o, lse

@@ -12,6 +12,14 @@ import oracle as O
 
 pytestmark = pytest.mark.gpu
 
+# Where the kernel's fp32 scores and the oracle's fp64 ones put some p on
+# opposite sides of an e4m3 rounding midpoint, both roundings are the method's
+# result: the oracle reports, per output element, what rounding each p within
+# FLIP_TOL (relative) of a midpoint the other way would change, and the bound
+# grants that. 2^-12 is far above the fp32 score error at these sizes (the
+# straddles seen were within 2^-22) and covers well under 1% of the p values.
+FLIP_TOL = 2.0 ** -12
+
 
 def _gpu_prepass(q, k, v, cu, mode, rotate, seed):
     import exact_attention_45_gb300 as A
@@ -53,7 +61,7 @@ def test_fp8_forward_varlen_matches_emulation(causal, mode):
     torch.cuda.synchronize()
     assert A.attn_get_device_error() == 0
     ref = O.fp8_prepass_varlen(q, k, v, cu, mode=mode, rotate=True, seed=1)
-    o_ref, l_ref = O.fp8_attention_emulated_varlen(ref, cu, causal=causal)
+    o_ref, l_ref, flip = O.fp8_attention_emulated_varlen(ref, cu, causal=causal, flip_tol=FLIP_TOL)
     rs, rh, ri = [], [], []
     for s, n in enumerate(lengths):
         for h in range(4):
@@ -64,7 +72,7 @@ def test_fp8_forward_varlen_matches_emulation(causal, mode):
     o_g = o.float().cpu().numpy()[tok, np.array(rh)]
     l_g = lse.cpu().numpy()[np.array(rh), tok]
     err = o_g - o_ref
-    bound = 1e-2 + 4e-3 * np.abs(o_ref)
+    bound = 1e-2 + 4e-3 * np.abs(o_ref) + flip
     assert float((np.abs(err) / bound).max()) <= 1.0 and float(np.sqrt((err ** 2).mean())) <= 2e-3
     assert np.abs(l_g - l_ref).max() <= 2e-3
 

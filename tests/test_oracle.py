@@ -466,6 +466,38 @@ def test_fp8_emulation_p_rounding_closed_form(p, rounded):
     assert abs(lse - math.log(l)) <= 1e-12
 
 
+@pytest.mark.parametrize("p,step", [
+    (0.59375, 2.0 ** -4),        # midpoint of 0.5625 and 0.625
+    (0.96875, 2.0 ** -4),        # midpoint of 0.9375 and 1.0 (top of the binade)
+    (2.0 ** -10, 2.0 ** -9),     # midpoint of 0 and the smallest subnormal
+    (0.3, 0.0),                  # 0.6 of the way between 0.28125 and 0.3125: no midpoint
+])
+def test_fp8_emulation_flip_allowance_closed_form(p, step):
+    # the one-row problem above: key 1 has p; the allowance for output channel 1
+    # is one e4m3 step of p times 7 / l, and zero where p is not on a midpoint
+    pre = _fp8_closed_form_problem([0.0, -1.0])
+    _, _, flip = O.fp8_attention_emulated(pre, scale=-math.log(p) / 7.0, rows=([0], [0], [0]), flip_tol=2.0 ** -12)
+    want = np.zeros(64)
+    want[1] = 7.0 * step / (1.0 + p)
+    assert np.abs(flip[0] - want).max() <= 1e-15, (flip[0][:2], want[:2])
+
+
+def test_fp8_emulation_flip_allowance_rescaled_by_a_raise():
+    # single-key blocks t = (0, log2 p, 12 * -log2 p) with p = 0.59375: the
+    # third block raises m to t_2 > 8, so key 1's allowance (and its share of
+    # O and l) is scaled by 2^-t_2; keys 0 and 2 have p = 1, exact in e4m3
+    p = 0.59375
+    t2 = 12.0 * -math.log2(p)
+    pre = _fp8_closed_form_problem([0.0, -1.0, 12.0])
+    o, _, flip = O.fp8_attention_emulated(pre, scale=-math.log(p) / 7.0, block_n=1, rows=([0], [0], [0]),
+                                          flip_tol=2.0 ** -12)
+    l = (1.0 + p) * 2.0 ** -t2 + 1.0
+    want = np.zeros(64)
+    want[1] = 7.0 * 2.0 ** -4 * 2.0 ** -t2 / l
+    assert np.abs(flip[0] - want).max() <= 1e-15, (flip[0][:3], want[:3])
+    assert abs(o[0, 1] - 7.0 * 0.625 * 2.0 ** -t2 / l) <= 1e-12 and abs(o[0, 2] - 7.0 / l) <= 1e-12
+
+
 def test_fp8_emulation_block_maximum_at_the_margin_keeps_m():
     # single-key blocks with t = 0, 8, -2 (sc = ln2/7): the second block's
     # maximum is exactly m + 8, which does not raise m (strict comparison), so
