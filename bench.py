@@ -701,12 +701,14 @@ def run_sweep(args):
 
 
 def run_sweep_fp8(args):
-    """FP8 forward over the FP8 benchmark set (one GPU): d=128, H=16,
-    N = 1024..16384 with B*N = 16384, outlier inputs, the four quantisation
-    variants (per-block or per-tensor scales, with or without the Hadamard
-    rotation), non-causal, and causal for per-block + rotation. Pre-pass and
-    forward timed separately (median of --sweep-reps, L2 flushed). One JSON
-    object per line on stdout."""
+    """FP8 forward over the FP8 benchmark set (one GPU): hidden size 2048
+    (d=128 with H=16, d=256 with H=8; --sweep-dims keeps a subset),
+    N = 1024..16384 with B*N = 16384, outlier inputs; at d=128 the four
+    quantisation variants (per-block or per-tensor scales, with or without the
+    Hadamard rotation) non-causal, and causal for per-block + rotation; at
+    d=256 per-block + rotation, non-causal and causal. Pre-pass and forward
+    timed separately (median of --sweep-reps, L2 flushed). One JSON object per
+    line on stdout."""
     import torch
 
     import attn_inputs as gen
@@ -730,10 +732,12 @@ def run_sweep_fp8(args):
         torch.cuda.synchronize()
         return statistics.median(a.elapsed_time(b) for a, b in ts) / 1e3
 
-    H, d = 16, 128
-    variants = [("block", True, False), ("block", False, False), ("tensor", True, False), ("tensor", False, False),
-                ("block", True, True)]
-    for N in (1024, 2048, 4096, 8192, 16384):
+    dims = [int(x) for x in args.sweep_dims.split(",") if x] or [128, 256]
+    all_variants = [("block", True, False), ("block", False, False), ("tensor", True, False),
+                    ("tensor", False, False), ("block", True, True)]
+    for d, N in ((d, N) for d in dims for N in (1024, 2048, 4096, 8192, 16384)):
+        H = 2048 // d
+        variants = all_variants if d == 128 else [("block", True, False), ("block", True, True)]
         B = 16384 // N
         q, k, v = (t.cuda() for t in gen.qkv_fixed(B, N, H, H, d, seed=0, dist="outlier"))
         o = torch.empty((B, N, H, d), dtype=torch.bfloat16, device="cuda")

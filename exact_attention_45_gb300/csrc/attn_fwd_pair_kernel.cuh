@@ -1,5 +1,6 @@
-// attn_fwd_pair_kernel.cuh -- BF16/FP16 forward for head dim 256 on pairs of
-// CTAs that share their tensor-core work (tcgen05 cta_group::2).
+// attn_fwd_pair_kernel.cuh -- forward for head dim 256 on pairs of CTAs that
+// share their tensor-core work (tcgen05 cta_group::2): BF16/FP16, and FP8
+// (e4m3 codes with block scales, fixed length).
 //
 // Same computation as the other forward kernels (tiling so the scores never
 // reach HBM: "FlashAttention: Fast and Memory-Efficient Exact Attention with
@@ -18,8 +19,13 @@
 //               TMEM, V's channels split 128 / 128 between the CTAs.
 // Per CTA, TMEM holds two S buffers (2 x 128 columns) and O (256 columns), so
 // S of block j+1 is computed while the softmax turns block j into P. Shared
-// memory per CTA: Q 64 KB + 2 ring slots x (K half 32 KB + V half 32 KB) +
-// output staging 16 KB.
+// memory per CTA (16-bit): Q 64 KB + 2 ring slots x (K half 32 KB + V half
+// 32 KB) + output staging 16 KB; FP8 halves the operand tiles (V comes
+// transposed, channels as rows, so both products are K-major) and keeps three
+// ring slots. FP8 follows the two-tile kernel's FP8 path: the dequantisation
+// scalar sq * sk of a 128 x 128 score block is folded into the softmax scale,
+// P (<= 2^8 under the lazy maximum) is rounded to e4m3, four per TMEM column,
+// and the epilogue applies V's channel scales.
 //
 // Roles per CTA (192 threads): warps 0-3 softmax / correction / epilogue of
 // this CTA's 128 rows (thread r owns row r = TMEM lane r); warp 4 TMA
@@ -42,21 +48,23 @@
 
 namespace attn45 {
 
-template <int D>
+template <int D, int ELEM = 2>
 struct PairTraits {
   static constexpr int BN = 128;                      // keys per block (over the pair)
-  static constexpr int NC = D / 64;                   // 128-byte chunks per Q / K row
-  static constexpr int Q_CHUNK = BLOCK_M * 128;       // 128 rows x 64 channels
-  static constexpr int Q_BYTES = BLOCK_M * D * 2;
+  static constexpr int NC = D * ELEM / 128;           // 128-byte chunks per Q / K row
+  static constexpr int Q_CHUNK = BLOCK_M * 128;       // 128 rows x 128 bytes
+  static constexpr int Q_BYTES = BLOCK_M * D * ELEM;
   static constexpr int K_ROWS = BN / 2;               // keys of a block held by one CTA
   static constexpr int K_CHUNK = K_ROWS * 128;
-  static constexpr int K_BYTES = K_ROWS * D * 2;
+  static constexpr int K_BYTES = K_ROWS * D * ELEM;
   static constexpr int V_COLS = D / 2;                // channels of V held by one CTA
-  static constexpr int V_NC = V_COLS / 64;
-  static constexpr int V_CHUNK = BN * 128;            // 128 keys x 64 channels, MN-major
-  static constexpr int V_BYTES = BN * V_COLS * 2;
+  // 16-bit: V tiles of 128 keys x 64 channels, MN-major; FP8: one V^T tile of
+  // V_COLS channel rows x 128 keys, K-major
+  static constexpr int V_NC = ELEM == 2 ? V_COLS / 64 : 1;
+  static constexpr int V_CHUNK = ELEM == 2 ? BN * 128 : V_COLS * 128;
+  static constexpr int V_BYTES = BN * V_COLS * ELEM;
   static constexpr int SLOT_BYTES = K_BYTES + V_BYTES;
-  static constexpr int STAGES = 2;
+  static constexpr int STAGES = ELEM == 2 ? 2 : 3;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_SLOT = Q_BYTES;
   static constexpr int OFF_STAGE = OFF_SLOT + STAGES * SLOT_BYTES;  // 4 softmax warps x 4 KB
@@ -74,7 +82,7 @@ struct PairTraits {
 
 struct BarsPair {
   uint64_t q_full, q_empty;
-  uint64_t slot_full[2], slot_empty[2];
+  uint64_t slot_full[3], slot_empty[3];
   uint64_t s_full[2], p_full[2];
   uint64_t o_done;
   uint64_t mma_done;
@@ -83,12 +91,16 @@ struct BarsPair {
 };
 static_assert(sizeof(BarsPair) <= 256, "barrier block");
 
-template <int D, bool CAUSAL, bool VARLEN, bool BF16>
+template <int D, bool CAUSAL, bool VARLEN, int KIND>
 __global__ void __launch_bounds__(192, 1)
 attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                      const FwdParams p) {
-  using T = PairTraits<D>;
+  constexpr bool FP8 = KIND == KIND_E4M3;
+  constexpr bool BF16 = KIND == KIND_BF16;
+  constexpr int ELEM = FP8 ? 1 : 2;
+  static_assert(!(FP8 && VARLEN), "FP8 on CTA pairs takes fixed-length batches");
+  using T = PairTraits<D, ELEM>;
   constexpr int BN = T::BN;
   constexpr bool STAGE_OUT = !VARLEN;
   extern __shared__ uint8_t smem_raw[];
@@ -160,8 +172,6 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       const uint32_t q_full_l = mapa_shared(&bars->q_full, 0);
-      uint32_t slot_full_l[T::STAGES];
-      for (int s = 0; s < T::STAGES; ++s) slot_full_l[s] = mapa_shared(&bars->slot_full[s], 0);
       int slot_it = 0, tile_i = 0;
       bool ok = true;
       for (int t = cluster_id; t < ntiles && ok; t += nclusters) {
@@ -175,7 +185,7 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (leader) mbar_expect_tx(&bars->q_full, 2 * T::Q_BYTES);
 #pragma unroll
         for (int c = 0; c < T::NC; ++c)
-          tma_load_4d_pair(&tmQ, q_full_l, sQ + c * T::Q_CHUNK, c * 64, tl.h,
+          tma_load_4d_pair(&tmQ, q_full_l, sQ + c * T::Q_CHUNK, c * (128 / ELEM), tl.h,
                            tl.tma_row0 + tl.sblk * SUPER_M + (int)rank * BLOCK_M, tl.tma_b);
         // slot j: K_j (j < nkv; this CTA's 64 keys) and V_{j-1} (j >= 1; this
         // CTA's 128 channels of all 128 keys)
@@ -184,19 +194,26 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           ok = mbar_wait(&bars->slot_empty[st], ((slot_it / T::STAGES) & 1) ^ 1, tmo, abort_flag, p.err);
           if (!ok) break;
           uint8_t* slot = sSlot + st * T::SLOT_BYTES;
+          const uint32_t slot_full_l = mapa_shared(&bars->slot_full[st], 0);
           if (leader)
             mbar_expect_tx(&bars->slot_full[st], (j < nkv ? 2 * T::K_BYTES : 0) + (j >= 1 ? 2 * T::V_BYTES : 0));
           if (j < nkv) {
 #pragma unroll
             for (int c = 0; c < T::NC; ++c)
-              tma_load_4d_pair(&tmK, slot_full_l[st], slot + c * T::K_CHUNK, c * 64, hk,
+              tma_load_4d_pair(&tmK, slot_full_l, slot + c * T::K_CHUNK, c * (128 / ELEM), hk,
                                tl.tma_row0 + j * BN + (int)rank * T::K_ROWS, tl.tma_b);
           }
           if (j >= 1) {
+            if constexpr (FP8) {
+              // V^T [B*Hkv][D][ldv]: 128 keys of this CTA's channel rows
+              tma_load_4d_pair(&tmV, slot_full_l, slot + T::K_BYTES, (j - 1) * BN, (int)rank * T::V_COLS,
+                               tl.seq * p.Hkv + hk, 0);
+            } else {
 #pragma unroll
-            for (int c = 0; c < T::V_NC; ++c)
-              tma_load_4d_pair(&tmV, slot_full_l[st], slot + T::K_BYTES + c * T::V_CHUNK,
-                               (int)rank * T::V_COLS + c * 64, hk, tl.tma_row0 + (j - 1) * BN, tl.tma_b);
+              for (int c = 0; c < T::V_NC; ++c)
+                tma_load_4d_pair(&tmV, slot_full_l, slot + T::K_BYTES + c * T::V_CHUNK,
+                                 (int)rank * T::V_COLS + c * 64, hk, tl.tma_row0 + (j - 1) * BN, tl.tma_b);
+            }
           }
         }
       }
@@ -214,8 +231,10 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // O += P(j-1) V_{j-1} once both CTAs' P(j-1) is stored, so the tensor core
     // computes the next scores while the softmax warps work.
     if (leader && lane == 0) {
-      constexpr uint32_t idesc_s = idesc_kind_f16(2 * BLOCK_M, BN, BF16, false);
-      constexpr uint32_t idesc_o = idesc_kind_f16(2 * BLOCK_M, D, BF16, true);
+      constexpr uint32_t idesc_s = FP8 ? idesc_kind_f8_e4m3(2 * BLOCK_M, BN) : idesc_kind_f16(2 * BLOCK_M, BN, BF16, false);
+      constexpr uint32_t idesc_o = FP8 ? idesc_kind_f8_e4m3(2 * BLOCK_M, D) : idesc_kind_f16(2 * BLOCK_M, D, BF16, true);
+      constexpr int S_STEPS = D * ELEM / 32;               // 32-byte K steps of Q K^T
+      constexpr int PV_STEPS = BN * ELEM / 32;             // 32-byte K steps of P V
       constexpr uint16_t both = 3;
       const uint32_t qa = smem_u32(sQ);
       const uint32_t slot_a = smem_u32(sSlot);
@@ -238,11 +257,15 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           if (j < nkv) {
             const uint32_t s_tmem = tmem + T::TMEM_S + (s_it & 1) * BN;
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
+            for (int k = 0; k < S_STEPS; ++k) {
               const uint32_t qo = (k >> 2) * T::Q_CHUNK + (k & 3) * 32;
               const uint32_t ko = (k >> 2) * T::K_CHUNK + (k & 3) * 32;
-              umma_f16_ss_pair(s_tmem, sdesc_kmajor_sw128(qa + qo), sdesc_kmajor_sw128(kb + ko), idesc_s,
-                               k > 0 ? 1u : 0u);
+              if constexpr (FP8)
+                umma_f8_ss_pair(s_tmem, sdesc_kmajor_sw128(qa + qo), sdesc_kmajor_sw128(kb + ko), idesc_s,
+                                k > 0 ? 1u : 0u);
+              else
+                umma_f16_ss_pair(s_tmem, sdesc_kmajor_sw128(qa + qo), sdesc_kmajor_sw128(kb + ko), idesc_s,
+                                 k > 0 ? 1u : 0u);
             }
             umma_commit_pair(&bars->s_full[s_it & 1], both);
             ++s_it;
@@ -254,9 +277,15 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             tc_fence_after();
             const uint32_t a_tmem = tmem + T::TMEM_S + (pv_it & 1) * BN;
 #pragma unroll
-            for (int k = 0; k < BN / 16; ++k)
-              umma_f16_ts_pair(tmem + T::TMEM_O, a_tmem + k * 8, sdesc_mnmajor_sw128(vb + k * 2048, T::V_CHUNK),
-                               idesc_o, (j > 1 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < PV_STEPS; ++k) {
+              // each K step is 8 TMEM columns of P (16 x 16-bit or 32 x 8-bit)
+              if constexpr (FP8)
+                umma_f8_ts_pair(tmem + T::TMEM_O, a_tmem + k * 8, sdesc_kmajor_sw128(vb + k * 32), idesc_o,
+                                (j > 1 || k > 0) ? 1u : 0u);
+              else
+                umma_f16_ts_pair(tmem + T::TMEM_O, a_tmem + k * 8, sdesc_mnmajor_sw128(vb + k * 2048, T::V_CHUNK),
+                                 idesc_o, (j > 1 || k > 0) ? 1u : 0u);
+            }
             umma_commit_pair(&bars->o_done, both);
             ++pv_it;
           }
@@ -273,7 +302,7 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int r = threadIdx.x;                         // row within this CTA's tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t to = tmem + lane_off + T::TMEM_O;
-    const uint32_t p_full_l[2] = {mapa_shared(&bars->p_full[0], 0), mapa_shared(&bars->p_full[1], 0)};
+    const uint32_t p_full_l0 = mapa_shared(&bars->p_full[0], 0), p_full_l1 = mapa_shared(&bars->p_full[1], 0);
     constexpr float lazy = LAZY_RESCALE_LOG2;
     int s_cnt = 0, o_cnt = 0;
     bool ok = true;
@@ -283,10 +312,24 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       if (nkv == 0) continue;
       const int row0 = tl.sblk * SUPER_M + (int)rank * BLOCK_M;   // first row of this CTA's tile
       const int i_row = row0 + r;
+      const int hk = tl.h / p.group;
+      // FP8 block scales [B][heads][ceil(N/128)]: this tile's Q block, key block j
+      const int nb128 = ceil_div(tl.n, BLOCK_M);
+      const size_t sk_row = ((size_t)tl.seq * p.Hkv + hk) * nb128;
+      float sq_x = 1.f, sk_j = 1.f;
+      if constexpr (FP8) {
+        sq_x = p.fp8_block ? __ldg(p.sq + ((size_t)tl.seq * p.H + tl.h) * nb128 + min(row0 >> 7, nb128 - 1))
+                           : __ldg(p.sq);
+        sk_j = p.fp8_block ? __ldg(p.sk + sk_row) : __ldg(p.sk);
+      }
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nkv; ++j) {
         const int sb = s_cnt & 1;
-        const float sl2 = p.scale_log2;
+        float sl2 = p.scale_log2;
+        if constexpr (FP8) {
+          sl2 *= sq_x * sk_j;
+          if (p.fp8_block && j + 1 < nkv) sk_j = __ldg(p.sk + sk_row + j + 1);
+        }
         ok = mbar_wait(&bars->s_full[sb], (s_cnt >> 1) & 1, tmo, abort_flag, p.err);
         ++s_cnt;
         if (!ok) break;
@@ -330,7 +373,8 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         const uint64_t negm2 = f2_pack(-m_use, -m_use);
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-        uint32_t pk[BN / 2];
+        constexpr int PW = FP8 ? BN / 4 : BN / 2;
+        uint32_t pk[PW];
 #pragma unroll
         for (int c = 0; c < BN; c += 4) {
           float a0, a1, b0, b1;
@@ -342,16 +386,21 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           b1 = ex2_approx(b1);
           acc0 = f2_add(acc0, f2_pack(a0, a1));
           acc1 = f2_add(acc1, f2_pack(b0, b1));
-          pk[c / 2] = pack2(a0, a1, BF16);
-          pk[c / 2 + 1] = pack2(b0, b1, BF16);
-          if (c == 60) tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          if constexpr (FP8) {
+            pk[c / 4] = pack_e4m3x4(a0, a1, b0, b1);     // P as e4m3, four per TMEM column
+          } else {
+            pk[c / 2] = pack2(a0, a1, BF16);
+            pk[c / 2 + 1] = pack2(b0, b1, BF16);
+            if (c == 60) tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          }
         }
         float sum0, sum1, sum2, sum3;
         f2_unpack(acc0, sum0, sum1);
         f2_unpack(acc1, sum2, sum3);
         l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
         m = m_new;
-        tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        if constexpr (FP8) tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        else tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         tmem_st_wait();
         if (j > 0) {
           // O += P(j-1) V_{j-1} was issued after S(j): wait for it before the
@@ -375,7 +424,7 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(p_full_l[sb]);
+        if (lane == 0) mbar_arrive_cluster(sb ? p_full_l1 : p_full_l0);
       }
       if (!ok) break;
       ok = mbar_wait(&bars->o_done, o_cnt & 1, tmo, abort_flag, p.err);
@@ -386,14 +435,26 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       const float inv_l = 1.f / l;
       const size_t tok = (size_t)tl.tok0 + (size_t)(valid ? i_row : 0);
       uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.o) + (tok * p.H + tl.h) * D);
+      const float* svp = FP8 ? (p.fp8_block ? p.sv + ((size_t)tl.seq * p.Hkv + hk) * D : p.sv) : nullptr;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t u[64];
         tmem_ld64(to + c * 64, u);
         uint32_t w[32];
+        if constexpr (FP8) {
+          // O / l times V's channel scale; BF16 output
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          w[i] = pack2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l, BF16);
+          for (int i = 0; i < 32; ++i) {
+            const int ch = c * 64 + 2 * i;
+            const float s0 = p.fp8_block ? __ldg(svp + ch) : __ldg(svp);
+            const float s1 = p.fp8_block ? __ldg(svp + ch + 1) : s0;
+            w[i] = pack2(__uint_as_float(u[2 * i]) * (s0 * inv_l), __uint_as_float(u[2 * i + 1]) * (s1 * inv_l), true);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            w[i] = pack2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l, BF16);
+        }
         if constexpr (STAGE_OUT) {
           // this warp's 32 rows x 64 columns, 128-byte swizzled, one bulk
           // tensor store (rows past the sequence end are clipped by the copy)

@@ -1,4 +1,4 @@
-// fp8_launchers.h -- host entry of the FP8 forward kernel (head dim 128).
+// fp8_launchers.h -- host entries of the FP8 forward kernels (head dims 128 and 256).
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -12,4 +12,10 @@ namespace attn45 {
 cudaError_t launch_fwd_fp8_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                 const CUtensorMap& o, const FwdParams& p, bool causal, bool varlen, int sm_count,
                                 cudaStream_t s);
+// Head dim 256, fixed length, on CTA pairs: q: e4m3 map {256, H, N, B} with
+// 128-byte x 128-row boxes; k: the same over Hkv with 64-row boxes (each CTA
+// of a pair loads 64 of a block's 128 keys); v: V^T map {ldv, 256, B*Hkv, 1}
+// with 128-key x 128-channel-row boxes; o: bf16 map with 64 x 32-row boxes.
+cudaError_t launch_fwd_fp8_d256(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                const CUtensorMap& o, const FwdParams& p, bool causal, int sm_count, cudaStream_t s);
 }  // namespace attn45

@@ -39,11 +39,11 @@ cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtens
 // CTA pairs (clusters of 2, head dim 256): persistent clusters, at most as
 // many as fit on the device at once (cudaOccupancyMaxActiveClusters, looked up
 // once per device and instantiation), each walking 256-row units.
-template <int D, bool CAUSAL, bool VARLEN, bool BF16>
+template <int D, bool CAUSAL, bool VARLEN, int KIND>
 cudaError_t launch_cta_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
                             FwdParams p, int sm_count, cudaStream_t stream) {
-  using T = PairTraits<D>;
-  auto kern = attn_fwd_pair_kernel<D, CAUSAL, VARLEN, BF16>;
+  using T = PairTraits<D, KIND == KIND_E4M3 ? 1 : 2>;
+  auto kern = attn_fwd_pair_kernel<D, CAUSAL, VARLEN, KIND>;
   const int smem = T::SMEM_FIXED + (VARLEN ? 4 * (p.nseq + 1) : 0);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
