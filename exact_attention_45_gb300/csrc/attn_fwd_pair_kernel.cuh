@@ -18,11 +18,15 @@
 //   O += P V    one M = 256, N = 256 pair MMA per 16 keys: P from each CTA's
 //               TMEM, V's channels split 128 / 128 between the CTAs.
 // Per CTA, TMEM holds two S buffers (2 x 128 columns) and O (256 columns), so
-// S of block j+1 is computed while the softmax turns block j into P. Shared
-// memory per CTA (16-bit): Q 64 KB + 2 ring slots x (K half 32 KB + V half
-// 32 KB) + output staging 16 KB; FP8 halves the operand tiles (V comes
-// transposed, channels as rows, so both products are K-major) and keeps three
-// ring slots. FP8 follows the two-tile kernel's FP8 path: the dequantisation
+// S of block j+1 is computed while the softmax turns block j into P.
+// 16-bit: K and V halves stream through rings of their own (2 + 2 stages), a
+// K stage released as soon as its Q K^T has run and K copied two blocks ahead
+// of V, so a V copy waits for the Q K^T two blocks back instead of competing
+// with the K copies; shared memory per CTA Q 64 KB + 2 x 32 KB + 2 x 32 KB +
+// output staging 16 KB. FP8 halves the operand tiles (V comes transposed,
+// channels as rows, so both products are K-major) and streams them through
+// three shared slots, slot j holding K_j and V_{j-1}, released after step j's
+// P V (the separate rings measured 5-9 % slower there). FP8 follows the two-tile kernel's FP8 path: the dequantisation
 // scalar sq * sk of a 128 x 128 score block is folded into the softmax scale,
 // P (<= 2^8 under the lazy maximum) is rounded to e4m3, four per TMEM column,
 // and the epilogue applies V's channel scales.
@@ -31,10 +35,11 @@
 // this CTA's 128 rows (thread r owns row r = TMEM lane r); warp 4 TMA
 // producer; warp 5 allocates TMEM (both CTAs) and, in the leader, issues every
 // MMA of the pair. Barrier protocol:
-//   q_full, slot_full  (leader)  both CTAs' copies count their bytes on the
-//                      leader's barrier; only the leader posts the total;
-//   q_empty, slot_empty, s_full, o_done  (both)  multicast commits of the
-//                      leader's MMAs;
+//   q_full, k_full, v_full, slot_full  (leader)  both CTAs' copies count
+//                      their bytes on the leader's barrier; only the leader
+//                      posts the total;
+//   q_empty, k_empty, v_empty, slot_empty, s_full, o_done  (both)  multicast
+//                      commits of the leader's MMAs;
 //   p_full[2] (leader) one arrival per softmax warp of both CTAs (8) once
 //                      its P stores are complete, after the previous P V has
 //                      landed (so O is stable for the rare correction).
@@ -63,11 +68,18 @@ struct PairTraits {
   static constexpr int V_NC = ELEM == 2 ? V_COLS / 64 : 1;
   static constexpr int V_CHUNK = ELEM == 2 ? BN * 128 : V_COLS * 128;
   static constexpr int V_BYTES = BN * V_COLS * ELEM;
+  // 16-bit: separate K and V rings; FP8: shared slots {K_j, V_{j-1}}
+  static constexpr bool SHARED_SLOTS = ELEM == 1;
+  static constexpr int K_STAGES = 2, V_STAGES = 2;
+  static constexpr int K_AHEAD = 2;                   // K_{j + K_AHEAD} is copied just before V_j
+  static constexpr int SLOTS = 3;
   static constexpr int SLOT_BYTES = K_BYTES + V_BYTES;
-  static constexpr int STAGES = ELEM == 2 ? 2 : 3;
+  static constexpr int RING_BYTES = SHARED_SLOTS ? SLOTS * SLOT_BYTES : K_STAGES * K_BYTES + V_STAGES * V_BYTES;
+  static constexpr int THREADS = 192;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_SLOT = Q_BYTES;
-  static constexpr int OFF_STAGE = OFF_SLOT + STAGES * SLOT_BYTES;  // 4 softmax warps x 4 KB
+  static constexpr int OFF_K = Q_BYTES;               // K ring, or the slots
+  static constexpr int OFF_V = OFF_K + K_STAGES * K_BYTES;
+  static constexpr int OFF_STAGE = OFF_K + RING_BYTES;  // 4 softmax warps x 4 KB
   static constexpr int STAGE_BYTES = 4 * 4096;
   static constexpr int OFF_BARS = OFF_STAGE + STAGE_BYTES;
   static constexpr int BARS_BYTES = 256;
@@ -82,6 +94,7 @@ struct PairTraits {
 
 struct BarsPair {
   uint64_t q_full, q_empty;
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t slot_full[3], slot_empty[3];
   uint64_t s_full[2], p_full[2];
   uint64_t o_done;
@@ -108,7 +121,6 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
   // one shared-memory offset
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sQ = smem + T::OFF_Q;
-  uint8_t* sSlot = smem + T::OFF_SLOT;
   BarsPair* bars = reinterpret_cast<BarsPair*>(smem + T::OFF_BARS);
   int* prefix = reinterpret_cast<int*>(smem + T::OFF_PREFIX);
   volatile int* abort_flag = &bars->abort;
@@ -121,7 +133,15 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
-    for (int s = 0; s < T::STAGES; ++s) {
+    for (int s = 0; s < T::K_STAGES; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < T::V_STAGES; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int s = 0; s < T::SLOTS; ++s) {
       mbar_init(&bars->slot_full[s], 1);
       mbar_init(&bars->slot_empty[s], 1);
     }
@@ -172,7 +192,7 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       const uint32_t q_full_l = mapa_shared(&bars->q_full, 0);
-      int slot_it = 0, tile_i = 0;
+      int k_it = 0, v_it = 0, slot_it = 0, tile_i = 0;
       bool ok = true;
       for (int t = cluster_id; t < ntiles && ok; t += nclusters) {
         const Tile2 tl = get_tile(t);
@@ -187,47 +207,78 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         for (int c = 0; c < T::NC; ++c)
           tma_load_4d_pair(&tmQ, q_full_l, sQ + c * T::Q_CHUNK, c * (128 / ELEM), tl.h,
                            tl.tma_row0 + tl.sblk * SUPER_M + (int)rank * BLOCK_M, tl.tma_b);
-        // slot j: K_j (j < nkv; this CTA's 64 keys) and V_{j-1} (j >= 1; this
-        // CTA's 128 channels of all 128 keys)
-        for (int j = 0; j <= nkv; ++j, ++slot_it) {
-          const int st = slot_it % T::STAGES;
-          ok = mbar_wait(&bars->slot_empty[st], ((slot_it / T::STAGES) & 1) ^ 1, tmo, abort_flag, p.err);
-          if (!ok) break;
-          uint8_t* slot = sSlot + st * T::SLOT_BYTES;
-          const uint32_t slot_full_l = mapa_shared(&bars->slot_full[st], 0);
-          if (leader)
-            mbar_expect_tx(&bars->slot_full[st], (j < nkv ? 2 * T::K_BYTES : 0) + (j >= 1 ? 2 * T::V_BYTES : 0));
-          if (j < nkv) {
+        // K_j: this CTA's 64 keys of block j
+        auto copy_k = [&](int j, uint8_t* dst, uint32_t full_l) {
 #pragma unroll
-            for (int c = 0; c < T::NC; ++c)
-              tma_load_4d_pair(&tmK, slot_full_l, slot + c * T::K_CHUNK, c * (128 / ELEM), hk,
-                               tl.tma_row0 + j * BN + (int)rank * T::K_ROWS, tl.tma_b);
+          for (int c = 0; c < T::NC; ++c)
+            tma_load_4d_pair(&tmK, full_l, dst + c * T::K_CHUNK, c * (128 / ELEM), hk,
+                             tl.tma_row0 + j * BN + (int)rank * T::K_ROWS, tl.tma_b);
+        };
+        // V_j: this CTA's D / 2 channels of the block's 128 keys
+        auto copy_v = [&](int j, uint8_t* dst, uint32_t full_l) {
+          if constexpr (FP8) {
+            // V^T [B*Hkv][D][ldv]: 128 keys of this CTA's channel rows
+            tma_load_4d_pair(&tmV, full_l, dst, j * BN, (int)rank * T::V_COLS, tl.seq * p.Hkv + hk, 0);
+          } else {
+#pragma unroll
+            for (int c = 0; c < T::V_NC; ++c)
+              tma_load_4d_pair(&tmV, full_l, dst + c * T::V_CHUNK, (int)rank * T::V_COLS + c * 64, hk,
+                               tl.tma_row0 + j * BN, tl.tma_b);
           }
-          if (j >= 1) {
-            if constexpr (FP8) {
-              // V^T [B*Hkv][D][ldv]: 128 keys of this CTA's channel rows
-              tma_load_4d_pair(&tmV, slot_full_l, slot + T::K_BYTES, (j - 1) * BN, (int)rank * T::V_COLS,
-                               tl.seq * p.Hkv + hk, 0);
-            } else {
-#pragma unroll
-              for (int c = 0; c < T::V_NC; ++c)
-                tma_load_4d_pair(&tmV, slot_full_l, slot + T::K_BYTES + c * T::V_CHUNK,
-                                 (int)rank * T::V_COLS + c * 64, hk, tl.tma_row0 + (j - 1) * BN, tl.tma_b);
-            }
+        };
+        if constexpr (T::SHARED_SLOTS) {
+          // slot j: K_j (j < nkv) and V_{j-1} (j >= 1)
+          for (int j = 0; j <= nkv; ++j, ++slot_it) {
+            const int st = slot_it % T::SLOTS;
+            ok = mbar_wait(&bars->slot_empty[st], ((slot_it / T::SLOTS) & 1) ^ 1, tmo, abort_flag, p.err);
+            if (!ok) break;
+            uint8_t* slot = smem + T::OFF_K + st * T::SLOT_BYTES;
+            const uint32_t full_l = mapa_shared(&bars->slot_full[st], 0);
+            if (leader)
+              mbar_expect_tx(&bars->slot_full[st], (j < nkv ? 2 * T::K_BYTES : 0) + (j >= 1 ? 2 * T::V_BYTES : 0));
+            if (j < nkv) copy_k(j, slot, full_l);
+            if (j >= 1) copy_v(j - 1, slot + T::K_BYTES, full_l);
+          }
+        } else {
+          auto load_k = [&](int j) -> bool {
+            const int ks = k_it % T::K_STAGES;
+            if (!mbar_wait(&bars->k_empty[ks], ((k_it / T::K_STAGES) & 1) ^ 1, tmo, abort_flag, p.err)) return false;
+            if (leader) mbar_expect_tx(&bars->k_full[ks], 2 * T::K_BYTES);
+            copy_k(j, smem + T::OFF_K + ks * T::K_BYTES, mapa_shared(&bars->k_full[ks], 0));
+            ++k_it;
+            return true;
+          };
+          auto load_v = [&](int j) -> bool {
+            const int vs = v_it % T::V_STAGES;
+            if (!mbar_wait(&bars->v_empty[vs], ((v_it / T::V_STAGES) & 1) ^ 1, tmo, abort_flag, p.err)) return false;
+            if (leader) mbar_expect_tx(&bars->v_full[vs], 2 * T::V_BYTES);
+            copy_v(j, smem + T::OFF_V + vs * T::V_BYTES, mapa_shared(&bars->v_full[vs], 0));
+            ++v_it;
+            return true;
+          };
+          // the order the MMAs consume them, K running K_AHEAD blocks ahead
+          for (int j = 0; j < min(T::K_AHEAD, nkv) && ok; ++j) ok = load_k(j);
+          for (int j = 0; j < nkv && ok; ++j) {
+            if (j + T::K_AHEAD < nkv) ok = load_k(j + T::K_AHEAD);
+            if (ok) ok = load_v(j);
           }
         }
       }
       // the leader's barriers count both CTAs' copies: never leave with one in
       // flight (already complete on the normal path)
       if (leader) {
-        for (int it = (slot_it > T::STAGES ? slot_it - T::STAGES : 0); it < slot_it; ++it)
-          mbar_wait_drain(&bars->slot_full[it % T::STAGES], (it / T::STAGES) & 1, tmo, p.err);
+        for (int it = (k_it > T::K_STAGES ? k_it - T::K_STAGES : 0); it < k_it; ++it)
+          mbar_wait_drain(&bars->k_full[it % T::K_STAGES], (it / T::K_STAGES) & 1, tmo, p.err);
+        for (int it = (v_it > T::V_STAGES ? v_it - T::V_STAGES : 0); it < v_it; ++it)
+          mbar_wait_drain(&bars->v_full[it % T::V_STAGES], (it / T::V_STAGES) & 1, tmo, p.err);
+        for (int it = (slot_it > T::SLOTS ? slot_it - T::SLOTS : 0); it < slot_it; ++it)
+          mbar_wait_drain(&bars->slot_full[it % T::SLOTS], (it / T::SLOTS) & 1, tmo, p.err);
         if (tile_i > 0) mbar_wait_drain(&bars->q_full, (tile_i - 1) & 1, tmo, p.err);
       }
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer (leader only)
-    // Per slot j: S(j) = Q K_j^T into S buffer (j-th S overall) & 1, then
+    // Step j: S(j) = Q K_j^T into S buffer (j-th S overall) & 1, then
     // O += P(j-1) V_{j-1} once both CTAs' P(j-1) is stored, so the tensor core
     // computes the next scores while the softmax warps work.
     if (leader && lane == 0) {
@@ -237,8 +288,8 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       constexpr int PV_STEPS = BN * ELEM / 32;             // 32-byte K steps of P V
       constexpr uint16_t both = 3;
       const uint32_t qa = smem_u32(sQ);
-      const uint32_t slot_a = smem_u32(sSlot);
-      int slot_it = 0, tile_i = 0, s_it = 0, pv_it = 0;
+      const uint32_t k_a = smem_u32(smem + T::OFF_K), v_a = smem_u32(smem + T::OFF_V);
+      int k_it = 0, v_it = 0, slot_it = 0, tile_i = 0, s_it = 0, pv_it = 0;
       bool ok = true;
       for (int t = cluster_id; t < ntiles && ok; t += nclusters) {
         const Tile2 tl = get_tile(t);
@@ -248,13 +299,21 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         ++tile_i;
         if (!ok) break;
         for (int j = 0; j <= nkv && ok; ++j, ++slot_it) {
-          const int st = slot_it % T::STAGES;
-          const uint32_t kb = slot_a + st * T::SLOT_BYTES;
-          const uint32_t vb = kb + T::K_BYTES;
-          ok = mbar_wait(&bars->slot_full[st], (slot_it / T::STAGES) & 1, tmo, abort_flag, p.err);
-          if (!ok) break;
-          tc_fence_after();
+          // shared slots: K_j and V_{j-1} arrive on one barrier
+          const int st = slot_it % T::SLOTS;
+          if constexpr (T::SHARED_SLOTS) {
+            ok = mbar_wait(&bars->slot_full[st], (slot_it / T::SLOTS) & 1, tmo, abort_flag, p.err);
+            if (!ok) break;
+            tc_fence_after();
+          }
           if (j < nkv) {
+            const int ks = k_it % T::K_STAGES;
+            const uint32_t kb = T::SHARED_SLOTS ? k_a + st * T::SLOT_BYTES : k_a + ks * T::K_BYTES;
+            if constexpr (!T::SHARED_SLOTS) {
+              ok = mbar_wait(&bars->k_full[ks], (k_it / T::K_STAGES) & 1, tmo, abort_flag, p.err);
+              if (!ok) break;
+              tc_fence_after();
+            }
             const uint32_t s_tmem = tmem + T::TMEM_S + (s_it & 1) * BN;
 #pragma unroll
             for (int k = 0; k < S_STEPS; ++k) {
@@ -268,11 +327,18 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                                  k > 0 ? 1u : 0u);
             }
             umma_commit_pair(&bars->s_full[s_it & 1], both);
+            if constexpr (!T::SHARED_SLOTS) umma_commit_pair(&bars->k_empty[ks], both);
+            if (j == nkv - 1) umma_commit_pair(&bars->q_empty, both);
             ++s_it;
+            ++k_it;
           }
           if (j >= 1) {
             // P(j-1) lives in the S buffer of the pv_it-th S
+            const int vs = v_it % T::V_STAGES;
+            const uint32_t vb = T::SHARED_SLOTS ? k_a + st * T::SLOT_BYTES + T::K_BYTES : v_a + vs * T::V_BYTES;
             ok = mbar_wait_cluster(&bars->p_full[pv_it & 1], (pv_it >> 1) & 1, tmo, abort_flag, p.err);
+            if constexpr (!T::SHARED_SLOTS)
+              if (ok) ok = mbar_wait(&bars->v_full[vs], (v_it / T::V_STAGES) & 1, tmo, abort_flag, p.err);
             if (!ok) break;
             tc_fence_after();
             const uint32_t a_tmem = tmem + T::TMEM_S + (pv_it & 1) * BN;
@@ -287,10 +353,11 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                                  idesc_o, (j > 1 || k > 0) ? 1u : 0u);
             }
             umma_commit_pair(&bars->o_done, both);
+            if constexpr (!T::SHARED_SLOTS) umma_commit_pair(&bars->v_empty[vs], both);
             ++pv_it;
+            ++v_it;
           }
-          umma_commit_pair(&bars->slot_empty[st], both);
-          if (j == nkv - 1) umma_commit_pair(&bars->q_empty, both);
+          if constexpr (T::SHARED_SLOTS) umma_commit_pair(&bars->slot_empty[st], both);
         }
       }
       umma_commit_pair(&bars->mma_done, 1);
