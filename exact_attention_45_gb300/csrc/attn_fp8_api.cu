@@ -150,7 +150,7 @@ int attn_fp8_prepass(const void* q, const void* k, const void* v, void* q8, void
   a.err = err;
   Prepass128Maps maps;
   const Prepass128Maps* mp = nullptr;
-  if (d == 128) {
+  if (d == 128 || (d == 256 && mode == ATTN_FP8_PER_BLOCK)) {
     if ((rc = api_make_map(&maps.in_q, false, q, d, H, N, B, 64, 128))) return rc;
     if ((rc = api_make_map(&maps.in_k, false, k, d, Hkv, N, B, 64, 128))) return rc;
     if ((rc = api_make_map(&maps.in_v, false, v, d, Hkv, N, B, 64, 128))) return rc;

@@ -386,10 +386,12 @@ __global__ void __launch_bounds__(1024) varlen_block_offsets_kernel(const int* c
 // One CTA = one 128-row block of Q or K; thread r owns row r.
 constexpr int QK128_SMEM = 1024 + 2 * 16384 + 16384;   // alignment + bf16 tile + code tile
 
-__device__ __forceinline__ void butterfly_pairs64(float (&x)[64], int h) {
-  // stage with span h >= 2: pairs (i, i+h) and (i+1, i+1+h) share one f32x2 op
+// Butterfly stage with span h >= 2 over E elements: pairs (i, i+h) and
+// (i+1, i+1+h) share one f32x2 op.
+template <int E>
+__device__ __forceinline__ void butterfly_pairs(float (&x)[E], int h) {
 #pragma unroll
-  for (int i = 0; i < 64; i += 2) {
+  for (int i = 0; i < E; i += 2) {
     if ((i & h) == 0) {
       const uint64_t a = f2_pack(x[i], x[i + 1]);
       const uint64_t b = f2_pack(x[i + h], x[i + h + 1]);
@@ -484,11 +486,11 @@ __global__ void __launch_bounds__(256, 3) qk128_kernel(const __grid_constant__ C
       x[i] = __fadd_rn(p0, p1);
       x[i + 1] = __fsub_rn(p0, p1);
     }
-    butterfly_pairs64(x, 2);
-    butterfly_pairs64(x, 4);
-    butterfly_pairs64(x, 8);
-    butterfly_pairs64(x, 16);
-    butterfly_pairs64(x, 32);
+    butterfly_pairs<64>(x, 2);
+    butterfly_pairs<64>(x, 4);
+    butterfly_pairs<64>(x, 8);
+    butterfly_pairs<64>(x, 16);
+    butterfly_pairs<64>(x, 32);
     // span 64: (x_i, x_{i+64}) -> (x_i + x_{i+64}, x_i - x_{i+64}); half 0 holds x_i
 #pragma unroll
     for (int i = 0; i < 64; ++i) {
@@ -666,30 +668,40 @@ __global__ void __launch_bounds__(128) v128_kernel(const __grid_constant__ CUten
   }
 }
 
-// ---------------------------------------------------------------- head dim 128, persistent (block scales)
+// ---------------------------------------------------------------- head dims 128 and 256, persistent (block scales)
 // Two persistent launches replace the per-block kernels for fixed-length
-// block quantisation at head dim 128 (two CTAs of 8 warps per SM; tiles of
-// 128 rows x 128 channels arrive by TMA into a ring; thread 0 issues the copy
-// of tile k + stages as soon as the CTA barrier that follows the reads of
-// tile k has passed, so no producer warp takes registers away):
-//  prep128_main_kernel: work list ordered by 128-row block (batch, block) and
+// block quantisation at head dims 128 and 256 (tiles of 128 rows x D channels
+// arrive by TMA into a ring, 64-channel boxes; thread 0 issues the copy of
+// tile k + stages as soon as the CTA barrier that follows the reads of tile k
+// has passed, so no producer warp takes registers away; two CTAs of 8 warps
+// per SM at D = 128, one at D = 256):
+//  prep_main_kernel: work list ordered by 128-row block (batch, block) and
 //    inside it [Q heads][K heads][V heads], so the V tiles (per-channel amax,
 //    atomicMax into sv) keep HBM busy while other CTAs do the Q/K arithmetic:
 //    sign flips, Walsh-Hadamard butterflies, block amax -> scale, e4m3 codes
-//    stored from registers (each thread writes its 64-byte half row). The Q/K
+//    stored from registers (each thread writes its half row). The Q/K
 //    arithmetic bounds this kernel.
-//  prep128_vcodes_kernel: re-reads the V tiles (part of V is still in L2) and
+//  prep_vcodes_kernel: re-reads the V tiles (part of V is still in L2) and
 //    writes the codes transposed (keys contiguous): each thread turns 4 rows x
-//    16 channels into 16 words of 4 keys by byte permutes in a swizzled code
-//    tile that leaves by a TMA store.
-constexpr int P128_THREADS = 256;
-constexpr int P128M_STAGES = 3;                                 // main kernel ring
-constexpr int P128M_SMEM = 1024 + P128M_STAGES * 32768;
-constexpr int P128V_STAGES = 2;                                 // V codes kernel ring
-constexpr int P128V_SMEM = 1024 + P128V_STAGES * 32768 + 2 * 16384;   // + two code tiles
+//    8 channels of each 64-channel chunk into words of 4 keys by byte
+//    permutes in a swizzled code tile that leaves by TMA stores (128 channel
+//    rows each).
+constexpr int P_THREADS = 256;
+template <int D>
+struct PrepTraits {
+  static constexpr int TILE = ROWS * D * 2;                 // bf16 tile bytes
+  static constexpr int NCH = D / 64;                        // 64-channel boxes of 16 KB
+  static constexpr int MAIN_STAGES = 3;
+  static constexpr int V_STAGES = 2;
+  static constexpr int MAIN_SMEM = 1024 + MAIN_STAGES * TILE;
+  static constexpr int CODE_TILE = D * ROWS;                // u8 [D channels][128 keys]
+  static constexpr int V_SMEM = 1024 + V_STAGES * TILE + 2 * CODE_TILE;
+  static constexpr int MIN_CTAS = D == 128 ? 2 : 1;
+  static constexpr int E = D / 2;                           // Q/K elements per thread (two threads per row)
+};
 
 template <int S>
-struct P128Ring {
+struct PrepRing {
   uint64_t full[S];
   int abort;
 };
@@ -699,7 +711,7 @@ enum : int { ORDER_MAIN = 0, ORDER_V = 1 };
 // item -> kind (0 Q, 1 K, 2 V), batch, head, 128-row block; by (batch, row
 // block), heads fastest. ORDER_MAIN: [Q heads][K heads][V heads] per row
 // block; ORDER_V: V heads only.
-__device__ __forceinline__ void p128_item(const PrepassArgs& a, int id, int order, int& kind, int& b, int& head,
+__device__ __forceinline__ void prep_item(const PrepassArgs& a, int id, int order, int& kind, int& b, int& head,
                                           int& blk) {
   const int per = order == ORDER_V ? a.Hkv : a.H + 2 * a.Hkv;
   const int rb = id / per;
@@ -713,40 +725,47 @@ __device__ __forceinline__ void p128_item(const PrepassArgs& a, int id, int orde
 }
 
 // Copy of the CTA's k-th tile (item blockIdx.x + k * gridDim.x) into stage k % S.
-template <int S>
-__device__ __forceinline__ void p128_load(const PrepassArgs& a, P128Ring<S>& sh, uint8_t* ring, int k, int total,
+template <int D, int S>
+__device__ __forceinline__ void prep_load(const PrepassArgs& a, PrepRing<S>& sh, uint8_t* ring, int k, int total,
                                           int order, const CUtensorMap* mq, const CUtensorMap* mk,
                                           const CUtensorMap* mv) {
+  using P = PrepTraits<D>;
   const int id = blockIdx.x + k * gridDim.x;
   if (id >= total) return;
   int kind, b, head, blk;
-  p128_item(a, id, order, kind, b, head, blk);
+  prep_item(a, id, order, kind, b, head, blk);
   const CUtensorMap* m = kind == 0 ? mq : (kind == 1 ? mk : mv);
   const int st = k % S;
-  uint8_t* tile = ring + st * 32768;
-  mbar_expect_tx(&sh.full[st], 32768);
-  tma_load_4d(m, &sh.full[st], tile, 0, head, blk * ROWS, b);
-  tma_load_4d(m, &sh.full[st], tile + 16384, 64, head, blk * ROWS, b);
+  uint8_t* tile = ring + st * P::TILE;
+  mbar_expect_tx(&sh.full[st], P::TILE);
+#pragma unroll
+  for (int c = 0; c < P::NCH; ++c) tma_load_4d(m, &sh.full[st], tile + c * 16384, c * 64, head, blk * ROWS, b);
 }
 
 // On the way out after an abort: wait (bounded) for copies still in flight.
 template <int S>
-__device__ __forceinline__ void p128_drain(const PrepassArgs& a, P128Ring<S>& sh, int k_done, int total) {
+__device__ __forceinline__ void prep_drain(const PrepassArgs& a, PrepRing<S>& sh, int k_done, int total) {
   for (int k = k_done; k < k_done + S; ++k)
     if ((int)blockIdx.x + k * (int)gridDim.x < total)
       mbar_wait_drain(&sh.full[k % S], (k / S) & 1, a.timeout_ns, a.err);
 }
 
-__global__ void __launch_bounds__(P128_THREADS, 2) prep128_main_kernel(
+template <int D>
+__global__ void __launch_bounds__(P_THREADS, PrepTraits<D>::MIN_CTAS) prep_main_kernel(
     const __grid_constant__ CUtensorMap in_q, const __grid_constant__ CUtensorMap in_k,
     const __grid_constant__ CUtensorMap in_v, const PrepassArgs a) {
-  constexpr int S = P128M_STAGES;
+  using P = PrepTraits<D>;
+  constexpr int S = P::MAIN_STAGES;
+  constexpr int E = P::E;
+  constexpr int U = D / 8;                         // 16-byte units of a row (8 channels each)
+  constexpr int G = P_THREADS / U;                 // row groups of the V amax
+  constexpr int GR = ROWS / G;                     // rows per group
   extern __shared__ uint8_t raw[];
-  uint8_t* ring = raw + ((1024 - (smem_u32(raw) & 1023)) & 1023);   // stages x 2 x [128 rows][128 B], swizzled
-  __shared__ P128Ring<S> sh;
+  uint8_t* ring = raw + ((1024 - (smem_u32(raw) & 1023)) & 1023);   // stages x NCH x [128 rows][128 B], swizzled
+  __shared__ PrepRing<S> sh;
   __shared__ float red[2][8];
-  __shared__ float vred[2][8][128];                // V amax: per warp (16 rows) and channel
-  __shared__ uint32_t xmask[64];
+  __shared__ float vred[2][8][D];                  // V amax: per warp and channel
+  __shared__ uint32_t xmask[D / 2];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int total = (a.B * a.H + 2 * a.B * a.Hkv) * a.nblk;
   if (t == 0) {
@@ -754,16 +773,16 @@ __global__ void __launch_bounds__(P128_THREADS, 2) prep128_main_kernel(
     sh.abort = 0;
     fence_mbar_init();
   }
-  if (t < 64) {
+  if (t < D / 2) {
     // sign flips as XOR masks on bf16 pairs (elements 2t, 2t+1)
     const uint32_t w = a.sign_bits[(2 * t) >> 5] >> ((2 * t) & 31);
     xmask[t] = a.rotate ? (((w & 1u) << 15) | (((w >> 1) & 1u) << 31)) : 0u;
   }
   __syncthreads();
   if (t == 0) {
-    for (int k = 0; k < S; ++k) p128_load(a, sh, ring, k, total, ORDER_MAIN, &in_q, &in_k, &in_v);
+    for (int k = 0; k < S; ++k) prep_load<D, S>(a, sh, ring, k, total, ORDER_MAIN, &in_q, &in_k, &in_v);
   }
-  // Q/K: lanes 2i, 2i+1 of a warp hold elements 0-63 / 64-127 of row warp * 16 + i
+  // Q/K: lanes 2i, 2i+1 of a warp hold elements [0, E) / [E, D) of row warp * 16 + i
   const int r = warp * 16 + (lane >> 1);
   const int half = lane & 1;
   int k = 0;
@@ -774,23 +793,23 @@ __global__ void __launch_bounds__(P128_THREADS, 2) prep128_main_kernel(
     ok = mbar_wait(&sh.full[st], (k / S) & 1, a.timeout_ns, &sh.abort, a.err);
     if (!ok) break;
     int kind, b, head, blk;
-    p128_item(a, id, ORDER_MAIN, kind, b, head, blk);
-    const uint8_t* tile = ring + st * 32768;
+    prep_item(a, id, ORDER_MAIN, kind, b, head, blk);
+    const uint8_t* tile = ring + st * P::TILE;
     const int row0 = blk * ROWS;
     const int nvalid = min(ROWS, a.N - row0);
     if (kind == 2) {
-      // V: per-channel amax of the block's valid rows. Thread t reads channels
-      // 8*o .. 8*o+7 (o = t % 16: 16-byte unit o % 8 of chunk o / 8) of rows
-      // 8*g .. 8*g+7 (g = t / 16); lanes t and t^16 combine their rows by a
-      // shuffle, the 8 warps through shared memory.
-      const int o = t & 15, g8 = t >> 4;
+      // V: per-channel amax of the block's valid rows. Thread t reads the 8
+      // channels of unit o = t % U (16-byte unit o % 8 of chunk o / 8) in
+      // rows GR * g .. + GR - 1 (g = t / U); lanes of a warp with the same
+      // unit combine by a shuffle (D = 128), the 8 warps through shared memory.
+      const int o = t % U, g = t / U;
       const uint8_t* base = tile + (o >> 3) * 16384;
       float cm[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) cm[i] = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int n = g8 * 8 + i;
+      for (int i = 0; i < GR; ++i) {
+        const int n = g * GR + i;
         if (n < nvalid) {
           const uint4 v = *reinterpret_cast<const uint4*>(base + n * 128 + (((o & 7) ^ (n & 7)) << 4));
           const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
@@ -801,63 +820,64 @@ __global__ void __launch_bounds__(P128_THREADS, 2) prep128_main_kernel(
           }
         }
       }
+      if constexpr (U < 32) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], 16));
-      if (lane < 16) {
+        for (int i = 0; i < 8; ++i) cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], 16));
+      }
+      if (lane < U) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) vred[pb][warp][8 * o + i] = cm[i];
       }
       __syncthreads();                                  // every thread has read the tile
-      if (t == 0) p128_load(a, sh, ring, k + S, total, ORDER_MAIN, &in_q, &in_k, &in_v);
-      if (t < 128) {
+      if (t == 0) prep_load<D, S>(a, sh, ring, k + S, total, ORDER_MAIN, &in_q, &in_k, &in_v);
+      if (t < D) {
         float m = vred[pb][0][t];
 #pragma unroll
         for (int w8 = 1; w8 < 8; ++w8) m = fmaxf(m, vred[pb][w8][t]);
-        atomicMax(reinterpret_cast<unsigned int*>(a.sv + ((size_t)b * a.Hkv + head) * 128 + t), __float_as_uint(m));
+        atomicMax(reinterpret_cast<unsigned int*>(a.sv + ((size_t)b * a.Hkv + head) * D + t), __float_as_uint(m));
       }
       continue;
     }
     // Q/K: rotate, block amax -> scale, codes
     const bool is_q = kind == 0;
-    float x[64];
-    const uint8_t* src = tile + half * 16384 + r * 128;
+    float x[E];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint4 v = *reinterpret_cast<const uint4*>(src + ((j ^ (r & 7)) << 4));
+    for (int j = 0; j < E / 8; ++j) {
+      // 16-byte unit j of this half row: chunk half * E / 64 + j / 8, unit j % 8
+      const uint8_t* src = tile + (half * (E / 64) + (j >> 3)) * 16384 + r * 128;
+      const uint4 v = *reinterpret_cast<const uint4*>(src + (((j & 7) ^ (r & 7)) << 4));
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int e = j * 8 + 2 * i;
-        const uint32_t u = w[i] ^ xmask[(half * 64 + e) >> 1];
+        const uint32_t u = w[i] ^ xmask[(half * E + e) >> 1];
         x[e] = __uint_as_float(u << 16);
         x[e + 1] = __uint_as_float(u & 0xFFFF0000u);
       }
     }
     if (a.rotate) {
+      // spans 1 .. E/2 inside the thread, span E across the lane pair
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
+      for (int i = 0; i < E; i += 2) {
         const float p0 = x[i], p1 = x[i + 1];
         x[i] = __fadd_rn(p0, p1);
         x[i + 1] = __fsub_rn(p0, p1);
       }
-      butterfly_pairs64(x, 2);
-      butterfly_pairs64(x, 4);
-      butterfly_pairs64(x, 8);
-      butterfly_pairs64(x, 16);
-      butterfly_pairs64(x, 32);
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
+      for (int h = 2; h < E; h *= 2) butterfly_pairs<E>(x, h);
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
         const float o = __shfl_xor_sync(0xffffffffu, x[i], 1);
         x[i] = half ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
       }
       const uint64_t c2 = f2_pack(a.inv_sqrt_d, a.inv_sqrt_d);
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) f2_unpack(f2_mul(f2_pack(x[i], x[i + 1]), c2), x[i], x[i + 1]);
+      for (int i = 0; i < E; i += 2) f2_unpack(f2_mul(f2_pack(x[i], x[i + 1]), c2), x[i], x[i + 1]);
     }
     float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
     if (r < nvalid) {
 #pragma unroll
-      for (int i = 0; i < 64; i += 4) {
+      for (int i = 0; i < E; i += 4) {
         m0 = fmaxf(m0, fabsf(x[i]));
         m1 = fmaxf(m1, fabsf(x[i + 1]));
         m2 = fmaxf(m2, fabsf(x[i + 2]));
@@ -869,7 +889,7 @@ __global__ void __launch_bounds__(P128_THREADS, 2) prep128_main_kernel(
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     if (lane == 0) red[pb][warp] = amax;
     __syncthreads();                                    // every thread has read the tile
-    if (t == 0) p128_load(a, sh, ring, k + S, total, ORDER_MAIN, &in_q, &in_k, &in_v);
+    if (t == 0) prep_load<D, S>(a, sh, ring, k + S, total, ORDER_MAIN, &in_q, &in_k, &in_v);
     amax = red[pb][0];
 #pragma unroll
     for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[pb][w]);
@@ -882,7 +902,7 @@ __global__ void __launch_bounds__(P128_THREADS, 2) prep128_main_kernel(
     if (dv.fast) {
       const uint64_t r2 = f2_pack(dv.r, dv.r), ns2 = f2_pack(-dv.s, -dv.s);
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
+      for (int i = 0; i < E; i += 2) {
         const uint64_t xv = f2_pack(x[i], x[i + 1]);
         const uint64_t q0 = f2_mul(xv, r2);
         const uint64_t e = f2_fma(q0, ns2, xv);
@@ -890,14 +910,14 @@ __global__ void __launch_bounds__(P128_THREADS, 2) prep128_main_kernel(
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) x[i] = __fdiv_rn(x[i], dv.s);
+      for (int i = 0; i < E; ++i) x[i] = __fdiv_rn(x[i], dv.s);
     }
     if (r < nvalid) {
       const int Hx = is_q ? a.H : a.Hkv;
-      uint4* dst = reinterpret_cast<uint4*>((is_q ? a.q8 : a.k8) + (((size_t)b * a.N + row0 + r) * Hx + head) * 128 +
-                                            half * 64);
+      uint4* dst = reinterpret_cast<uint4*>((is_q ? a.q8 : a.k8) + (((size_t)b * a.N + row0 + r) * Hx + head) * D +
+                                            half * E);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < E / 16; ++j) {
         const int e = j * 16;
         dst[j] = make_uint4(e4m3x4(x[e], x[e + 1], x[e + 2], x[e + 3]), e4m3x4(x[e + 4], x[e + 5], x[e + 6], x[e + 7]),
                             e4m3x4(x[e + 8], x[e + 9], x[e + 10], x[e + 11]),
@@ -905,18 +925,19 @@ __global__ void __launch_bounds__(P128_THREADS, 2) prep128_main_kernel(
       }
     }
   }
-  if (t == 0 && !ok) p128_drain(a, sh, k, total);
+  if (t == 0 && !ok) prep_drain(a, sh, k, total);
 }
 
-__global__ void __launch_bounds__(P128_THREADS, 2) prep128_vcodes_kernel(const __grid_constant__ CUtensorMap in_v,
-                                                                          const __grid_constant__ CUtensorMap out_vt,
-                                                                          const PrepassArgs a) {
-  constexpr int S = P128V_STAGES;
+template <int D>
+__global__ void __launch_bounds__(P_THREADS, PrepTraits<D>::MIN_CTAS) prep_vcodes_kernel(
+    const __grid_constant__ CUtensorMap in_v, const __grid_constant__ CUtensorMap out_vt, const PrepassArgs a) {
+  using P = PrepTraits<D>;
+  constexpr int S = P::V_STAGES;
   extern __shared__ uint8_t raw[];
-  uint8_t* ring = raw + ((1024 - (smem_u32(raw) & 1023)) & 1023);   // stages x 2 x [128 rows][128 B], swizzled
-  uint8_t* codes = ring + S * 32768;               // 2 x [128 channels][128 keys] u8, 128-byte swizzled
-  __shared__ P128Ring<S> sh;
-  __shared__ float vdiv_s[2][128], vdiv_r[2][128];  // per-channel scale and RN(1/scale)
+  uint8_t* ring = raw + ((1024 - (smem_u32(raw) & 1023)) & 1023);   // stages x NCH x [128 rows][128 B], swizzled
+  uint8_t* codes = ring + S * P::TILE;             // 2 x [D channels][128 keys] u8, 128-byte swizzled
+  __shared__ PrepRing<S> sh;
+  __shared__ float vdiv_s[2][D], vdiv_r[2][D];     // per-channel scale and RN(1/scale)
   __shared__ int vdiv_slow[2];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int total = a.B * a.Hkv * a.nblk;
@@ -928,10 +949,10 @@ __global__ void __launch_bounds__(P128_THREADS, 2) prep128_vcodes_kernel(const _
   if (t == 32) tma_prefetch_desc(&out_vt);
   __syncthreads();
   if (t == 0) {
-    for (int k = 0; k < S; ++k) p128_load(a, sh, ring, k, total, ORDER_V, &in_v, &in_v, &in_v);
+    for (int k = 0; k < S; ++k) prep_load<D, S>(a, sh, ring, k, total, ORDER_V, &in_v, &in_v, &in_v);
   }
-  // thread (warp w, lane q): rows 4q .. 4q+3 and the 16 channels of 16-byte
-  // unit o = (w + q) % 8 in both 64-channel chunks; over the CTA every (row
+  // thread (warp w, lane q): rows 4q .. 4q+3 and the 8 channels of 16-byte
+  // unit o = (w + q) % 8 in every 64-channel chunk; over the CTA every (row
   // quad, unit) pair is taken once, and both the unit loads and the
   // transposed 32-bit stores are free of shared-memory bank conflicts
   const int q = lane, o = (warp + lane) & 7;
@@ -943,26 +964,26 @@ __global__ void __launch_bounds__(P128_THREADS, 2) prep128_vcodes_kernel(const _
     ok = mbar_wait(&sh.full[st], (k / S) & 1, a.timeout_ns, &sh.abort, a.err);
     if (!ok) break;
     int kind, b, head, blk;
-    p128_item(a, id, ORDER_V, kind, b, head, blk);
-    const uint8_t* tile = ring + st * 32768;
+    prep_item(a, id, ORDER_V, kind, b, head, blk);
+    const uint8_t* tile = ring + st * P::TILE;
     const int nvalid = min(ROWS, a.N - blk * ROWS);
-    if (t < 128) {
+    if (t < D) {
       // divisor of channel t: scale from the channel amax, and its reciprocal
       const Divider dv(scale_from_amax(
-          __uint_as_float(*reinterpret_cast<volatile const unsigned int*>(a.sv + ((size_t)b * a.Hkv + head) * 128 + t))));
+          __uint_as_float(*reinterpret_cast<volatile const unsigned int*>(a.sv + ((size_t)b * a.Hkv + head) * D + t))));
       vdiv_s[pb][t] = dv.s;
       vdiv_r[pb][t] = dv.r;
       if (t == 0) vdiv_slow[pb] = 0;
     }
-    uint8_t* ct = codes + (n_v & 1) * 16384;
+    uint8_t* ct = codes + (n_v & 1) * P::CODE_TILE;
     ++n_v;
-    if (t == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // ct's previous store has read it
+    if (t == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // ct's previous stores have read it
     __syncthreads();
-    if (t < 128 && !Divider(vdiv_s[pb][t]).fast) vdiv_slow[pb] = 1;
+    if (t < D && !Divider(vdiv_s[pb][t]).fast) vdiv_slow[pb] = 1;
     __syncthreads();
     const bool slow = vdiv_slow[pb] != 0;
 #pragma unroll
-    for (int ck = 0; ck < 2; ++ck) {
+    for (int ck = 0; ck < P::NCH; ++ck) {
       const int c0 = ck * 64 + 8 * o;                 // first of this thread's 8 channels
       uint32_t cw[4][4];                              // [row i][channel pair m]: e4m3 codes (lo, hi)
 #pragma unroll
@@ -1006,13 +1027,15 @@ __global__ void __launch_bounds__(P128_THREADS, 2) prep128_vcodes_kernel(const _
     fence_proxy_async_smem();
     __syncthreads();                                  // tile read, code tile written
     if (t == 0) {
-      p128_load(a, sh, ring, k + S, total, ORDER_V, &in_v, &in_v, &in_v);
-      tma_store_4d(&out_vt, ct, blk * ROWS, 0, b * a.Hkv + head, 0);
+      prep_load<D, S>(a, sh, ring, k + S, total, ORDER_V, &in_v, &in_v, &in_v);
+      // one bulk group per tile: 128 channel rows per store
+#pragma unroll
+      for (int h = 0; h < D / 128; ++h) tma_store_4d(&out_vt, ct + h * 16384, blk * ROWS, h * 128, b * a.Hkv + head, 0);
       tma_store_commit();
     }
   }
   if (t == 0) {
-    if (!ok) p128_drain(a, sh, k, total);
+    if (!ok) prep_drain(a, sh, k, total);
     tma_store_wait_all();
   }
 }
@@ -1076,6 +1099,21 @@ cudaError_t launch_fp8_prepass_varlen(const PrepassArgs& a, int d, const Prepass
   return cudaGetLastError();
 }
 
+template <int D>
+static cudaError_t launch_prep_persistent(const PrepassArgs& a, const Prepass128Maps& maps, int nqk, int nv,
+                                          int sm_count, cudaStream_t s) {
+  using P = PrepTraits<D>;
+  cudaError_t e = cudaFuncSetAttribute(prep_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::MAIN_SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(prep_vcodes_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::V_SMEM);
+  if (e != cudaSuccess) return e;
+  const int g1 = min(nqk + nv, P::MIN_CTAS * sm_count), g2 = min(nv, P::MIN_CTAS * sm_count);
+  prep_main_kernel<D><<<g1, P_THREADS, P::MAIN_SMEM, s>>>(maps.in_q, maps.in_k, maps.in_v, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  prep_vcodes_kernel<D><<<g2, P_THREADS, P::V_SMEM, s>>>(maps.in_v, maps.out_vt, a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps* maps, int sm_count,
                                cudaStream_t s) {
   const size_t nsv = a.block_mode ? (size_t)a.B * a.Hkv * d : 1;
@@ -1088,18 +1126,12 @@ cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps
   const int nqk = (a.B * a.H + a.B * a.Hkv) * a.nblk;
   const int nv = a.B * a.Hkv * a.nblk;
   const bool fast_qk = d == 128 && maps != nullptr;
-  if (fast_qk && a.block_mode) {
+  if (maps != nullptr && a.block_mode && (d == 128 || d == 256)) {
     // persistent kernels: Q/K codes and V channel amax in one pass, V codes in
     // a second one, then the amax values become scales
-    e = cudaFuncSetAttribute(prep128_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P128M_SMEM);
+    e = d == 128 ? launch_prep_persistent<128>(a, *maps, nqk, nv, sm_count, s)
+                 : launch_prep_persistent<256>(a, *maps, nqk, nv, sm_count, s);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prep128_vcodes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P128V_SMEM);
-    if (e != cudaSuccess) return e;
-    const int g1 = min(nqk + nv, 2 * sm_count), g2 = min(nv, 2 * sm_count);
-    prep128_main_kernel<<<g1, P128_THREADS, P128M_SMEM, s>>>(maps->in_q, maps->in_k, maps->in_v, a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    prep128_vcodes_kernel<<<g2, P128_THREADS, P128V_SMEM, s>>>(maps->in_v, maps->out_vt, a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     finalize_kernel<<<(int)((nsv + 255) / 256), 256, 0, s>>>(a.sq, a.sk, a.sv, (int)nsv, 0);
     return cudaGetLastError();
   }

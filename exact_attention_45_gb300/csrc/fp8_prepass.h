@@ -26,16 +26,17 @@ struct PrepassArgs {
   int* blk_off;
 };
 
-// Tensor maps of the head-dim-128 path: bf16 inputs (Q, K, V) {128, heads, N, B}
-// with 64 x 128-row boxes, e4m3 outputs {128, heads, N, B} with 128 x 128-row
-// boxes (per-tensor scales), and (fixed length) the transposed V codes {ldv,
-// 128, B * Hkv} with 128 keys x 128 channel-row boxes; 128-byte swizzle.
+// Tensor maps of the TMA-fed pre-pass kernels (head dim 128, and head dim 256
+// with block scales): bf16 inputs (Q, K, V) {d, heads, N, B} with 64 x 128-row
+// boxes, e4m3 outputs {d, heads, N, B} with 128 x 128-row boxes (per-tensor
+// scales, d = 128), and (fixed length) the transposed V codes {ldv, d,
+// B * Hkv} with 128 keys x 128 channel-row boxes; 128-byte swizzle.
 struct Prepass128Maps {
   CUtensorMap in_q, in_k, in_v, out_q, out_k, out_vt;
 };
 
 // memsets of the scale outputs, two passes of the pre-pass kernels, finalise.
-// maps: required for the fast head-dim-128 path (nullptr selects the generic one).
+// maps: required for the TMA-fed kernels (nullptr selects the generic ones).
 cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps* maps, int sm_count,
                                cudaStream_t s);
 // Packed sequences: block offsets, two passes, finalise. maps (head dim 128,

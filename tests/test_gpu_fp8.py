@@ -52,6 +52,22 @@ def test_prepass_bit_exact(d, mode, rotate):
         assert np.array_equal(pre[name].cpu().numpy(), ref[name]), name
 
 
+@pytest.mark.parametrize("d,B", [(128, 4), (256, 2)])
+def test_prepass_persistent_many_tiles_bit_exact(d, B):
+    # block scales at head dims 128 and 256 run on persistent kernels fed by a
+    # ring of TMA copies: enough 128-row tiles that every CTA goes around the
+    # ring more than once, the last block of each sequence ragged (2000 rows)
+    N, H, Hkv = 2000, 8, 4
+    q, k, v = gen.qkv_fixed(B, N, H, Hkv, d, seed=20 + d, dist="outlier")
+    pre = _prepass_gpu(q, k, v, "block", True, seed=6)
+    ref = O.fp8_prepass(q, k, v, mode="block", rotate=True, seed=6)
+    for name in ("q8", "k8", "sq", "sk", "sv"):
+        assert np.array_equal(pre[name].cpu().numpy(), ref[name]), name
+    vt = pre["vt8"].cpu().numpy()
+    assert np.array_equal(vt[..., :N], ref["vt8"])
+    assert np.all(vt[..., N:] == 0)
+
+
 def _emulated_check(B, N, H, Hkv, causal, mode, rotate, seed, rows=None, d=128):
     import exact_attention_45_gb300 as A
     q, k, v = gen.qkv_fixed(B, N, H, Hkv, d, seed=seed, dist="outlier")
