@@ -42,7 +42,10 @@
 //                      commits of the leader's MMAs;
 //   p_full[2] (leader) one arrival per softmax warp of both CTAs (8) once
 //                      its P stores are complete, after the previous P V has
-//                      landed (so O is stable for the rare correction).
+//                      landed (so O is stable for the rare correction); the
+//                      P stores are ordered before the MMAs by tcgen05.wait::st
+//                      and the tcgen05 fences on both sides of this barrier,
+//                      so its arrivals carry no cluster-scope release.
 // Every wait is bounded (timeout -> abort flag + device error word).
 #pragma once
 #include <cuda_bf16.h>
@@ -336,7 +339,7 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             // P(j-1) lives in the S buffer of the pv_it-th S
             const int vs = v_it % T::V_STAGES;
             const uint32_t vb = T::SHARED_SLOTS ? k_a + st * T::SLOT_BYTES + T::K_BYTES : v_a + vs * T::V_BYTES;
-            ok = mbar_wait_cluster(&bars->p_full[pv_it & 1], (pv_it >> 1) & 1, tmo, abort_flag, p.err);
+            ok = mbar_wait(&bars->p_full[pv_it & 1], (pv_it >> 1) & 1, tmo, abort_flag, p.err);
             if constexpr (!T::SHARED_SLOTS)
               if (ok) ok = mbar_wait(&bars->v_full[vs], (v_it / T::V_STAGES) & 1, tmo, abort_flag, p.err);
             if (!ok) break;
