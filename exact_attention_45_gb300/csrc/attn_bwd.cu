@@ -20,7 +20,10 @@
 // TMA, warp 9 lane 0 issues the MMAs. TMEM: S (128 cols, reused for dQ), dP (128), dV (d),
 // dK (d). Shared memory: K_j, V_j, two Q tiles (Q_{i+1} arrives while block i
 // runs), the dO_i tile and the bf16 P and dS tiles that feed the last three
-// products (MN-major for P^T / dS^T, K-major for dS).
+// products (MN-major for P^T / dS^T, K-major for dS). P is signalled before dS
+// is stored, so dV runs while dS is written; each warpgroup stages its half of
+// dQ in the P and dS chunks it writes itself and waits only for its own
+// previous reduction before overwriting them.
 // Per query block the MMA thread issues dP = dO_i V^T first (its TMEM columns
 // are free once the softmax warps have read the previous dP) and S = Q_i K^T
 // once the previous dQ has been read out of S's columns; dO_i is released
@@ -49,8 +52,8 @@ struct BwdTraits {
 };
 
 struct BwdBars {
-  uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, p_full, dq_full, dq_empty, dkv_full,
-      dkv_empty, done;
+  uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, p_full, ds_full, dq_full, dq_empty,
+      dkv_full, dkv_empty, done;
   uint32_t tmem_base;
   int abort;
 };
@@ -119,6 +122,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(&bars->do_empty, 1);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->p_full, BWD_COMPUTE);
+    mbar_init(&bars->ds_full, BWD_COMPUTE);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_empty, BWD_COMPUTE);
     mbar_init(&bars->dkv_full, 1);
@@ -236,6 +240,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         sdesc_mnmajor_sw128(sdo + k * 2048, T::CHUNK), id_mm, (it > 0 || k > 0) ? 1u : 0u);
           }
           umma_commit(&bars->do_empty);                   // dO_i is read by nothing after dV
+          // dS is stored while dV runs
+          ok = mbar_wait(&bars->ds_full, blk_it & 1, tmo, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             umma_f16_ss(tmem + T::T_DK, sdesc_mnmajor_sw128(sds + k * 2048, T::CHUNK),
@@ -340,30 +348,35 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
               dw[e / 2] = pack16<BF16>(d0, d1);
             }
           }
-          // the previous block's dQ reduction reads the P/dS tiles as its
-          // staging: wait for it only now, after the loads and the arithmetic
+          // this warpgroup's previous dQ reduction reads chunk c of the P and
+          // dS tiles as its staging: wait for it only now, after the loads and
+          // the arithmetic
           if (blk_it > 0) {
-            if (threadIdx.x == 0) tma_store_wait_read();
-            named_bar_sync(1, BWD_COMPUTE);
+            if (r == 0) tma_store_wait_read();
+            named_bar_sync(2 + half, 128);
           }
-          // keys c*64 .. c*64+63 fill chunk c of the row: 16-byte unit q at q ^ (r % 8)
+          // keys c*64 .. c*64+63 fill chunk c of the row: 16-byte unit q at q ^ (r % 8);
+          // P first (the dV product starts on it), then dS
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t off = c * T::CHUNK + ((q ^ (r & 7)) << 4);
-            st_shared_v4(prow + off, pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
-            st_shared_v4(dsrow + off, dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
-          }
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(prow + c * T::CHUNK + ((q ^ (r & 7)) << 4), pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+          fence_proxy_async_smem();                           // P visible to the MMAs
+          tc_fence_before();                                  // S, dP read out of TMEM
+          mbar_arrive(&bars->p_full);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(dsrow + c * T::CHUNK + ((q ^ (r & 7)) << 4), dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
         }
-        fence_proxy_async_smem();                             // P, dS visible to the MMAs
-        tc_fence_before();
-        mbar_arrive(&bars->p_full);
+        fence_proxy_async_smem();                             // dS visible to the MMAs
+        mbar_arrive(&bars->ds_full);
         // dQ_i rows: add into the fp32 accumulator
         ok = mbar_wait(&bars->dq_full, blk_it & 1, tmo, abort_flag, p.err);
         if (!ok) break;
         tc_fence_after();
-        // dQ rows (this warpgroup's D/2 columns) -> staging: chunk cc (32 fp32
-        // columns, 16 KB) row r, 16-byte unit v at v ^ (r % 8), the bulk
-        // reduction's 128-byte swizzle
+        // dQ rows (this warpgroup's D/2 columns) -> staging in the chunks of the
+        // P and dS tiles this warpgroup writes (chunk `half` of each): 32 fp32
+        // columns per 16 KB chunk, row r, 16-byte unit v at v ^ (r % 8), the
+        // bulk reduction's 128-byte swizzle
         {
           constexpr int HC = D / 2;                            // columns per warpgroup
           uint32_t qu[HC];
@@ -375,17 +388,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           mbar_arrive(&bars->dq_empty);
 #pragma unroll
           for (int v4 = 0; v4 < HC / 4; ++v4) {
-            const int cc = half * (HC / 32) + (v4 >> 3);
-            const uint32_t off = cc * T::CHUNK + ((((v4 & 7) ^ (r & 7))) << 4);
-            st_shared_v4(prow + off, qu[4 * v4], qu[4 * v4 + 1], qu[4 * v4 + 2], qu[4 * v4 + 3]);
+            const uint32_t base = (v4 >> 3) == 0 ? prow : dsrow;   // 32-column piece 0 / 1
+            const uint32_t off = half * T::CHUNK + ((((v4 & 7) ^ (r & 7))) << 4);
+            st_shared_v4(base + off, qu[4 * v4], qu[4 * v4 + 1], qu[4 * v4 + 2], qu[4 * v4 + 3]);
           }
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, BWD_COMPUTE);
-        if (threadIdx.x == 0) {
-          // rows past the sequence end fall outside the map and are dropped
-          for (int cc = 0; cc < D / 32; ++cc)
-            tma_reduce_add_4d(&tmDQ, tp + cc * T::CHUNK, cc * 32, h, i * 128, u.b);
+        named_bar_sync(2 + half, 128);
+        if (r == 0) {
+          // this warpgroup's columns half * D/2 ..; rows past the sequence end
+          // fall outside the map and are dropped
+          for (int cc = 0; cc < D / 64; ++cc)
+            tma_reduce_add_4d(&tmDQ, (cc == 0 ? tp : tds) + half * T::CHUNK, half * (D / 2) + cc * 32, h, i * 128, u.b);
           tma_store_commit();
         }
       }
@@ -421,7 +435,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_before();
       mbar_arrive(&bars->dkv_empty);
     }
-    if (threadIdx.x == 0) tma_store_wait_all();               // no reduction outlives the CTA
+    if (r == 0) tma_store_wait_all();                        // no reduction outlives the CTA
   }
 
   tc_fence_before();

@@ -2,9 +2,10 @@
 study of the pages' claim.
 
 * The FP8 forward at B=4, N=4096, H=16, d=128 (block scales + rotation,
-  outlier inputs), causal and not, and over the packed GQA configuration (8
-  sequences of 1k-32k tokens, H=32, Hkv=8, causal), against the oracle's FP8
-  emulation on >= 512 sampled rows with the bounds of the small FP8 tests.
+  outlier inputs), causal and not, at B=4, N=4096, H=8, d=256 (CTA pairs), and
+  over the packed GQA configuration (8 sequences of 1k-32k tokens, H=32,
+  Hkv=8, causal), against the oracle's FP8 emulation on >= 512 sampled rows
+  with the bounds of the small FP8 tests.
   Block-mode scales belong to one (batch or sequence, head), so the oracle
   quantises only the (batch, KV head) slices the sampled rows need; their codes
   and scales are those of the whole tensor.
@@ -88,6 +89,24 @@ def test_fp8_forward_full_size_matches_emulation(causal):
     o_ref, l_ref, flip = _emulate_fixed_rows(q, k, v, (rb, rh, ri), causal, SEED)
     _within_emulation_bounds(o_h[rb, ri, rh], l_h[rb, rh, ri], o_ref, l_ref, flip,
                              f"FP8 B{B} N{N} H{H} causal={causal}")
+
+
+def test_fp8_forward_d256_full_size_matches_emulation():
+    # head dim 256 (CTA pairs) at the FP8 sweep's N = 4096 point: B = 4, H = 8,
+    # per-block scales + rotation, outlier inputs, non-causal
+    import exact_attention_45_gb300 as A
+    B, N, H, d = 4, 4096, 8, 256
+    q, k, v = gen.qkv_fixed(B, N, H, H, d, seed=SEED, dist="outlier")
+    o, lse = A.attn_fwd_fp8_auto(q.cuda(), k.cuda(), v.cuda(), causal=False, mode="block", rotate=True,
+                                 hadamard_seed=SEED)
+    torch.cuda.synchronize()
+    assert A.attn_get_device_error() == 0
+    o_h, l_h = o.float().cpu().numpy(), lse.cpu().numpy()
+    assert np.isfinite(o_h).all() and np.isfinite(l_h).all()
+    rb, rh, ri = gen.sample_rows([N] * B, H, 512, seed=5)
+    assert rb.size >= 512
+    o_ref, l_ref, flip = _emulate_fixed_rows(q, k, v, (rb, rh, ri), False, SEED)
+    _within_emulation_bounds(o_h[rb, ri, rh], l_h[rb, rh, ri], o_ref, l_ref, flip, f"FP8 d256 B{B} N{N} H{H}")
 
 
 def _varlen_pair_rows(lengths, g, pairs, per_pair, seed):
