@@ -29,6 +29,8 @@ struct FwdParams {
   int ntiles;              // fixed: work units (set by the launcher); varlen: counted on the device
   int vt_ld;               // FP8 only: row stride (keys) of transposed V
   int fp8_block;           // FP8 only: 1 = per-block/per-channel scales, 0 = per-tensor
+  int fp8_d;               // FP8 only: head dim of the e4m3 data (0 = the kernel's); 64 runs on the
+                           // head-dim-128 kernel: the copies zero-fill channels 64-127, which are not stored
   float scale_log2;        // softmax scale * log2(e)
   const int* seqlens;      // decode only: cached keys per sequence (device, nseq)
   int num_splits;          // decode only: key-range splits per (sequence, KV head)

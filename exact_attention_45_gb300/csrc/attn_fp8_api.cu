@@ -91,7 +91,7 @@ int check_shape(int B, int H, int Hkv, int N, int d, int mode) {
 // Checks of the forward step's own arguments, made by the combined calls
 // before the pre-pass runs, so a call that is bound to fail writes nothing.
 int check_fwd_fp8_args(int d, int causal, float scale, const void* o, const float* lse) {
-  if (d != 128 && d != 256) return api_fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward is built for head dims 128 and 256");
+  if (d != 64 && d != 128 && d != 256) return api_fail(ATTN_ERR_UNSUPPORTED, "head dim not in {64,128,256}");
   if (causal != 0 && causal != 1) return api_fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
   if (!(scale > 0.f) || !std::isfinite(scale)) return api_fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
   if (!o || !lse) return api_fail(ATTN_ERR_INVALID_ARG, "null pointer");
@@ -169,7 +169,6 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* s
                  float scale, int mode, void* stream) {
   int rc = check_shape(B, H, Hkv, N, d, mode);
   if (rc) return rc;
-  if (d != 128 && d != 256) return api_fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward is built for head dims 128 and 256");
   if (causal != 0 && causal != 1) return api_fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
   if (!(scale > 0.f) || !std::isfinite(scale)) return api_fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
   if (!q8 || !k8 || !vt8 || !sq || !sk || !sv || !o || !lse) return api_fail(ATTN_ERR_INVALID_ARG, "null pointer");
@@ -182,12 +181,14 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* s
   const int ldv = attn_fp8_vt_ld(N);
   CUtensorMap mq, mk, mv, mo;
   // head dim 256 runs on CTA pairs: each CTA of a pair loads 64 keys of a
-  // 128-key block and 128 of V's channel rows
+  // 128-key block and 128 of V's channel rows. Head dim 64 runs on the
+  // head-dim-128 kernel: its 128-byte boxes reach past the 64 channels of a
+  // row (and the 64 channel rows of V^T), which the copies fill with zeros.
   const bool pair = d == 256;
   if ((rc = api_make_map(&mq, true, q8, d, H, N, B, 128, 128))) return rc;
   if ((rc = api_make_map(&mk, true, k8, d, Hkv, N, B, 128, pair ? 64 : 128))) return rc;
-  // V^T codes: [B*Hkv][d][ldv] read as boxes of (128 keys) x (channel rows)
-  if ((rc = api_make_map_rows(&mv, vt8, ldv, d, (uint64_t)B * Hkv, 128, pair ? 128 : d))) return rc;
+  // V^T codes: [B*Hkv][d][ldv] read as boxes of (128 keys) x (128 channel rows)
+  if ((rc = api_make_map_rows(&mv, vt8, ldv, d, (uint64_t)B * Hkv, 128, 128))) return rc;
   // bf16 output: 64 columns x 32 rows per bulk store (one warp's rows)
   if ((rc = api_make_map(&mo, false, o, d, H, N, B, 64, 32))) return rc;
   FwdParams p;
@@ -205,6 +206,7 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* s
   p.group = H / Hkv;
   p.vt_ld = ldv;
   p.fp8_block = mode == ATTN_FP8_PER_BLOCK;
+  p.fp8_d = d;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = api_timeout_ns();
   p.err = err;

@@ -628,9 +628,12 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const float inv_l = 1.f / l;
       const size_t tok = (size_t)tl.tok0 + (size_t)(valid ? i_row : 0);
       uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.o) + (tok * p.H + tl.h) * D);
-      const float* svp = FP8 ? (p.fp8_block ? p.sv + ((size_t)tl.seq * p.Hkv + hk) * D : p.sv) : nullptr;
+      // channels of the output (FP8 head dim 64 runs here with zero channels 64-127)
+      const int dch = (FP8 && p.fp8_d > 0) ? p.fp8_d : D;
+      const float* svp = FP8 ? (p.fp8_block ? p.sv + ((size_t)tl.seq * p.Hkv + hk) * dch : p.sv) : nullptr;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
+        if (FP8 && c * 64 >= dch) break;
         uint32_t u[64];
         tmem_ld64(to + c * 64, u);
         if constexpr (DECODE) {

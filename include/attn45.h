@@ -121,8 +121,9 @@ ATTN45_API int attn_fp8_prepass(const void* q, const void* k, const void* v, voi
  *   raised only when a block's maximum exceeds it by more than 8 (log2
  *   units), so every p = 2^(t - m) is <= 2^8. p is rounded to e4m3 with no
  *   extra multiplier (codes <= 256 < 448, never saturated) for the P*V
- *   product; the row normaliser sums the unrounded p. d must be 128 or 256
- *   (256 runs on pairs of CTAs that share each tensor-core product).
+ *   product; the row normaliser sums the unrounded p. d = 64, 128 or 256
+ *   (256 runs on pairs of CTAs that share each tensor-core product; 64 runs
+ *   on the head-dim-128 kernel, whose copies zero-fill channels 64-127).
  */
 ATTN45_API int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* sq, const float* sk,
                  const float* sv, void* o, float* lse, int B, int H, int Hkv, int N, int d, int causal,
@@ -132,7 +133,7 @@ ATTN45_API int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, con
  * attn_fwd_fp8_auto -- pre-pass + FP8 forward in one call, with the
  * quantised tensors placed in a caller-provided device workspace of at least
  * attn_fp8_workspace_size() bytes (256-byte aligned). Every argument the
- * forward step checks (d = 128 or 256, causal, scale, o, lse) is checked before the
+ * forward step checks (causal, scale, o, lse) is checked before the
  * pre-pass runs, so a rejected call writes nothing.
  */
 ATTN45_API size_t attn_fp8_workspace_size(int B, int H, int Hkv, int N, int d, int mode);

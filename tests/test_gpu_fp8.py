@@ -124,6 +124,34 @@ def test_fp8_forward_d256_short():
     _emulated_check(3, 77, 2, 1, False, "block", True, seed=13, d=256)
 
 
+# head dim 64: the head-dim-128 kernel, whose copies zero-fill channels 64-127
+# of Q, K and V^T; only the 64 real output channels are stored
+@pytest.mark.parametrize("mode", ["block", "tensor"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_d64_matches_emulation(mode, causal):
+    _emulated_check(2, 300, 4, 2, causal, mode, True, seed=21, d=64)
+
+
+def test_fp8_forward_d64_no_rotation_gqa_several_units():
+    _emulated_check(1, 1000, 8, 2, True, "block", False, seed=22, d=64)
+
+
+def test_fp8_d64_output_rows_are_exactly_64_channels():
+    # the output tensor's neighbours are untouched (nothing is stored past
+    # channel 63 of a row)
+    import exact_attention_45_gb300 as A
+    B, N, H, d = 1, 200, 2, 64
+    q, k, v = (t.cuda() for t in gen.qkv_fixed(B, N, H, H, d, seed=23, dist="outlier"))
+    pre = A.attn_fp8_prepass(q, k, v, mode="block", rotate=True, hadamard_seed=3)
+    buf = torch.full((B * N * H * d + 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[:B * N * H * d].view(B, N, H, d)
+    o, _ = A.attn_fwd_fp8(pre, out=out)
+    torch.cuda.synchronize()
+    assert A.attn_get_device_error() == 0
+    assert torch.isfinite(o.float()).all()
+    assert torch.all(buf[B * N * H * d:] == 7.0)
+
+
 def test_fp8_auto_equals_two_calls():
     import exact_attention_45_gb300 as A
     q, k, v = (t.cuda() for t in gen.qkv_fixed(2, 640, 4, 4, 128, seed=3, dist="outlier"))
