@@ -150,13 +150,14 @@ int attn_fp8_prepass(const void* q, const void* k, const void* v, void* q8, void
   a.err = err;
   Prepass128Maps maps;
   const Prepass128Maps* mp = nullptr;
-  if (d == 128 || (d == 256 && mode == ATTN_FP8_PER_BLOCK)) {
+  if (d == 128 || mode == ATTN_FP8_PER_BLOCK) {
     if ((rc = api_make_map(&maps.in_q, false, q, d, H, N, B, 64, 128))) return rc;
     if ((rc = api_make_map(&maps.in_k, false, k, d, Hkv, N, B, 64, 128))) return rc;
     if ((rc = api_make_map(&maps.in_v, false, v, d, Hkv, N, B, 64, 128))) return rc;
     if ((rc = api_make_map(&maps.out_q, true, q8, d, H, N, B, 128, 128))) return rc;
     if ((rc = api_make_map(&maps.out_k, true, k8, d, Hkv, N, B, 128, 128))) return rc;
-    if ((rc = api_make_map_rows(&maps.out_vt, vt8, attn_fp8_vt_ld(N), d, (uint64_t)B * Hkv, 128, 128))) return rc;
+    if ((rc = api_make_map_rows(&maps.out_vt, vt8, attn_fp8_vt_ld(N), d, (uint64_t)B * Hkv, 128, d < 128 ? d : 128)))
+      return rc;
     mp = &maps;
   }
   cudaError_t e = launch_fp8_prepass(a, d, mp, sm, static_cast<cudaStream_t>(stream));

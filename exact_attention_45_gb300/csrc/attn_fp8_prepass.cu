@@ -668,13 +668,13 @@ __global__ void __launch_bounds__(128) v128_kernel(const __grid_constant__ CUten
   }
 }
 
-// ---------------------------------------------------------------- head dims 128 and 256, persistent (block scales)
+// ---------------------------------------------------------------- head dims 64, 128, 256, persistent (block scales)
 // Two persistent launches replace the per-block kernels for fixed-length
-// block quantisation at head dims 128 and 256 (tiles of 128 rows x D channels
-// arrive by TMA into a ring, 64-channel boxes; thread 0 issues the copy of
-// tile k + stages as soon as the CTA barrier that follows the reads of tile k
-// has passed, so no producer warp takes registers away; two CTAs of 8 warps
-// per SM at D = 128, one at D = 256):
+// block quantisation (tiles of 128 rows x D channels arrive by TMA into a
+// ring, 64-channel boxes; thread 0 issues the copy of tile k + stages as soon
+// as the CTA barrier that follows the reads of tile k has passed, so no
+// producer warp takes registers away; three CTAs of 8 warps per SM at D = 64,
+// two at D = 128, one at D = 256):
 //  prep_main_kernel: work list ordered by 128-row block (batch, block) and
 //    inside it [Q heads][K heads][V heads], so the V tiles (per-channel amax,
 //    atomicMax into sv) keep HBM busy while other CTAs do the Q/K arithmetic:
@@ -696,7 +696,7 @@ struct PrepTraits {
   static constexpr int MAIN_SMEM = 1024 + MAIN_STAGES * TILE;
   static constexpr int CODE_TILE = D * ROWS;                // u8 [D channels][128 keys]
   static constexpr int V_SMEM = 1024 + V_STAGES * TILE + 2 * CODE_TILE;
-  static constexpr int MIN_CTAS = D == 128 ? 2 : 1;
+  static constexpr int MIN_CTAS = D == 64 ? 3 : (D == 128 ? 2 : 1);
   static constexpr int E = D / 2;                           // Q/K elements per thread (two threads per row)
 };
 
@@ -820,10 +820,10 @@ __global__ void __launch_bounds__(P_THREADS, PrepTraits<D>::MIN_CTAS) prep_main_
           }
         }
       }
-      if constexpr (U < 32) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], 16));
-      }
+      for (int off = U; off < 32; off <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], off));
       if (lane < U) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) vred[pb][warp][8 * o + i] = cm[i];
@@ -843,9 +843,11 @@ __global__ void __launch_bounds__(P_THREADS, PrepTraits<D>::MIN_CTAS) prep_main_
     float x[E];
 #pragma unroll
     for (int j = 0; j < E / 8; ++j) {
-      // 16-byte unit j of this half row: chunk half * E / 64 + j / 8, unit j % 8
-      const uint8_t* src = tile + (half * (E / 64) + (j >> 3)) * 16384 + r * 128;
-      const uint4 v = *reinterpret_cast<const uint4*>(src + (((j & 7) ^ (r & 7)) << 4));
+      // 16-byte unit j of this half row: elements e0 .. e0+7 of the row, in
+      // 64-channel chunk e0 / 64 at unit (e0 / 8) % 8
+      const int e0 = half * E + j * 8;
+      const uint8_t* src = tile + (e0 >> 6) * 16384 + r * 128;
+      const uint4 v = *reinterpret_cast<const uint4*>(src + ((((e0 >> 3) & 7) ^ (r & 7)) << 4));
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -1028,9 +1030,10 @@ __global__ void __launch_bounds__(P_THREADS, PrepTraits<D>::MIN_CTAS) prep_vcode
     __syncthreads();                                  // tile read, code tile written
     if (t == 0) {
       prep_load<D, S>(a, sh, ring, k + S, total, ORDER_V, &in_v, &in_v, &in_v);
-      // one bulk group per tile: 128 channel rows per store
+      // one bulk group per tile: up to 128 channel rows per store
 #pragma unroll
-      for (int h = 0; h < D / 128; ++h) tma_store_4d(&out_vt, ct + h * 16384, blk * ROWS, h * 128, b * a.Hkv + head, 0);
+      for (int h = 0; h < (D + 127) / 128; ++h)
+        tma_store_4d(&out_vt, ct + h * 16384, blk * ROWS, h * 128, b * a.Hkv + head, 0);
       tma_store_commit();
     }
   }
@@ -1126,11 +1129,12 @@ cudaError_t launch_fp8_prepass(const PrepassArgs& a, int d, const Prepass128Maps
   const int nqk = (a.B * a.H + a.B * a.Hkv) * a.nblk;
   const int nv = a.B * a.Hkv * a.nblk;
   const bool fast_qk = d == 128 && maps != nullptr;
-  if (maps != nullptr && a.block_mode && (d == 128 || d == 256)) {
+  if (maps != nullptr && a.block_mode) {
     // persistent kernels: Q/K codes and V channel amax in one pass, V codes in
     // a second one, then the amax values become scales
-    e = d == 128 ? launch_prep_persistent<128>(a, *maps, nqk, nv, sm_count, s)
-                 : launch_prep_persistent<256>(a, *maps, nqk, nv, sm_count, s);
+    e = d == 64 ? launch_prep_persistent<64>(a, *maps, nqk, nv, sm_count, s)
+                : (d == 128 ? launch_prep_persistent<128>(a, *maps, nqk, nv, sm_count, s)
+                            : launch_prep_persistent<256>(a, *maps, nqk, nv, sm_count, s));
     if (e != cudaSuccess) return e;
     finalize_kernel<<<(int)((nsv + 255) / 256), 256, 0, s>>>(a.sq, a.sk, a.sv, (int)nsv, 0);
     return cudaGetLastError();

@@ -26,11 +26,12 @@ struct PrepassArgs {
   int* blk_off;
 };
 
-// Tensor maps of the TMA-fed pre-pass kernels (head dim 128, and head dim 256
-// with block scales): bf16 inputs (Q, K, V) {d, heads, N, B} with 64 x 128-row
-// boxes, e4m3 outputs {d, heads, N, B} with 128 x 128-row boxes (per-tensor
-// scales, d = 128), and (fixed length) the transposed V codes {ldv, d,
-// B * Hkv} with 128 keys x 128 channel-row boxes; 128-byte swizzle.
+// Tensor maps of the TMA-fed pre-pass kernels (head dim 128, and head dims 64
+// and 256 with block scales): bf16 inputs (Q, K, V) {d, heads, N, B} with 64 x
+// 128-row boxes, e4m3 outputs {d, heads, N, B} with 128 x 128-row boxes
+// (per-tensor scales, d = 128), and (fixed length) the transposed V codes
+// {ldv, d, B * Hkv} with 128 keys x min(d, 128) channel-row boxes; 128-byte
+// swizzle.
 struct Prepass128Maps {
   CUtensorMap in_q, in_k, in_v, out_q, out_k, out_vt;
 };

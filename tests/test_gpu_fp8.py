@@ -52,9 +52,9 @@ def test_prepass_bit_exact(d, mode, rotate):
         assert np.array_equal(pre[name].cpu().numpy(), ref[name]), name
 
 
-@pytest.mark.parametrize("d,B", [(128, 4), (256, 2)])
+@pytest.mark.parametrize("d,B", [(64, 8), (128, 4), (256, 2)])
 def test_prepass_persistent_many_tiles_bit_exact(d, B):
-    # block scales at head dims 128 and 256 run on persistent kernels fed by a
+    # block scales at head dims 64, 128 and 256 run on persistent kernels fed by a
     # ring of TMA copies: enough 128-row tiles that every CTA goes around the
     # ring more than once, the last block of each sequence ragged (2000 rows)
     N, H, Hkv = 2000, 8, 4
