@@ -334,6 +334,18 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         ++tile_i;
         // slot j: K_j (j < nkv) and V_{j-1} (j >= 1)
         for (int j = 0; j <= nkv; ++j, ++slot_it) {
+          // 16-bit kinds: the next unit's Q tiles are prefetched into L2 four key
+          // blocks before this unit ends, so their copy (issued once this unit's
+          // last Q K^T has run) does not wait on HBM between units (measured
+          // +1.6 % at d = 128; no gain for FP8)
+          if (!FP8 && !DECODE && j == max(nkv - 4, 0) && t + (int)gridDim.x < ntiles) {
+            const Tile2 tn = get_tile(t + gridDim.x);
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+#pragma unroll
+              for (int c = 0; c < T::NC; ++c)
+                tma_prefetch_l2_4d(&tmQ, c * (128 / ELEM), tn.h, tn.tma_row0 + tn.sblk * SUPER_M + x * BLOCK_M, tn.tma_b);
+          }
           const int st = slot_it % STAGES;
           ok = mbar_wait(&bars->slot_empty[st], ((slot_it / STAGES) & 1) ^ 1, tmo, abort_flag, p.err);
           if (!ok) break;
