@@ -4,30 +4,32 @@
 // "trains Transformers faster"; it consumes the forward's logsumexp, so P is
 // recomputed from S and lse instead of stored). For a key block j of 128 keys
 // and every query block i of 128 rows that sees it (every head of the group
-// for grouped-query attention):
-//     S  = Q_i K_j^T                 P  = exp(scale S - lse_i)      (recomputed)
-//     dP = dO_i V_j^T                dS = scale P * (dP - D_i),  D_i = rowsum(dO_i * O_i)
-//     dV_j += P^T dO_i               dK_j += dS^T Q_i               dQ_i += dS K_j
+// for grouped-query attention), with keys on the TMEM lanes:
+//     S^T = K_j Q_i^T               P^T = exp(scale S^T - lse_i)  (lse per column)
+//     dP^T = V_j dO_i^T             dS^T = scale P^T * (dP^T - D_i), D_i = rowsum(dO_i * O_i)
+//     dV_j += P^T dO_i              dK_j += dS^T Q_i               dQ_i += dS K_j
 // One CTA owns a (batch, KV head, key block) unit: dV_j and dK_j stay in TMEM
-// across all its query blocks and are written once; dQ_i is produced per
-// block in TMEM, staged in shared memory (over the P/dS tiles, which its
-// GEMM has finished reading) and added into an fp32 accumulator in HBM by bulk
-// tensor reductions (other key blocks add to the same rows); converted at the end.
+// across all its query blocks and are written once; P^T and dS^T are written
+// back over S^T and dP^T in TMEM and are the A operands of dV and dK, so P never
+// goes through shared memory; dS is also stored to shared memory (rows = keys)
+// as dQ's A operand. dQ_i is produced per block in TMEM, staged in shared
+// memory (over the dS tile and the free P tile) and added into an fp32
+// accumulator in HBM by bulk tensor reductions (other key blocks add to the
+// same rows); converted at the end.
 //
 // Roles (320 threads): warps 0-7 compute (thread r of a warpgroup owns TMEM
-// lane r: query row r for S/dP/dQ, key r for dV/dK; warpgroup 0 takes the
-// first half of the columns, warpgroup 1 the second), warp 8 lane 0 loads by
-// TMA, warp 9 lane 0 issues the MMAs. TMEM: S (128 cols, reused for dQ), dP (128), dV (d),
-// dK (d). Shared memory: K_j, V_j, two Q tiles (Q_{i+1} arrives while block i
-// runs), the dO_i tile and the bf16 P and dS tiles that feed the last three
-// products (MN-major for P^T / dS^T, K-major for dS). P is signalled before dS
-// is stored, so dV runs while dS is written; each warpgroup stages its half of
-// dQ in the P and dS chunks it writes itself and waits only for its own
-// previous reduction before overwriting them.
-// Per query block the MMA thread issues dP = dO_i V^T first (its TMEM columns
-// are free once the softmax warps have read the previous dP) and S = Q_i K^T
-// once the previous dQ has been read out of S's columns; dO_i is released
-// after dV, Q_i after dK, so both next copies overlap the rest of the block.
+// lane r: key r for S^T/dP^T/dV/dK, query row r for dQ; warpgroup 0 takes
+// query columns 0-63, warpgroup 1 columns 64-127), warp 8 lane 0 loads by
+// TMA, warp 9 lane 0 issues the MMAs. TMEM: S^T (128 cols, reused for dQ),
+// dP^T (128), dV (d), dK (d). Shared memory: K_j, V_j, two Q tiles (Q_{i+1}
+// arrives while block i runs), the dO_i tile, the dS tile, the dQ staging
+// half (the old P tile), and the block's lse / D per query.
+// Per query block the MMA thread issues dP^T = V dO_i^T first (after the
+// previous dK, which read dS^T from those columns), S^T = K Q_i^T once the
+// previous dQ has been read out of S's columns, then dV and dK as soon as P^T
+// and dS^T are in TMEM (while the compute warps store dS), and dQ once dS is
+// stored. Each warpgroup stages its half of dQ in the chunks of the two tiles
+// it writes itself and waits only for its own previous reduction.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include "api_internal.h"
@@ -46,7 +48,8 @@ struct BwdTraits {
   static constexpr int OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE;   // Q: two tiles (block parity)
   static constexpr int OFF_DO = 4 * TILE;
   static constexpr int OFF_P = 5 * TILE, OFF_DS = OFF_P + PTILE;
-  static constexpr int OFF_BARS = OFF_DS + PTILE;
+  static constexpr int OFF_LSD = OFF_DS + PTILE;      // lse*log2(e) and D of the block's 128 queries
+  static constexpr int OFF_BARS = OFF_LSD + 256 * 4;
   static constexpr int SMEM = OFF_BARS + 256 + 1024;  // + alignment slack
   static constexpr int T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
 };
@@ -191,12 +194,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_kk = idesc_kind_f16_ab(128, 128, BF16, false, false);   // S, dP
-      constexpr uint32_t id_mm = idesc_kind_f16_ab(128, D, BF16, true, true);       // dV, dK
-      constexpr uint32_t id_km = idesc_kind_f16_ab(128, D, BF16, false, true);      // dQ
+      constexpr uint32_t id_kk = idesc_kind_f16_ab(128, 128, BF16, false, false);   // S^T, dP^T
+      constexpr uint32_t id_ts = idesc_kind_f16(128, D, BF16, true);                // dV, dK (A in TMEM)
+      constexpr uint32_t id_mm = idesc_kind_f16_ab(128, D, BF16, true, true);       // dQ
       const uint32_t sk = smem_u32(smem + T::OFF_K), sv = smem_u32(smem + T::OFF_V);
       const uint32_t sq0 = smem_u32(smem + T::OFF_Q), sdo = smem_u32(smem + T::OFF_DO);
-      const uint32_t sp = smem_u32(smem + T::OFF_P), sds = smem_u32(smem + T::OFF_DS);
+      const uint32_t sds = smem_u32(smem + T::OFF_DS);
+      // TMEM column of K step k (16 queries) of P^T / dS^T: queries 0-63 in the
+      // first 32 columns of the warpgroup-0 half, 64-127 in those of the other
+      auto pcol = [](int k) -> uint32_t { return k < 4 ? 8 * k : 64 + 8 * (k - 4); };
       int unit_i = 0, blk_it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < nunits && ok; t += gridDim.x, ++unit_i) {
@@ -205,17 +211,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int it = 0; it < u.nblk && ok; ++it, ++blk_it) {
           const int qs = blk_it & 1;
           const uint32_t sq = sq0 + qs * T::TILE;
-          // dP = dO_i V_j^T first: its columns were read before the previous
-          // P-ready arrival (K-major operands, K = d)
+          // dP^T = V_j dO_i^T (keys on the TMEM lanes): its columns held the
+          // previous block's dS^T, which the previous dK has read (issued
+          // before this, executed in order)
           ok = mbar_wait(&bars->do_full, blk_it & 1, tmo, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < KS; ++k) {
             const uint32_t off = (k >> 2) * T::CHUNK + (k & 3) * 32;
-            umma_f16_ss(tmem + T::T_DP, sdesc_kmajor_sw128(sdo + off), sdesc_kmajor_sw128(sv + off), id_kk, k > 0);
+            umma_f16_ss(tmem + T::T_DP, sdesc_kmajor_sw128(sv + off), sdesc_kmajor_sw128(sdo + off), id_kk, k > 0);
           }
-          // S = Q_i K_j^T once Q_i has landed and the previous block's dQ has
+          // S^T = K_j Q_i^T once Q_i has landed and the previous block's dQ has
           // been read out of S's columns
           ok = mbar_wait(&bars->q_full[qs], (blk_it >> 1) & 1, tmo, abort_flag, p.err);
           if (ok && blk_it > 0) ok = mbar_wait(&bars->dq_empty, (blk_it - 1) & 1, tmo, abort_flag, p.err);
@@ -224,40 +231,36 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
           for (int k = 0; k < KS; ++k) {
             const uint32_t off = (k >> 2) * T::CHUNK + (k & 3) * 32;
-            umma_f16_ss(tmem + T::T_S, sdesc_kmajor_sw128(sq + off), sdesc_kmajor_sw128(sk + off), id_kk, k > 0);
+            umma_f16_ss(tmem + T::T_S, sdesc_kmajor_sw128(sk + off), sdesc_kmajor_sw128(sq + off), id_kk, k > 0);
           }
           umma_commit(&bars->s_full);
+          // P^T and dS^T in TMEM (over S^T and dP^T)
           ok = mbar_wait(&bars->p_full, blk_it & 1, tmo, abort_flag, p.err);
           // the previous unit's dK/dV must have been read before they restart at zero
           if (ok && it == 0 && unit_i > 0) ok = mbar_wait(&bars->dkv_empty, (unit_i - 1) & 1, tmo, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
-          // dV += P^T dO_i, dK += dS^T Q_i: K = 128 query rows; A (P^T, dS^T) and
-          // B (dO_i, Q_i) MN-major: 16 query rows per step = 2048 bytes
+          // dV += P^T dO_i, dK += dS^T Q_i: A from TMEM (K = 128 queries), B
+          // (dO_i, Q_i) MN-major: 16 query rows per step = 2048 bytes
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            umma_f16_ss(tmem + T::T_DV, sdesc_mnmajor_sw128(sp + k * 2048, T::CHUNK),
-                        sdesc_mnmajor_sw128(sdo + k * 2048, T::CHUNK), id_mm, (it > 0 || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < 8; ++k)
+            umma_f16_ts(tmem + T::T_DV, tmem + T::T_S + pcol(k), sdesc_mnmajor_sw128(sdo + k * 2048, T::CHUNK), id_ts,
+                        (it > 0 || k > 0) ? 1u : 0u);
           umma_commit(&bars->do_empty);                   // dO_i is read by nothing after dV
-          // dS is stored while dV runs
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            umma_f16_ts(tmem + T::T_DK, tmem + T::T_DP + pcol(k), sdesc_mnmajor_sw128(sq + k * 2048, T::CHUNK), id_ts,
+                        (it > 0 || k > 0) ? 1u : 0u);
+          umma_commit(&bars->q_empty[qs]);                 // Q_i is read by nothing after dK
+          // dQ_i = dS K_j: A = dS in shared memory (rows = keys, queries
+          // contiguous: MN-major, K = 128 keys), B = K_j MN-major (N = d)
           ok = mbar_wait(&bars->ds_full, blk_it & 1, tmo, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            umma_f16_ss(tmem + T::T_DK, sdesc_mnmajor_sw128(sds + k * 2048, T::CHUNK),
-                        sdesc_mnmajor_sw128(sq + k * 2048, T::CHUNK), id_mm, (it > 0 || k > 0) ? 1u : 0u);
-          }
-          // Q_i is read by nothing after dK
-          umma_commit(&bars->q_empty[qs]);
-          // dQ_i = dS K_j: A = dS K-major (K = 128 keys), B = K_j MN-major (N = d)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t aoff = (k >> 2) * T::CHUNK + (k & 3) * 32;
-            umma_f16_ss(tmem + T::T_S, sdesc_kmajor_sw128(sds + aoff), sdesc_mnmajor_sw128(sk + k * 2048, T::CHUNK),
-                        id_km, k > 0 ? 1u : 0u);
-          }
+          for (int k = 0; k < 8; ++k)
+            umma_f16_ss(tmem + T::T_S, sdesc_mnmajor_sw128(sds + k * 2048, T::CHUNK),
+                        sdesc_mnmajor_sw128(sk + k * 2048, T::CHUNK), id_mm, k > 0 ? 1u : 0u);
           umma_commit(&bars->dq_full);
         }
         if (!ok) break;
@@ -277,92 +280,100 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const float scale = p.scale;
     uint8_t* tp = smem + T::OFF_P;
     uint8_t* tds = smem + T::OFF_DS;
-    // row r of a P/dS tile: chunk (64 keys) at +16 KB, 16-byte unit u at u ^ (r % 8)
+    // row r of the dS tile (key r, queries contiguous) and of the dQ staging:
+    // chunk (64 columns) at +16 KB, 16-byte unit u at u ^ (r % 8)
     const uint32_t prow = smem_u32(tp) + r * 128;
     const uint32_t dsrow = smem_u32(tds) + r * 128;
+    float* lsd_base = reinterpret_cast<float*>(smem + T::OFF_LSD);
+    static_assert(T::SMEM <= 227 * 1024, "backward shared memory");
     int unit_i = 0, blk_it = 0;
-    float lse_next = 0.f, d_next = 0.f;
     bool ok = true;
     for (int t = blockIdx.x; t < nunits && ok; t += gridDim.x, ++unit_i) {
       const BwdUnit u = bwd_unit(p, t, CAUSAL);
+      const int key = u.j * 128 + r;                           // this thread's key row (S^T, dP^T)
       for (int it = 0; it < u.nblk && ok; ++it, ++blk_it) {
         const int h = u.hkv * p.group + it / u.nI;
         const int i = bwd_qblock(u, it);
-        const int qrow = i * 128 + r;
-        const bool row_ok = qrow < p.N;
-        const size_t lrow = ((size_t)u.b * p.H + h) * p.N + (row_ok ? qrow : 0);
-        // this row's lse and D were fetched during the previous block (not for
-        // a unit's first block)
-        if (it == 0) {
-          lse_next = row_ok ? __ldg(p.lse + lrow) : 0.f;
-          d_next = row_ok ? __ldg(p.dvec + lrow) : 0.f;
+        // lse * log2(e) (warpgroup 0) and D (warpgroup 1) of the block's 128
+        // queries into shared memory. Rewriting them is safe: this thread has
+        // passed the previous block's dQ-ready barrier, which needed every
+        // thread's dS-ready arrival, made after its last read of them
+        float* lsd = lsd_base;
+        {
+          const int qrow = i * 128 + r;
+          float v = 0.f;
+          if (qrow < p.N) {
+            const size_t lrow = ((size_t)u.b * p.H + h) * p.N + qrow;
+            v = half == 0 ? __ldg(p.lse + lrow) * 1.4426950408889634f : __ldg(p.dvec + lrow);
+          }
+          lsd[half * 128 + r] = v;
         }
-        const float lse2 = lse_next * 1.4426950408889634f;
-        const float Drow = d_next;
-        if (it + 1 < u.nblk) {
-          const int h1 = u.hkv * p.group + (it + 1) / u.nI;
-          const int q1 = bwd_qblock(u, it + 1) * 128 + r;
-          const size_t l1 = ((size_t)u.b * p.H + h1) * p.N + (q1 < p.N ? q1 : 0);
-          lse_next = __ldg(p.lse + l1);
-          d_next = __ldg(p.dvec + l1);
-        }
+        named_bar_sync(1, BWD_COMPUTE);
         ok = mbar_wait(&bars->s_full, blk_it & 1, tmo, abort_flag, p.err);
         if (!ok) break;
         tc_fence_after();
-        // keys of this block visible to row qrow
-        int kmax = p.N - u.j * 128;                            // keys past the end are masked
-        if (CAUSAL) kmax = min(kmax, qrow - u.j * 128 + 1);
-        if (!row_ok) kmax = 0;
+        // queries of this block visible to this key: [qlo, qhi)
+        int qlo = 0, qhi = min(128, p.N - i * 128);
+        if (CAUSAL) qlo = max(0, key - i * 128);             // query >= key
+        if (key >= p.N) qhi = 0;
         {
-          const int c = half;                                  // keys c*64 .. c*64+63
+          const int c = half;                                  // queries c*64 .. c*64+63
           uint32_t su[64], du[64];
           tmem_ld64_pair(tmem + lane_off + T::T_S + c * 64, su, tmem + lane_off + T::T_DP + c * 64, du);
+          const float4* l4 = reinterpret_cast<const float4*>(lsd + c * 64);
+          const float4* d4 = reinterpret_cast<const float4*>(lsd + 128 + c * 64);
           uint32_t pw[32], dw[32];
-          if (kmax >= (c + 1) * 64) {
-            // no key of this half is masked for this row: packed pairs, the same
+          if (qlo <= c * 64 && qhi >= (c + 1) * 64) {
+            // no query of this half is masked for this key: packed pairs, the same
             // roundings as below (p = 2^(s * scale * log2 e - lse * log2 e);
             // dS = (scale * p) * (dP - D))
-            const uint64_t sl2x2 = f2_pack(sl2, sl2), nlse2 = f2_pack(-lse2, -lse2);
-            const uint64_t sc2 = f2_pack(scale, scale), d2 = f2_pack(Drow, Drow);
+            const uint64_t sl2x2 = f2_pack(sl2, sl2), sc2 = f2_pack(scale, scale);
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-              float p0, p1;
-              f2_unpack(f2_fma(f2_pack(to_f(su[e]), to_f(su[e + 1])), sl2x2, nlse2), p0, p1);
-              p0 = ex2_approx(p0);
-              p1 = ex2_approx(p1);
-              const uint64_t pp = f2_pack(p0, p1);
-              float d0, d1;
-              f2_unpack(f2_mul(f2_mul(pp, sc2), f2_sub(f2_pack(to_f(du[e]), to_f(du[e + 1])), d2)), d0, d1);
-              pw[e / 2] = pack16<BF16>(p0, p1);
-              dw[e / 2] = pack16<BF16>(d0, d1);
+            for (int e4 = 0; e4 < 16; ++e4) {
+              const float4 lv = l4[e4], dv4 = d4[e4];
+              const float lq[4] = {lv.x, lv.y, lv.z, lv.w}, dq[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+#pragma unroll
+              for (int e2 = 0; e2 < 4; e2 += 2) {
+                const int e = 4 * e4 + e2;
+                float p0, p1;
+                f2_unpack(f2_fma(f2_pack(to_f(su[e]), to_f(su[e + 1])), sl2x2, f2_pack(-lq[e2], -lq[e2 + 1])), p0, p1);
+                p0 = ex2_approx(p0);
+                p1 = ex2_approx(p1);
+                const uint64_t pp = f2_pack(p0, p1);
+                float d0, d1;
+                f2_unpack(f2_mul(f2_mul(pp, sc2), f2_sub(f2_pack(to_f(du[e]), to_f(du[e + 1])), f2_pack(dq[e2], dq[e2 + 1]))),
+                          d0, d1);
+                pw[e / 2] = pack16<BF16>(p0, p1);
+                dw[e / 2] = pack16<BF16>(d0, d1);
+              }
             }
           } else {
 #pragma unroll
             for (int e = 0; e < 64; e += 2) {
-              const int key = c * 64 + e;
-              const float p0 = key < kmax ? ex2_approx(to_f(su[e]) * sl2 - lse2) : 0.f;
-              const float p1 = key + 1 < kmax ? ex2_approx(to_f(su[e + 1]) * sl2 - lse2) : 0.f;
-              const float d0 = scale * p0 * (to_f(du[e]) - Drow);
-              const float d1 = scale * p1 * (to_f(du[e + 1]) - Drow);
+              const int q = c * 64 + e;
+              const bool v0 = q >= qlo && q < qhi, v1 = q + 1 >= qlo && q + 1 < qhi;
+              const float p0 = v0 ? ex2_approx(to_f(su[e]) * sl2 - lsd[q]) : 0.f;
+              const float p1 = v1 ? ex2_approx(to_f(su[e + 1]) * sl2 - lsd[q + 1]) : 0.f;
+              const float d0 = scale * p0 * (to_f(du[e]) - lsd[128 + q]);
+              const float d1 = scale * p1 * (to_f(du[e + 1]) - lsd[128 + q + 1]);
               pw[e / 2] = pack16<BF16>(p0, p1);
               dw[e / 2] = pack16<BF16>(d0, d1);
             }
           }
+          // P^T over the first 32 of this half's S^T columns, dS^T over the
+          // first 32 of its dP^T columns (the A operands of dV and dK)
+          tmem_st32(tmem + lane_off + T::T_S + c * 64, pw);
+          tmem_st32(tmem + lane_off + T::T_DP + c * 64, dw);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->p_full);
           // this warpgroup's previous dQ reduction reads chunk c of the P and
-          // dS tiles as its staging: wait for it only now, after the loads and
-          // the arithmetic
+          // dS tiles as its staging: wait for it only now
           if (blk_it > 0) {
             if (r == 0) tma_store_wait_read();
             named_bar_sync(2 + half, 128);
           }
-          // keys c*64 .. c*64+63 fill chunk c of the row: 16-byte unit q at q ^ (r % 8);
-          // P first (the dV product starts on it), then dS
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            st_shared_v4(prow + c * T::CHUNK + ((q ^ (r & 7)) << 4), pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
-          fence_proxy_async_smem();                           // P visible to the MMAs
-          tc_fence_before();                                  // S, dP read out of TMEM
-          mbar_arrive(&bars->p_full);
+          // dS for dQ: row = key r, queries c*64 .. c*64+63 in chunk c, 16-byte unit q at q ^ (r % 8)
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             st_shared_v4(dsrow + c * T::CHUNK + ((q ^ (r & 7)) << 4), dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
@@ -373,10 +384,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         ok = mbar_wait(&bars->dq_full, blk_it & 1, tmo, abort_flag, p.err);
         if (!ok) break;
         tc_fence_after();
-        // dQ rows (this warpgroup's D/2 columns) -> staging in the chunks of the
-        // P and dS tiles this warpgroup writes (chunk `half` of each): 32 fp32
-        // columns per 16 KB chunk, row r, 16-byte unit v at v ^ (r % 8), the
-        // bulk reduction's 128-byte swizzle
+        // dQ rows (query r, this warpgroup's D/2 columns) -> staging in the
+        // chunks of the P and dS tiles this warpgroup writes (chunk `half` of
+        // each): 32 fp32 columns per 16 KB chunk, row r, 16-byte unit v at
+        // v ^ (r % 8), the bulk reduction's 128-byte swizzle
         {
           constexpr int HC = D / 2;                            // columns per warpgroup
           uint32_t qu[HC];
@@ -408,7 +419,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       ok = mbar_wait(&bars->dkv_full, unit_i & 1, tmo, abort_flag, p.err);
       if (!ok) break;
       tc_fence_after();
-      const int key = u.j * 128 + r;
       const bool key_ok = key < p.N;
       const size_t krow = (((size_t)u.b * p.N + (key_ok ? key : 0)) * p.Hkv + u.hkv) * D;
       uint4* dkp = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.dk) + krow);
