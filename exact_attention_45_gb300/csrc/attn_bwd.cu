@@ -89,6 +89,27 @@ __device__ __forceinline__ int bwd_qblock(const BwdUnit& u, int it) { return u.i
 
 __device__ __forceinline__ float to_f(uint32_t u) { return __uint_as_float(u); }
 
+// Two TMEM loads of 32 lanes x 32 columns (e.g. the same rows of two regions)
+// with one wait for both.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t (&a)[32], uint32_t tb, uint32_t (&b)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]),
+        "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]),
+        "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]),
+        "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]), "=r"(b[0]),
+        "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]),
+        "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]),
+        "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]),
+        "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
   uint32_t r;
@@ -318,46 +339,48 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (key >= p.N) qhi = 0;
         {
           const int c = half;                                  // queries c*64 .. c*64+63
-          uint32_t su[64], du[64];
-          tmem_ld64_pair(tmem + lane_off + T::T_S + c * 64, su, tmem + lane_off + T::T_DP + c * 64, du);
-          const float4* l4 = reinterpret_cast<const float4*>(lsd + c * 64);
-          const float4* d4 = reinterpret_cast<const float4*>(lsd + 128 + c * 64);
           uint32_t pw[32], dw[32];
-          if (qlo <= c * 64 && qhi >= (c + 1) * 64) {
-            // no query of this half is masked for this key: packed pairs, the same
-            // roundings as below (p = 2^(s * scale * log2 e - lse * log2 e);
-            // dS = (scale * p) * (dP - D))
-            const uint64_t sl2x2 = f2_pack(sl2, sl2), sc2 = f2_pack(scale, scale);
 #pragma unroll
-            for (int e4 = 0; e4 < 16; ++e4) {
-              const float4 lv = l4[e4], dv4 = d4[e4];
-              const float lq[4] = {lv.x, lv.y, lv.z, lv.w}, dq[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+          for (int hh = 0; hh < 2; ++hh) {
+            // 32 query columns at a time keep fewer registers live
+            const int cb = c * 64 + hh * 32;                   // first query column of this piece
+            uint32_t su[32], du[32];
+            tmem_ld32x2(tmem + lane_off + T::T_S + cb, su, tmem + lane_off + T::T_DP + cb, du);
+            const float4* l4 = reinterpret_cast<const float4*>(lsd + cb);
+            const float4* d4 = reinterpret_cast<const float4*>(lsd + 128 + cb);
+            if (qlo <= cb && qhi >= cb + 32) {
+              const uint64_t sl2x2 = f2_pack(sl2, sl2), sc2 = f2_pack(scale, scale);
 #pragma unroll
-              for (int e2 = 0; e2 < 4; e2 += 2) {
-                const int e = 4 * e4 + e2;
-                float p0, p1;
-                f2_unpack(f2_fma(f2_pack(to_f(su[e]), to_f(su[e + 1])), sl2x2, f2_pack(-lq[e2], -lq[e2 + 1])), p0, p1);
-                p0 = ex2_approx(p0);
-                p1 = ex2_approx(p1);
-                const uint64_t pp = f2_pack(p0, p1);
-                float d0, d1;
-                f2_unpack(f2_mul(f2_mul(pp, sc2), f2_sub(f2_pack(to_f(du[e]), to_f(du[e + 1])), f2_pack(dq[e2], dq[e2 + 1]))),
-                          d0, d1);
-                pw[e / 2] = pack16<BF16>(p0, p1);
-                dw[e / 2] = pack16<BF16>(d0, d1);
+              for (int e4 = 0; e4 < 8; ++e4) {
+                const float4 lv = l4[e4], dv4 = d4[e4];
+                const float lq[4] = {lv.x, lv.y, lv.z, lv.w}, dq[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+#pragma unroll
+                for (int e2 = 0; e2 < 4; e2 += 2) {
+                  const int e = 4 * e4 + e2;
+                  float p0, p1;
+                  f2_unpack(f2_fma(f2_pack(to_f(su[e]), to_f(su[e + 1])), sl2x2, f2_pack(-lq[e2], -lq[e2 + 1])), p0, p1);
+                  p0 = ex2_approx(p0);
+                  p1 = ex2_approx(p1);
+                  const uint64_t pp = f2_pack(p0, p1);
+                  float d0, d1;
+                  f2_unpack(f2_mul(f2_mul(pp, sc2), f2_sub(f2_pack(to_f(du[e]), to_f(du[e + 1])), f2_pack(dq[e2], dq[e2 + 1]))),
+                            d0, d1);
+                  pw[hh * 16 + e / 2] = pack16<BF16>(p0, p1);
+                  dw[hh * 16 + e / 2] = pack16<BF16>(d0, d1);
+                }
               }
-            }
-          } else {
+            } else {
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-              const int q = c * 64 + e;
-              const bool v0 = q >= qlo && q < qhi, v1 = q + 1 >= qlo && q + 1 < qhi;
-              const float p0 = v0 ? ex2_approx(to_f(su[e]) * sl2 - lsd[q]) : 0.f;
-              const float p1 = v1 ? ex2_approx(to_f(su[e + 1]) * sl2 - lsd[q + 1]) : 0.f;
-              const float d0 = scale * p0 * (to_f(du[e]) - lsd[128 + q]);
-              const float d1 = scale * p1 * (to_f(du[e + 1]) - lsd[128 + q + 1]);
-              pw[e / 2] = pack16<BF16>(p0, p1);
-              dw[e / 2] = pack16<BF16>(d0, d1);
+              for (int e = 0; e < 32; e += 2) {
+                const int q = cb + e;
+                const bool v0 = q >= qlo && q < qhi, v1 = q + 1 >= qlo && q + 1 < qhi;
+                const float p0 = v0 ? ex2_approx(to_f(su[e]) * sl2 - lsd[q]) : 0.f;
+                const float p1 = v1 ? ex2_approx(to_f(su[e + 1]) * sl2 - lsd[q + 1]) : 0.f;
+                const float d0 = scale * p0 * (to_f(du[e]) - lsd[128 + q]);
+                const float d1 = scale * p1 * (to_f(du[e + 1]) - lsd[128 + q + 1]);
+                pw[hh * 16 + e / 2] = pack16<BF16>(p0, p1);
+                dw[hh * 16 + e / 2] = pack16<BF16>(d0, d1);
+              }
             }
           }
           // P^T over the first 32 of this half's S^T columns, dS^T over the
