@@ -406,9 +406,10 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         tc_fence_after();
         const uint32_t ts = tmem + lane_off + T::TMEM_S + sb * BN;
         float s[BN];
+        float mx;                                     // row maximum of the block's scores
         {
           uint32_t u[BN];
-          tmem_ld128(ts, u);
+          tmem_ld128_max(ts, u, mx);
 #pragma unroll
           for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(u[i]);
         }
@@ -422,19 +423,21 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll
           for (int c = 0; c < BN; ++c)
             if (c >= limit) s[c] = -INFINITY;
-        }
-        float mxa = fmax3(s[0], s[1], s[2]), mxb = fmax3(s[3], s[4], s[5]);
-        float mxc = fmax3(s[6], s[7], s[8]), mxd = fmax3(s[9], s[10], s[11]);
+          // the load's maximum may come from a masked key: recompute it
+          float mxa = fmax3(s[0], s[1], s[2]), mxb = fmax3(s[3], s[4], s[5]);
+          float mxc = fmax3(s[6], s[7], s[8]), mxd = fmax3(s[9], s[10], s[11]);
 #pragma unroll
-        for (int c = 12; c < BN - 4; c += 8) {
-          mxa = fmax3(mxa, s[c], s[c + 1]);
-          mxb = fmax3(mxb, s[c + 2], s[c + 3]);
-          mxc = fmax3(mxc, s[c + 4], s[c + 5]);
-          mxd = fmax3(mxd, s[c + 6], s[c + 7]);
+          for (int c = 12; c < BN - 4; c += 8) {
+            mxa = fmax3(mxa, s[c], s[c + 1]);
+            mxb = fmax3(mxb, s[c + 2], s[c + 3]);
+            mxc = fmax3(mxc, s[c + 4], s[c + 5]);
+            mxd = fmax3(mxd, s[c + 6], s[c + 7]);
+          }
+          mxa = fmax3(mxa, s[BN - 4], s[BN - 3]);
+          mxb = fmax3(mxb, s[BN - 2], s[BN - 1]);
+          mx = fmaxf(fmaxf(mxa, mxb), fmaxf(mxc, mxd));
         }
-        mxa = fmax3(mxa, s[BN - 4], s[BN - 3]);
-        mxb = fmax3(mxb, s[BN - 2], s[BN - 1]);
-        const float mx = fmaxf(fmaxf(mxa, mxb), fmaxf(mxc, mxd)) * sl2;
+        mx *= sl2;
         // the running maximum moves only past the lazy margin (2^8)
         const bool raise = mx > m + lazy;
         const float m_new = raise ? mx : m;
