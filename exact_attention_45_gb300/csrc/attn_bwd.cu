@@ -218,9 +218,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       constexpr uint32_t id_kk = idesc_kind_f16_ab(128, 128, BF16, false, false);   // S^T, dP^T
       constexpr uint32_t id_ts = idesc_kind_f16(128, D, BF16, true);                // dV, dK (A in TMEM)
       constexpr uint32_t id_mm = idesc_kind_f16_ab(128, D, BF16, true, true);       // dQ
-      const uint32_t sk = smem_u32(smem + T::OFF_K), sv = smem_u32(smem + T::OFF_V);
-      const uint32_t sq0 = smem_u32(smem + T::OFF_Q), sdo = smem_u32(smem + T::OFF_DO);
-      const uint32_t sds = smem_u32(smem + T::OFF_DS);
+      // descriptor low halves of each operand's first byte, K-major (S^T, dP^T)
+      // and MN-major (dV, dK, dQ): every MMA's descriptor is one of these plus
+      // a constant, so the issue path carries no descriptor arithmetic
+      const uint32_t k_km = sdesc_lo_kmajor_sw128(smem_u32(smem + T::OFF_K));
+      const uint32_t v_km = sdesc_lo_kmajor_sw128(smem_u32(smem + T::OFF_V));
+      const uint32_t q_km = sdesc_lo_kmajor_sw128(smem_u32(smem + T::OFF_Q));
+      const uint32_t do_km = sdesc_lo_kmajor_sw128(smem_u32(smem + T::OFF_DO));
+      const uint32_t k_mn = sdesc_lo_mnmajor_sw128(smem_u32(smem + T::OFF_K), T::CHUNK);
+      const uint32_t q_mn = sdesc_lo_mnmajor_sw128(smem_u32(smem + T::OFF_Q), T::CHUNK);
+      const uint32_t do_mn = sdesc_lo_mnmajor_sw128(smem_u32(smem + T::OFF_DO), T::CHUNK);
+      const uint32_t ds_mn = sdesc_lo_mnmajor_sw128(smem_u32(smem + T::OFF_DS), T::CHUNK);
       // TMEM column of K step k (16 queries) of P^T / dS^T: queries 0-63 in the
       // first 32 columns of the warpgroup-0 half, 64-127 in those of the other
       auto pcol = [](int k) -> uint32_t { return k < 4 ? 8 * k : 64 + 8 * (k - 4); };
@@ -231,7 +239,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         ok = mbar_wait(&bars->kv_full, unit_i & 1, tmo, abort_flag, p.err);
         for (int it = 0; it < u.nblk && ok; ++it, ++blk_it) {
           const int qs = blk_it & 1;
-          const uint32_t sq = sq0 + qs * T::TILE;
+          const uint32_t qt = qs * (T::TILE >> 4);        // Q_i's buffer, in descriptor units
           // dP^T = V_j dO_i^T (keys on the TMEM lanes): its columns held the
           // previous block's dS^T, which the previous dK has read (issued
           // before this, executed in order)
@@ -240,8 +248,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < KS; ++k) {
-            const uint32_t off = (k >> 2) * T::CHUNK + (k & 3) * 32;
-            umma_f16_ss(tmem + T::T_DP, sdesc_kmajor_sw128(sv + off), sdesc_kmajor_sw128(sdo + off), id_kk, k > 0);
+            const uint32_t off = ((k >> 2) * T::CHUNK + (k & 3) * 32) >> 4;
+            umma_f16_ss_lo(tmem + T::T_DP, v_km + off, do_km + off, id_kk, k > 0);
           }
           // S^T = K_j Q_i^T once Q_i has landed and the previous block's dQ has
           // been read out of S's columns
@@ -251,8 +259,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < KS; ++k) {
-            const uint32_t off = (k >> 2) * T::CHUNK + (k & 3) * 32;
-            umma_f16_ss(tmem + T::T_S, sdesc_kmajor_sw128(sk + off), sdesc_kmajor_sw128(sq + off), id_kk, k > 0);
+            const uint32_t off = ((k >> 2) * T::CHUNK + (k & 3) * 32) >> 4;
+            umma_f16_ss_lo(tmem + T::T_S, k_km + off, q_km + qt + off, id_kk, k > 0);
           }
           umma_commit(&bars->s_full);
           // P^T and dS^T in TMEM (over S^T and dP^T)
@@ -265,13 +273,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           // (dO_i, Q_i) MN-major: 16 query rows per step = 2048 bytes
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            umma_f16_ts(tmem + T::T_DV, tmem + T::T_S + pcol(k), sdesc_mnmajor_sw128(sdo + k * 2048, T::CHUNK), id_ts,
-                        (it > 0 || k > 0) ? 1u : 0u);
+            umma_f16_ts_lo(tmem + T::T_DV, tmem + T::T_S + pcol(k), do_mn + k * (2048 >> 4), id_ts,
+                           (it > 0 || k > 0) ? 1u : 0u);
           umma_commit(&bars->do_empty);                   // dO_i is read by nothing after dV
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            umma_f16_ts(tmem + T::T_DK, tmem + T::T_DP + pcol(k), sdesc_mnmajor_sw128(sq + k * 2048, T::CHUNK), id_ts,
-                        (it > 0 || k > 0) ? 1u : 0u);
+            umma_f16_ts_lo(tmem + T::T_DK, tmem + T::T_DP + pcol(k), q_mn + qt + k * (2048 >> 4), id_ts,
+                           (it > 0 || k > 0) ? 1u : 0u);
           umma_commit(&bars->q_empty[qs]);                 // Q_i is read by nothing after dK
           // dQ_i = dS K_j: A = dS in shared memory (rows = keys, queries
           // contiguous: MN-major, K = 128 keys), B = K_j MN-major (N = d)
@@ -280,8 +288,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            umma_f16_ss(tmem + T::T_S, sdesc_mnmajor_sw128(sds + k * 2048, T::CHUNK),
-                        sdesc_mnmajor_sw128(sk + k * 2048, T::CHUNK), id_mm, k > 0 ? 1u : 0u);
+            umma_f16_ss_lo(tmem + T::T_S, ds_mn + k * (2048 >> 4), k_mn + k * (2048 >> 4), id_mm, k > 0 ? 1u : 0u);
           umma_commit(&bars->dq_full);
         }
         if (!ok) break;

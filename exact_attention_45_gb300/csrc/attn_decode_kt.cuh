@@ -300,7 +300,12 @@ __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_c
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_kind_f16_ab(128, NQ, BF16, false, false);
       constexpr uint32_t id_o = idesc_kind_f16_ab(128, NQ, BF16, true, false);
-      const uint32_t sq = smem_u32(smem + C::OFF_Q), sp = smem_u32(smem + C::OFF_P);
+      // descriptor low halves of stage 0's K and V^T, of Q and of P: every
+      // MMA's descriptor is one of these plus a constant
+      const uint32_t k_lo = sdesc_lo_kmajor_sw128(smem_u32(smem));
+      const uint32_t v_lo = sdesc_lo_mnmajor_sw128(smem_u32(smem + C::NCH * KT_CHUNK), KT_CHUNK);
+      const uint32_t q_lo = sdesc_lo_kmajor_sw128(smem_u32(smem + C::OFF_Q));
+      const uint32_t p_lo = sdesc_lo_kmajor_sw128(smem_u32(smem + C::OFF_P));
       uint32_t piece_first = 0;                     // bit (tile & 31): first tile of its piece
       int ns = 0, np = 0, k = -1;
       uint64_t t0 = global_timer_ns();
@@ -315,11 +320,11 @@ __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_c
             if (first) ++k;
             piece_first = first ? (piece_first | (1u << (ns & 31))) : (piece_first & ~(1u << (ns & 31)));
             tc_fence_after();
-            const uint32_t sk = smem_u32(smem + st * C::STAGE), sqb = sq + (k & 1) * C::QBYTES;
+            const uint32_t kb = k_lo + st * (C::STAGE >> 4), qb = q_lo + (k & 1) * (C::QBYTES >> 4);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-              umma_f16_ss(tmem + sb * NQ, sdesc_kmajor_sw128(sk + (kk >> 2) * KT_CHUNK + (kk & 3) * 32),
-                          sdesc_kmajor_sw128(sqb + (kk >> 2) * C::QCH + (kk & 3) * 32), id_s, kk > 0 ? 1u : 0u);
+              umma_f16_ss_lo(tmem + sb * NQ, kb + (((kk >> 2) * KT_CHUNK + (kk & 3) * 32) >> 4),
+                             qb + (((kk >> 2) * C::QCH + (kk & 3) * 32) >> 4), id_s, kk > 0 ? 1u : 0u);
             umma_commit(&bars->s_full[sb]);
             if (last) umma_commit(&bars->q_free[k & 1]);
             pos.next(p);
@@ -333,12 +338,11 @@ __global__ void __launch_bounds__(KT_THREADS, 1) decode_kt_kernel(const __grid_c
           tc_fence_after();
           // V^T as A with M = 128: for D = 64 its second 64 rows read the next
           // 16 KB of shared memory (in bounds) into O^T rows that are never used
-          const uint32_t sv = smem_u32(smem + st * C::STAGE + C::NCH * KT_CHUNK);
+          const uint32_t vb = v_lo + st * (C::STAGE >> 4), pbl = p_lo + pb * (C::PBYTES >> 4);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_f16_ss(tmem + C::COL_O, sdesc_mnmajor_sw128(sv + kk * 2048, KT_CHUNK),
-                        sdesc_kmajor_sw128(sp + pb * C::PBYTES + (kk >> 2) * C::PCH + (kk & 3) * 32), id_o,
-                        (pf && kk == 0) ? 0u : 1u);
+            umma_f16_ss_lo(tmem + C::COL_O, vb + kk * (2048 >> 4), pbl + (((kk >> 2) * C::PCH + (kk & 3) * 32) >> 4),
+                           id_o, (pf && kk == 0) ? 0u : 1u);
           umma_commit(&bars->empty[st]);
           umma_commit(&bars->pv_done[pb]);
           ++np;

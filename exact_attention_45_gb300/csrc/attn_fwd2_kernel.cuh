@@ -394,9 +394,12 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       constexpr uint32_t idesc_o = FP8 ? idesc_kind_f8_e4m3(BLOCK_M, D) : idesc_kind_f16(BLOCK_M, D, BF16, true);
       constexpr int PV_STEPS = BN * ELEM / 32;               // 32-byte K steps of P V
       constexpr int S_STEPS = D * ELEM / 32;                 // 32-byte K steps of Q K^T
-      const uint32_t qa = smem_u32(sQ);
-      const uint32_t ka = smem_u32(sK);
-      const uint32_t va = smem_u32(sV);
+      // descriptor low halves of the operands' first bytes; every MMA's
+      // descriptor is one of these plus a constant (the issue path between
+      // S_B(j) and P_A(j) V_j has no descriptor arithmetic left to do)
+      const uint32_t q_lo = sdesc_lo_kmajor_sw128(smem_u32(sQ));
+      const uint32_t k_lo = sdesc_lo_kmajor_sw128(smem_u32(sK));
+      const uint32_t v_lo = FP8 ? sdesc_lo_kmajor_sw128(smem_u32(sV)) : sdesc_lo_mnmajor_sw128(smem_u32(sV), T::KV_CHUNK);
       int slot_it = 0, tile_i = 0;
       int p_cnt0 = 0, p_cnt1 = 0;
       bool ok = true;
@@ -410,8 +413,8 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (!ok) break;
         for (int j = 0; j <= nkv && ok; ++j, ++slot_it) {
           const int st = slot_it % STAGES;
-          const uint32_t vbase = va + st * T::KV_BYTES;
-          const uint32_t kb = ka + st * T::KV_BYTES;
+          const uint32_t vb_lo = v_lo + st * (T::KV_BYTES >> 4);
+          const uint32_t kb_lo = k_lo + st * (T::KV_BYTES >> 4);
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
             if (!ok) continue;
@@ -432,26 +435,21 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               for (int k = 0; k < PV_STEPS; ++k) {
                 // each K step is 8 TMEM columns of P (16 x 16-bit or 32 x 8-bit)
                 if constexpr (FP8)
-                  umma_f8_ts(o_tmem, s_tmem + k * 8, sdesc_kmajor_sw128(vbase + k * 32), idesc_o,
-                             (j > 1 || k > 0) ? 1u : 0u);
+                  umma_f8_ts_lo(o_tmem, s_tmem + k * 8, vb_lo + k * (32 >> 4), idesc_o, (j > 1 || k > 0) ? 1u : 0u);
                 else
-                  umma_f16_ts(o_tmem, s_tmem + k * 8, sdesc_mnmajor_sw128(vbase + k * 2048, T::KV_CHUNK), idesc_o,
-                              (j > 1 || k > 0) ? 1u : 0u);
+                  umma_f16_ts_lo(o_tmem, s_tmem + k * 8, vb_lo + k * (2048 >> 4), idesc_o, (j > 1 || k > 0) ? 1u : 0u);
               }
               if (j == nb[x]) umma_commit(&bars->o_done[x]);   // last P V of this tile
             }
             if (j < nb[x]) {
-              const uint32_t qx = qa + x * T::Q_BYTES;
 #pragma unroll
               for (int k = 0; k < S_STEPS; ++k) {
-                const uint32_t qo = (k >> 2) * T::Q_CHUNK + (k & 3) * 32;
-                const uint32_t ko = (k >> 2) * T::KV_CHUNK + (k & 3) * 32;
+                const uint32_t qo = (x * T::Q_BYTES + (k >> 2) * T::Q_CHUNK + (k & 3) * 32) >> 4;
+                const uint32_t ko = ((k >> 2) * T::KV_CHUNK + (k & 3) * 32) >> 4;
                 if constexpr (FP8)
-                  umma_f8_ss(s_tmem, sdesc_kmajor_sw128(qx + qo), sdesc_kmajor_sw128(kb + ko), idesc_s,
-                             k > 0 ? 1u : 0u);
+                  umma_f8_ss_lo(s_tmem, q_lo + qo, kb_lo + ko, idesc_s, k > 0 ? 1u : 0u);
                 else
-                  umma_f16_ss(s_tmem, sdesc_kmajor_sw128(qx + qo), sdesc_kmajor_sw128(kb + ko), idesc_s,
-                              k > 0 ? 1u : 0u);
+                  umma_f16_ss_lo(s_tmem, q_lo + qo, kb_lo + ko, idesc_s, k > 0 ? 1u : 0u);
               }
               umma_commit(&bars->s_full[x]);
             }

@@ -290,8 +290,17 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
       constexpr int S_STEPS = D * ELEM / 32;               // 32-byte K steps of Q K^T
       constexpr int PV_STEPS = BN * ELEM / 32;             // 32-byte K steps of P V
       constexpr uint16_t both = 3;
-      const uint32_t qa = smem_u32(sQ);
-      const uint32_t k_a = smem_u32(smem + T::OFF_K), v_a = smem_u32(smem + T::OFF_V);
+      // descriptor low halves of the operands' first bytes: each MMA's
+      // descriptor is one of these plus a constant, so no descriptor
+      // arithmetic sits between S(j)'s last MMA and P(j-1) V's first
+      const uint32_t q_lo = sdesc_lo_kmajor_sw128(smem_u32(sQ));
+      const uint32_t k_lo = sdesc_lo_kmajor_sw128(smem_u32(smem + T::OFF_K));
+      const uint32_t v_lo = FP8 ? sdesc_lo_kmajor_sw128(smem_u32(smem + T::OFF_V))
+                                : sdesc_lo_mnmajor_sw128(smem_u32(smem + T::OFF_V), T::V_CHUNK);
+      // the V of a shared slot sits K_BYTES after the slot's K (read with the
+      // V operand's own layout)
+      const uint32_t kv_lo = FP8 ? sdesc_lo_kmajor_sw128(smem_u32(smem + T::OFF_K) + T::K_BYTES)
+                                 : sdesc_lo_mnmajor_sw128(smem_u32(smem + T::OFF_K) + T::K_BYTES, T::V_CHUNK);
       int k_it = 0, v_it = 0, slot_it = 0, tile_i = 0, s_it = 0, pv_it = 0;
       bool ok = true;
       for (int t = cluster_id; t < ntiles && ok; t += nclusters) {
@@ -311,7 +320,7 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           }
           if (j < nkv) {
             const int ks = k_it % T::K_STAGES;
-            const uint32_t kb = T::SHARED_SLOTS ? k_a + st * T::SLOT_BYTES : k_a + ks * T::K_BYTES;
+            const uint32_t kb_lo = k_lo + (T::SHARED_SLOTS ? st * (T::SLOT_BYTES >> 4) : ks * (T::K_BYTES >> 4));
             if constexpr (!T::SHARED_SLOTS) {
               ok = mbar_wait(&bars->k_full[ks], (k_it / T::K_STAGES) & 1, tmo, abort_flag, p.err);
               if (!ok) break;
@@ -320,14 +329,12 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const uint32_t s_tmem = tmem + T::TMEM_S + (s_it & 1) * BN;
 #pragma unroll
             for (int k = 0; k < S_STEPS; ++k) {
-              const uint32_t qo = (k >> 2) * T::Q_CHUNK + (k & 3) * 32;
-              const uint32_t ko = (k >> 2) * T::K_CHUNK + (k & 3) * 32;
+              const uint32_t qo = ((k >> 2) * T::Q_CHUNK + (k & 3) * 32) >> 4;
+              const uint32_t ko = ((k >> 2) * T::K_CHUNK + (k & 3) * 32) >> 4;
               if constexpr (FP8)
-                umma_f8_ss_pair(s_tmem, sdesc_kmajor_sw128(qa + qo), sdesc_kmajor_sw128(kb + ko), idesc_s,
-                                k > 0 ? 1u : 0u);
+                umma_f8_ss_pair_lo(s_tmem, q_lo + qo, kb_lo + ko, idesc_s, k > 0 ? 1u : 0u);
               else
-                umma_f16_ss_pair(s_tmem, sdesc_kmajor_sw128(qa + qo), sdesc_kmajor_sw128(kb + ko), idesc_s,
-                                 k > 0 ? 1u : 0u);
+                umma_f16_ss_pair_lo(s_tmem, q_lo + qo, kb_lo + ko, idesc_s, k > 0 ? 1u : 0u);
             }
             umma_commit_pair(&bars->s_full[s_it & 1], both);
             if constexpr (!T::SHARED_SLOTS) umma_commit_pair(&bars->k_empty[ks], both);
@@ -338,7 +345,7 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           if (j >= 1) {
             // P(j-1) lives in the S buffer of the pv_it-th S
             const int vs = v_it % T::V_STAGES;
-            const uint32_t vb = T::SHARED_SLOTS ? k_a + st * T::SLOT_BYTES + T::K_BYTES : v_a + vs * T::V_BYTES;
+            const uint32_t vb_lo = T::SHARED_SLOTS ? kv_lo + st * (T::SLOT_BYTES >> 4) : v_lo + vs * (T::V_BYTES >> 4);
             ok = mbar_wait(&bars->p_full[pv_it & 1], (pv_it >> 1) & 1, tmo, abort_flag, p.err);
             if constexpr (!T::SHARED_SLOTS)
               if (ok) ok = mbar_wait(&bars->v_full[vs], (v_it / T::V_STAGES) & 1, tmo, abort_flag, p.err);
@@ -349,11 +356,11 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             for (int k = 0; k < PV_STEPS; ++k) {
               // each K step is 8 TMEM columns of P (16 x 16-bit or 32 x 8-bit)
               if constexpr (FP8)
-                umma_f8_ts_pair(tmem + T::TMEM_O, a_tmem + k * 8, sdesc_kmajor_sw128(vb + k * 32), idesc_o,
-                                (j > 1 || k > 0) ? 1u : 0u);
+                umma_f8_ts_pair_lo(tmem + T::TMEM_O, a_tmem + k * 8, vb_lo + k * (32 >> 4), idesc_o,
+                                   (j > 1 || k > 0) ? 1u : 0u);
               else
-                umma_f16_ts_pair(tmem + T::TMEM_O, a_tmem + k * 8, sdesc_mnmajor_sw128(vb + k * 2048, T::V_CHUNK),
-                                 idesc_o, (j > 1 || k > 0) ? 1u : 0u);
+                umma_f16_ts_pair_lo(tmem + T::TMEM_O, a_tmem + k * 8, vb_lo + k * (2048 >> 4), idesc_o,
+                                    (j > 1 || k > 0) ? 1u : 0u);
             }
             umma_commit_pair(&bars->o_done, both);
             if constexpr (!T::SHARED_SLOTS) umma_commit_pair(&bars->v_empty[vs], both);
