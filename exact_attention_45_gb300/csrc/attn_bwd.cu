@@ -214,7 +214,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // the whole warp runs the loop (convergent control flow); one elected
+    // lane issues each MMA and commit
+    {
       constexpr uint32_t id_kk = idesc_kind_f16_ab(128, 128, BF16, false, false);   // S^T, dP^T
       constexpr uint32_t id_ts = idesc_kind_f16(128, D, BF16, true);                // dV, dK (A in TMEM)
       constexpr uint32_t id_mm = idesc_kind_f16_ab(128, D, BF16, true, true);       // dQ
@@ -236,66 +238,66 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       bool ok = true;
       for (int t = blockIdx.x; t < nunits && ok; t += gridDim.x, ++unit_i) {
         const BwdUnit u = bwd_unit(p, t, CAUSAL);
-        ok = mbar_wait(&bars->kv_full, unit_i & 1, tmo, abort_flag, p.err);
+        ok = mbar_wait_warp(&bars->kv_full, unit_i & 1, tmo, abort_flag, p.err);
         for (int it = 0; it < u.nblk && ok; ++it, ++blk_it) {
           const int qs = blk_it & 1;
           const uint32_t qt = qs * (T::TILE >> 4);        // Q_i's buffer, in descriptor units
           // dP^T = V_j dO_i^T (keys on the TMEM lanes): its columns held the
           // previous block's dS^T, which the previous dK has read (issued
           // before this, executed in order)
-          ok = mbar_wait(&bars->do_full, blk_it & 1, tmo, abort_flag, p.err);
+          ok = mbar_wait_warp(&bars->do_full, blk_it & 1, tmo, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < KS; ++k) {
             const uint32_t off = ((k >> 2) * T::CHUNK + (k & 3) * 32) >> 4;
-            umma_f16_ss_lo(tmem + T::T_DP, v_km + off, do_km + off, id_kk, k > 0);
+            umma_f16_ss_lo_w(tmem + T::T_DP, v_km + off, do_km + off, id_kk, k > 0);
           }
           // S^T = K_j Q_i^T once Q_i has landed and the previous block's dQ has
           // been read out of S's columns
-          ok = mbar_wait(&bars->q_full[qs], (blk_it >> 1) & 1, tmo, abort_flag, p.err);
-          if (ok && blk_it > 0) ok = mbar_wait(&bars->dq_empty, (blk_it - 1) & 1, tmo, abort_flag, p.err);
+          ok = mbar_wait_warp(&bars->q_full[qs], (blk_it >> 1) & 1, tmo, abort_flag, p.err);
+          if (ok && blk_it > 0) ok = mbar_wait_warp(&bars->dq_empty, (blk_it - 1) & 1, tmo, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < KS; ++k) {
             const uint32_t off = ((k >> 2) * T::CHUNK + (k & 3) * 32) >> 4;
-            umma_f16_ss_lo(tmem + T::T_S, k_km + off, q_km + qt + off, id_kk, k > 0);
+            umma_f16_ss_lo_w(tmem + T::T_S, k_km + off, q_km + qt + off, id_kk, k > 0);
           }
-          umma_commit(&bars->s_full);
+          umma_commit_w(&bars->s_full);
           // P^T and dS^T in TMEM (over S^T and dP^T)
-          ok = mbar_wait(&bars->p_full, blk_it & 1, tmo, abort_flag, p.err);
+          ok = mbar_wait_warp(&bars->p_full, blk_it & 1, tmo, abort_flag, p.err);
           // the previous unit's dK/dV must have been read before they restart at zero
-          if (ok && it == 0 && unit_i > 0) ok = mbar_wait(&bars->dkv_empty, (unit_i - 1) & 1, tmo, abort_flag, p.err);
+          if (ok && it == 0 && unit_i > 0) ok = mbar_wait_warp(&bars->dkv_empty, (unit_i - 1) & 1, tmo, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
           // dV += P^T dO_i, dK += dS^T Q_i: A from TMEM (K = 128 queries), B
           // (dO_i, Q_i) MN-major: 16 query rows per step = 2048 bytes
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            umma_f16_ts_lo(tmem + T::T_DV, tmem + T::T_S + pcol(k), do_mn + k * (2048 >> 4), id_ts,
+            umma_f16_ts_lo_w(tmem + T::T_DV, tmem + T::T_S + pcol(k), do_mn + k * (2048 >> 4), id_ts,
                            (it > 0 || k > 0) ? 1u : 0u);
-          umma_commit(&bars->do_empty);                   // dO_i is read by nothing after dV
+          umma_commit_w(&bars->do_empty);                   // dO_i is read by nothing after dV
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            umma_f16_ts_lo(tmem + T::T_DK, tmem + T::T_DP + pcol(k), q_mn + qt + k * (2048 >> 4), id_ts,
+            umma_f16_ts_lo_w(tmem + T::T_DK, tmem + T::T_DP + pcol(k), q_mn + qt + k * (2048 >> 4), id_ts,
                            (it > 0 || k > 0) ? 1u : 0u);
-          umma_commit(&bars->q_empty[qs]);                 // Q_i is read by nothing after dK
+          umma_commit_w(&bars->q_empty[qs]);                 // Q_i is read by nothing after dK
           // dQ_i = dS K_j: A = dS in shared memory (rows = keys, queries
           // contiguous: MN-major, K = 128 keys), B = K_j MN-major (N = d)
-          ok = mbar_wait(&bars->ds_full, blk_it & 1, tmo, abort_flag, p.err);
+          ok = mbar_wait_warp(&bars->ds_full, blk_it & 1, tmo, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            umma_f16_ss_lo(tmem + T::T_S, ds_mn + k * (2048 >> 4), k_mn + k * (2048 >> 4), id_mm, k > 0 ? 1u : 0u);
-          umma_commit(&bars->dq_full);
+            umma_f16_ss_lo_w(tmem + T::T_S, ds_mn + k * (2048 >> 4), k_mn + k * (2048 >> 4), id_mm, k > 0 ? 1u : 0u);
+          umma_commit_w(&bars->dq_full);
         }
         if (!ok) break;
-        umma_commit(&bars->dkv_full);
-        umma_commit(&bars->kv_empty);
+        umma_commit_w(&bars->dkv_full);
+        umma_commit_w(&bars->kv_empty);
       }
-      umma_commit(&bars->done);
+      umma_commit_w(&bars->done);
       mbar_wait_drain(&bars->done, 0, tmo, p.err);
     }
     __syncwarp();

@@ -389,7 +389,9 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     // barrier costs the tensor pipe idle time even when it is already
     // complete): once per block for tile A (its P and the slot's data, see
     // the watcher) and once for tile B.
-    if (lane == 0) {
+    // The whole warp runs the loop (convergent control flow); one elected
+    // lane issues each MMA and commit.
+    {
       constexpr uint32_t idesc_s = FP8 ? idesc_kind_f8_e4m3(BLOCK_M, BN) : idesc_kind_f16(BLOCK_M, BN, BF16, false);
       constexpr uint32_t idesc_o = FP8 ? idesc_kind_f8_e4m3(BLOCK_M, D) : idesc_kind_f16(BLOCK_M, D, BF16, true);
       constexpr int PV_STEPS = BN * ELEM / 32;               // 32-byte K steps of P V
@@ -408,7 +410,7 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const int nb[2] = {tile2_blocks<CAUSAL, BN>(tl, 0), tile2_blocks<CAUSAL, BN>(tl, 1)};
         const int nkv = max(nb[0], nb[1]);
         if (nkv == 0) continue;
-        ok = mbar_wait(&bars->q_full, tile_i & 1, tmo, abort_flag, p.err);
+        ok = mbar_wait_warp(&bars->q_full, tile_i & 1, tmo, abort_flag, p.err);
         ++tile_i;
         if (!ok) break;
         for (int j = 0; j <= nkv && ok; ++j, ++slot_it) {
@@ -421,9 +423,9 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             const bool pv = j >= 1 && j - 1 < nb[x];
             int& pc = x == 0 ? p_cnt0 : p_cnt1;
             if (x == 0 && (!WATCH || !pv))
-              ok = mbar_wait(&bars->slot_full[st], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);
+              ok = mbar_wait_warp(&bars->slot_full[st], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);
             if (ok && pv) {
-              ok = mbar_wait(&bars->p_full[x], pc & 1, tmo, abort_flag, p.err);
+              ok = mbar_wait_warp(&bars->p_full[x], pc & 1, tmo, abort_flag, p.err);
               ++pc;
             }
             if (!ok) continue;
@@ -435,11 +437,11 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               for (int k = 0; k < PV_STEPS; ++k) {
                 // each K step is 8 TMEM columns of P (16 x 16-bit or 32 x 8-bit)
                 if constexpr (FP8)
-                  umma_f8_ts_lo(o_tmem, s_tmem + k * 8, vb_lo + k * (32 >> 4), idesc_o, (j > 1 || k > 0) ? 1u : 0u);
+                  umma_f8_ts_lo_w(o_tmem, s_tmem + k * 8, vb_lo + k * (32 >> 4), idesc_o, (j > 1 || k > 0) ? 1u : 0u);
                 else
-                  umma_f16_ts_lo(o_tmem, s_tmem + k * 8, vb_lo + k * (2048 >> 4), idesc_o, (j > 1 || k > 0) ? 1u : 0u);
+                  umma_f16_ts_lo_w(o_tmem, s_tmem + k * 8, vb_lo + k * (2048 >> 4), idesc_o, (j > 1 || k > 0) ? 1u : 0u);
               }
-              if (j == nb[x]) umma_commit(&bars->o_done[x]);   // last P V of this tile
+              if (j == nb[x]) umma_commit_w(&bars->o_done[x]);   // last P V of this tile
             }
             if (j < nb[x]) {
 #pragma unroll
@@ -447,19 +449,19 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 const uint32_t qo = (x * T::Q_BYTES + (k >> 2) * T::Q_CHUNK + (k & 3) * 32) >> 4;
                 const uint32_t ko = ((k >> 2) * T::KV_CHUNK + (k & 3) * 32) >> 4;
                 if constexpr (FP8)
-                  umma_f8_ss_lo(s_tmem, q_lo + qo, kb_lo + ko, idesc_s, k > 0 ? 1u : 0u);
+                  umma_f8_ss_lo_w(s_tmem, q_lo + qo, kb_lo + ko, idesc_s, k > 0 ? 1u : 0u);
                 else
-                  umma_f16_ss_lo(s_tmem, q_lo + qo, kb_lo + ko, idesc_s, k > 0 ? 1u : 0u);
+                  umma_f16_ss_lo_w(s_tmem, q_lo + qo, kb_lo + ko, idesc_s, k > 0 ? 1u : 0u);
               }
-              umma_commit(&bars->s_full[x]);
+              umma_commit_w(&bars->s_full[x]);
             }
           }
           if (!ok) break;
-          umma_commit(&bars->slot_empty[st]);
-          if (j == nkv - 1) umma_commit(&bars->q_empty);
+          umma_commit_w(&bars->slot_empty[st]);
+          if (j == nkv - 1) umma_commit_w(&bars->q_empty);
         }
       }
-      umma_commit(&bars->mma_done);
+      umma_commit_w(&bars->mma_done);
       mbar_wait_drain(&bars->mma_done, 0, tmo, p.err);
     }
     __syncwarp();

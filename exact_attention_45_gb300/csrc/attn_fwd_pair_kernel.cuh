@@ -284,7 +284,9 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // Step j: S(j) = Q K_j^T into S buffer (j-th S overall) & 1, then
     // O += P(j-1) V_{j-1} once both CTAs' P(j-1) is stored, so the tensor core
     // computes the next scores while the softmax warps work.
-    if (leader && lane == 0) {
+    // the whole warp runs the loop (convergent control flow); one elected
+    // lane issues each MMA and commit
+    if (leader) {
       constexpr uint32_t idesc_s = FP8 ? idesc_kind_f8_e4m3(2 * BLOCK_M, BN) : idesc_kind_f16(2 * BLOCK_M, BN, BF16, false);
       constexpr uint32_t idesc_o = FP8 ? idesc_kind_f8_e4m3(2 * BLOCK_M, D) : idesc_kind_f16(2 * BLOCK_M, D, BF16, true);
       constexpr int S_STEPS = D * ELEM / 32;               // 32-byte K steps of Q K^T
@@ -307,14 +309,14 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         const Tile2 tl = get_tile(t);
         const int nkv = pair_blocks(tl);
         if (nkv == 0) continue;
-        ok = mbar_wait(&bars->q_full, tile_i & 1, tmo, abort_flag, p.err);
+        ok = mbar_wait_warp(&bars->q_full, tile_i & 1, tmo, abort_flag, p.err);
         ++tile_i;
         if (!ok) break;
         for (int j = 0; j <= nkv && ok; ++j, ++slot_it) {
           // shared slots: K_j and V_{j-1} arrive on one barrier
           const int st = slot_it % T::SLOTS;
           if constexpr (T::SHARED_SLOTS) {
-            ok = mbar_wait(&bars->slot_full[st], (slot_it / T::SLOTS) & 1, tmo, abort_flag, p.err);
+            ok = mbar_wait_warp(&bars->slot_full[st], (slot_it / T::SLOTS) & 1, tmo, abort_flag, p.err);
             if (!ok) break;
             tc_fence_after();
           }
@@ -322,7 +324,7 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const int ks = k_it % T::K_STAGES;
             const uint32_t kb_lo = k_lo + (T::SHARED_SLOTS ? st * (T::SLOT_BYTES >> 4) : ks * (T::K_BYTES >> 4));
             if constexpr (!T::SHARED_SLOTS) {
-              ok = mbar_wait(&bars->k_full[ks], (k_it / T::K_STAGES) & 1, tmo, abort_flag, p.err);
+              ok = mbar_wait_warp(&bars->k_full[ks], (k_it / T::K_STAGES) & 1, tmo, abort_flag, p.err);
               if (!ok) break;
               tc_fence_after();
             }
@@ -332,13 +334,13 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
               const uint32_t qo = ((k >> 2) * T::Q_CHUNK + (k & 3) * 32) >> 4;
               const uint32_t ko = ((k >> 2) * T::K_CHUNK + (k & 3) * 32) >> 4;
               if constexpr (FP8)
-                umma_f8_ss_pair_lo(s_tmem, q_lo + qo, kb_lo + ko, idesc_s, k > 0 ? 1u : 0u);
+                umma_f8_ss_pair_lo_w(s_tmem, q_lo + qo, kb_lo + ko, idesc_s, k > 0 ? 1u : 0u);
               else
-                umma_f16_ss_pair_lo(s_tmem, q_lo + qo, kb_lo + ko, idesc_s, k > 0 ? 1u : 0u);
+                umma_f16_ss_pair_lo_w(s_tmem, q_lo + qo, kb_lo + ko, idesc_s, k > 0 ? 1u : 0u);
             }
-            umma_commit_pair(&bars->s_full[s_it & 1], both);
-            if constexpr (!T::SHARED_SLOTS) umma_commit_pair(&bars->k_empty[ks], both);
-            if (j == nkv - 1) umma_commit_pair(&bars->q_empty, both);
+            umma_commit_pair_w(&bars->s_full[s_it & 1], both);
+            if constexpr (!T::SHARED_SLOTS) umma_commit_pair_w(&bars->k_empty[ks], both);
+            if (j == nkv - 1) umma_commit_pair_w(&bars->q_empty, both);
             ++s_it;
             ++k_it;
           }
@@ -346,9 +348,9 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             // P(j-1) lives in the S buffer of the pv_it-th S
             const int vs = v_it % T::V_STAGES;
             const uint32_t vb_lo = T::SHARED_SLOTS ? kv_lo + st * (T::SLOT_BYTES >> 4) : v_lo + vs * (T::V_BYTES >> 4);
-            ok = mbar_wait(&bars->p_full[pv_it & 1], (pv_it >> 1) & 1, tmo, abort_flag, p.err);
+            ok = mbar_wait_warp(&bars->p_full[pv_it & 1], (pv_it >> 1) & 1, tmo, abort_flag, p.err);
             if constexpr (!T::SHARED_SLOTS)
-              if (ok) ok = mbar_wait(&bars->v_full[vs], (v_it / T::V_STAGES) & 1, tmo, abort_flag, p.err);
+              if (ok) ok = mbar_wait_warp(&bars->v_full[vs], (v_it / T::V_STAGES) & 1, tmo, abort_flag, p.err);
             if (!ok) break;
             tc_fence_after();
             const uint32_t a_tmem = tmem + T::TMEM_S + (pv_it & 1) * BN;
@@ -356,21 +358,21 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             for (int k = 0; k < PV_STEPS; ++k) {
               // each K step is 8 TMEM columns of P (16 x 16-bit or 32 x 8-bit)
               if constexpr (FP8)
-                umma_f8_ts_pair_lo(tmem + T::TMEM_O, a_tmem + k * 8, vb_lo + k * (32 >> 4), idesc_o,
+                umma_f8_ts_pair_lo_w(tmem + T::TMEM_O, a_tmem + k * 8, vb_lo + k * (32 >> 4), idesc_o,
                                    (j > 1 || k > 0) ? 1u : 0u);
               else
-                umma_f16_ts_pair_lo(tmem + T::TMEM_O, a_tmem + k * 8, vb_lo + k * (2048 >> 4), idesc_o,
+                umma_f16_ts_pair_lo_w(tmem + T::TMEM_O, a_tmem + k * 8, vb_lo + k * (2048 >> 4), idesc_o,
                                     (j > 1 || k > 0) ? 1u : 0u);
             }
-            umma_commit_pair(&bars->o_done, both);
-            if constexpr (!T::SHARED_SLOTS) umma_commit_pair(&bars->v_empty[vs], both);
+            umma_commit_pair_w(&bars->o_done, both);
+            if constexpr (!T::SHARED_SLOTS) umma_commit_pair_w(&bars->v_empty[vs], both);
             ++pv_it;
             ++v_it;
           }
-          if constexpr (T::SHARED_SLOTS) umma_commit_pair(&bars->slot_empty[st], both);
+          if constexpr (T::SHARED_SLOTS) umma_commit_pair_w(&bars->slot_empty[st], both);
         }
       }
-      umma_commit_pair(&bars->mma_done, 1);
+      umma_commit_pair_w(&bars->mma_done, 1);
       mbar_wait_drain(&bars->mma_done, 0, tmo, p.err);
     }
     __syncwarp();
