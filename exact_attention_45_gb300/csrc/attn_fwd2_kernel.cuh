@@ -87,6 +87,7 @@ struct Bars2 {
   uint64_t q_full, q_empty;
   uint64_t slot_full[4], slot_empty[4];
   uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t p_half[2];                            // P of a block's first 64 keys is in TMEM
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -268,9 +269,11 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       mbar_init(&bars->s_full[x], 1);
       mbar_init(&bars->o_done[x], 1);
     }
-    // tile A's P-ready barrier also carries "slot j has landed" from the
+    // tile A's first-half-P barrier also carries "slot j has landed" from the
     // watcher warp, so the MMA thread waits once for both
-    mbar_init(&bars->p_full[0], WATCH ? 129 : 128);
+    mbar_init(&bars->p_half[0], WATCH ? 129 : 128);
+    mbar_init(&bars->p_half[1], 128);
+    mbar_init(&bars->p_full[0], 128);
     mbar_init(&bars->p_full[1], 128);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -387,8 +390,8 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     // so tile A's softmax of block j overlaps tile B's two GEMMs and vice
     // versa. The issuing thread waits as little as possible (a wait on a
     // barrier costs the tensor pipe idle time even when it is already
-    // complete): once per block for tile A (its P and the slot's data, see
-    // the watcher) and once for tile B.
+    // complete): twice per block and tile, for the first half of P (for tile
+    // A together with the slot's data, see the watcher) and for the rest.
     // The whole warp runs the loop (convergent control flow); one elected
     // lane issues each MMA and commit.
     {
@@ -424,10 +427,10 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             int& pc = x == 0 ? p_cnt0 : p_cnt1;
             if (x == 0 && (!WATCH || !pv))
               ok = mbar_wait_warp(&bars->slot_full[st], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);
-            if (ok && pv) {
-              ok = mbar_wait_warp(&bars->p_full[x], pc & 1, tmo, abort_flag, p.err);
-              ++pc;
-            }
+            // P(j-1) V goes out in two halves: keys 0-63 once their P is in
+            // TMEM (the softmax stores it halfway through its loop), keys
+            // 64-127 once the whole tile is
+            if (ok && pv) ok = mbar_wait_warp(&bars->p_half[x], pc & 1, tmo, abort_flag, p.err);
             if (!ok) continue;
             tc_fence_after();
             const uint32_t s_tmem = tmem + T::TMEM_S + x * BN;
@@ -435,12 +438,19 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               const uint32_t o_tmem = tmem + T::TMEM_O + x * D;
 #pragma unroll
               for (int k = 0; k < PV_STEPS; ++k) {
+                if (k == PV_STEPS / 2) {
+                  ok = mbar_wait_warp(&bars->p_full[x], pc & 1, tmo, abort_flag, p.err);
+                  if (!ok) break;
+                  tc_fence_after();
+                }
                 // each K step is 8 TMEM columns of P (16 x 16-bit or 32 x 8-bit)
                 if constexpr (FP8)
                   umma_f8_ts_lo_w(o_tmem, s_tmem + k * 8, vb_lo + k * (32 >> 4), idesc_o, (j > 1 || k > 0) ? 1u : 0u);
                 else
                   umma_f16_ts_lo_w(o_tmem, s_tmem + k * 8, vb_lo + k * (2048 >> 4), idesc_o, (j > 1 || k > 0) ? 1u : 0u);
               }
+              ++pc;
+              if (!ok) continue;
               if (j == nb[x]) umma_commit_w(&bars->o_done[x]);   // last P V of this tile
             }
             if (j < nb[x]) {
@@ -487,9 +497,9 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           ok = mbar_wait(&bars->slot_full[slot_it % STAGES], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);
           if (!ok) break;
           if (j >= 1 && j - 1 < na) {
-            if (arrivals > 0) ok = mbar_wait(&bars->p_full[0], (arrivals - 1) & 1, tmo, abort_flag, p.err);
+            if (arrivals > 0) ok = mbar_wait(&bars->p_half[0], (arrivals - 1) & 1, tmo, abort_flag, p.err);
             if (!ok) break;
-            mbar_arrive(&bars->p_full[0]);
+            mbar_arrive(&bars->p_half[0]);
             ++arrivals;
           }
         }
@@ -577,6 +587,10 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const float m_new = raise ? mx : m;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = raise ? ex2_approx(m - m_use) : 1.f;
+        // O_x is rescaled (below) when any row of the warp raised its maximum;
+        // such a warp reports its first half of P only after the rescale, so
+        // no P V of this block reaches O_x before it
+        const bool corr = j > 0 && __any_sync(0xffffffffu, raise);
         // p = 2^(s * scale * log2(e) - m): the affine step and the row sum run
         // as packed f32x2 operations, the exponentials on the MUFU unit
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
@@ -603,8 +617,17 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           } else {
             pk[c / 2] = pack2(a0, a1, BF16);
             pk[c / 2 + 1] = pack2(b0, b1, BF16);
-            // first 64 keys' P leave for TMEM halfway (keeps register use down)
-            if (c == 60) tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          }
+          if (c == 60) {
+            // the first 64 keys' P leaves for TMEM halfway, and the MMA thread
+            // may start on it
+            if constexpr (FP8) tmem_st16(ts, &pk[0]);
+            else tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            if (!corr) {
+              tmem_st_wait();
+              tc_fence_before();
+              mbar_arrive(&bars->p_half[x]);
+            }
           }
         }
         float sum0, sum1, sum2, sum3;
@@ -612,14 +635,14 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         f2_unpack(acc1, sum2, sum3);
         l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
         m = m_new;
-        if constexpr (FP8) tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        if constexpr (FP8) tmem_st16(ts + 16, &pk[16]);
         else tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         // the stores read their source registers asynchronously: completing
         // them here frees those registers for the (rare) correction below
         tmem_st_wait();
         // correction: O_x += P(j-1) V has completed (it was issued before
         // S_x(j), whose completion we just observed), so O_x is stable.
-        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+        if (corr) {
 #pragma unroll 1
           for (int c = 0; c < D / 64; ++c) {
             uint32_t u[64];
@@ -630,6 +653,8 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             tmem_st32(to + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
           }
           tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->p_half[x]);
         }
         tc_fence_before();
         mbar_arrive(&bars->p_full[x]);
