@@ -87,7 +87,7 @@ struct Bars2 {
   uint64_t q_full, q_empty;
   uint64_t slot_full[4], slot_empty[4];
   uint64_t s_full[2], p_full[2], o_done[2];
-  uint64_t p_half[2];                            // P of a block's first 64 keys is in TMEM
+  uint64_t p_part[2][3];                         // P of a block's key parts 0..NP-2 is in TMEM
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -239,6 +239,13 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   constexpr bool FP8 = KIND == KIND_E4M3;
   constexpr bool BF16 = KIND == KIND_BF16;
   constexpr int ELEM = FP8 ? 1 : 2;
+  // P V in NP parts of KP keys (PCOLS TMEM columns of P each). Halves: with
+  // quarters the tensor pipe waited between the 16-bit parts (BF16 d = 128
+  // 1835 -> 1555 TFLOP/s)
+  constexpr int NP = 2;
+  constexpr int KP = BN / NP;
+  constexpr int PCOLS = FP8 ? KP / 4 : KP / 2;
+  static_assert(NP <= 4 && BN % NP == 0 && (PCOLS == 16 || PCOLS == 32), "P parts");
   constexpr bool STAGE_OUT = !VARLEN && !DECODE;
   static_assert(!DECODE || (!CAUSAL && !VARLEN && !FP8), "decode units are non-causal 16-bit fixed-cache");
   // Slot watcher (16-bit kinds): measured to help when the GEMMs are long
@@ -269,10 +276,10 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       mbar_init(&bars->s_full[x], 1);
       mbar_init(&bars->o_done[x], 1);
     }
-    // tile A's first-half-P barrier also carries "slot j has landed" from the
-    // watcher warp, so the MMA thread waits once for both
-    mbar_init(&bars->p_half[0], WATCH ? 129 : 128);
-    mbar_init(&bars->p_half[1], 128);
+    // tile A's first-part-of-P barrier also carries "slot j has landed" from
+    // the watcher warp, so the MMA thread waits once for both
+    for (int x = 0; x < 2; ++x)
+      for (int q = 0; q < 3; ++q) mbar_init(&bars->p_part[x][q], (x == 0 && q == 0 && WATCH) ? 129 : 128);
     mbar_init(&bars->p_full[0], 128);
     mbar_init(&bars->p_full[1], 128);
     mbar_init(&bars->mma_done, 1);
@@ -427,10 +434,10 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             int& pc = x == 0 ? p_cnt0 : p_cnt1;
             if (x == 0 && (!WATCH || !pv))
               ok = mbar_wait_warp(&bars->slot_full[st], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);
-            // P(j-1) V goes out in two halves: keys 0-63 once their P is in
-            // TMEM (the softmax stores it halfway through its loop), keys
-            // 64-127 once the whole tile is
-            if (ok && pv) ok = mbar_wait_warp(&bars->p_half[x], pc & 1, tmo, abort_flag, p.err);
+            // P(j-1) V goes out in NP parts of BN / NP keys, each as soon as
+            // the softmax has stored that part's P (it stores them as its loop
+            // goes); the last part waits for the whole tile
+            if (ok && pv) ok = mbar_wait_warp(&bars->p_part[x][0], pc & 1, tmo, abort_flag, p.err);
             if (!ok) continue;
             tc_fence_after();
             const uint32_t s_tmem = tmem + T::TMEM_S + x * BN;
@@ -438,8 +445,10 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               const uint32_t o_tmem = tmem + T::TMEM_O + x * D;
 #pragma unroll
               for (int k = 0; k < PV_STEPS; ++k) {
-                if (k == PV_STEPS / 2) {
-                  ok = mbar_wait_warp(&bars->p_full[x], pc & 1, tmo, abort_flag, p.err);
+                if (k > 0 && k % (PV_STEPS / NP) == 0) {
+                  const int part = k / (PV_STEPS / NP);
+                  ok = mbar_wait_warp(part == NP - 1 ? &bars->p_full[x] : &bars->p_part[x][part], pc & 1, tmo,
+                                      abort_flag, p.err);
                   if (!ok) break;
                   tc_fence_after();
                 }
@@ -497,9 +506,9 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           ok = mbar_wait(&bars->slot_full[slot_it % STAGES], (slot_it / STAGES) & 1, tmo, abort_flag, p.err);
           if (!ok) break;
           if (j >= 1 && j - 1 < na) {
-            if (arrivals > 0) ok = mbar_wait(&bars->p_half[0], (arrivals - 1) & 1, tmo, abort_flag, p.err);
+            if (arrivals > 0) ok = mbar_wait(&bars->p_part[0][0], (arrivals - 1) & 1, tmo, abort_flag, p.err);
             if (!ok) break;
-            mbar_arrive(&bars->p_half[0]);
+            mbar_arrive(&bars->p_part[0][0]);
             ++arrivals;
           }
         }
@@ -588,8 +597,8 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = raise ? ex2_approx(m - m_use) : 1.f;
         // O_x is rescaled (below) when any row of the warp raised its maximum;
-        // such a warp reports its first half of P only after the rescale, so
-        // no P V of this block reaches O_x before it
+        // such a warp reports its parts of P only after the rescale, so no
+        // P V of this block reaches O_x before it
         const bool corr = j > 0 && __any_sync(0xffffffffu, raise);
         // p = 2^(s * scale * log2(e) - m): the affine step and the row sum run
         // as packed f32x2 operations, the exponentials on the MUFU unit
@@ -618,15 +627,16 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             pk[c / 2] = pack2(a0, a1, BF16);
             pk[c / 2 + 1] = pack2(b0, b1, BF16);
           }
-          if (c == 60) {
-            // the first 64 keys' P leaves for TMEM halfway, and the MMA thread
-            // may start on it
-            if constexpr (FP8) tmem_st16(ts, &pk[0]);
-            else tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-            if (!corr) {
+          if ((c + 4) % KP == 0) {
+            // a part's P leaves for TMEM as soon as it is complete; but for the
+            // last, the MMA thread may start on it
+            const int part = c / KP;
+            if constexpr (PCOLS == 16) tmem_st16(ts + part * 16, &pk[part * 16]);
+            else tmem_st32(ts + part * 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[part * 32]));
+            if (!corr && part < NP - 1) {
               tmem_st_wait();
               tc_fence_before();
-              mbar_arrive(&bars->p_half[x]);
+              mbar_arrive(&bars->p_part[x][part]);
             }
           }
         }
@@ -635,8 +645,6 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         f2_unpack(acc1, sum2, sum3);
         l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
         m = m_new;
-        if constexpr (FP8) tmem_st16(ts + 16, &pk[16]);
-        else tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         // the stores read their source registers asynchronously: completing
         // them here frees those registers for the (rare) correction below
         tmem_st_wait();
@@ -654,7 +662,8 @@ attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           }
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(&bars->p_half[x]);
+#pragma unroll
+          for (int q = 0; q < NP - 1; ++q) mbar_arrive(&bars->p_part[x][q]);
         }
         tc_fence_before();
         mbar_arrive(&bars->p_full[x]);
